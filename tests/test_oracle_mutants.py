@@ -1,0 +1,55 @@
+"""The oracle pins must catch plausible mistakes.
+
+Each case plants one mistake in a copy of the oracle's C source (on the CPU,
+in a temporary directory) and runs the pin suite against that copy: the suite
+has to fail. The real oracle is never modified.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTANTS = {
+    "unbiased_variance": ("var /= d;", "var /= (d - 1);"),
+    "no_mean_subtraction": ("z[i] = (H(x, i) - mean) * inv", "z[i] = H(x, i) * inv"),
+    "dropped_b1": ("double a = HOPT(b1, j, 0.0);", "double a = 0.0;"),
+    "no_relu": ("if (a < 0.0) a = 0.0;", ""),
+    "fc2_wrong_index": ("fc2T + (size_t)j * d;", "fc2T + (size_t)t * d;"),
+    "dropped_new_token": ("for (int c = 0; c < dh; ++c) Hout[c] += sc[cnt] * vnew[c];", ""),
+    "dropped_scale": ("sc[t] = s * scale;", "sc[t] = s;"),
+    "gqa_interleaved": ("int j = u * G + g;", "int j = g * D->hkv + u;"),
+    "wo_transposed": ("WoT + ((size_t)j * D->dh + c) * D->d", "WoT + ((size_t)c * D->h + j) * D->d"),
+    "pool_unnormalised": ("pooled[(size_t)u * n + p] += sc[p] / Z;", "pooled[(size_t)u * n + p] += sc[p];"),
+    "pool_not_causal": ("int pt = n - W + t;", "int pt = n - 1;"),
+    "relu_always": ("u[j] = (relu && acc < 0.0) ? 0.0 : acc;", "u[j] = (acc < 0.0) ? 0.0 : acc;"),
+    "ties_to_higher": ("return (x->i < y->i) ? -1 : (x->i > y->i);",
+                       "return (x->i > y->i) ? -1 : (x->i < y->i);"),
+    "window_off_by_one": ("if (p < n_sinks || p >= n - W) {", "if (p < n_sinks || p > n - W) {"),
+    "round_half_away": ("double r = nearbyint(a / q);", "double r = round(a / q);"),
+    "v_new_unrounded": ("vd[c] = or_h2d(vnew16[(size_t)u * dh + c]);", ""),
+    "predictor_transposed_p2": ("const uint16_t* row = P2 + (size_t)n * r;\n    for (int j = 0; j < r; ++j) acc += H(row, j) * u[j];",
+                                "for (int j = 0; j < r; ++j) acc += H(P2, (size_t)j * N + n) * u[j];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(os.path.join(ROOT, "oracle", "dv_oracle.c")).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    shutil.copytree(os.path.join(ROOT, "oracle"), tmp_path / "oracle",
+                    ignore=shutil.ignore_patterns("*.so", "__pycache__"))
+    (tmp_path / "oracle" / "dv_oracle.c").write_text(src.replace(old, new))
+    os.makedirs(tmp_path / "tests")
+    for f in ("conftest.py", "test_oracle_pins.py"):
+        shutil.copy(os.path.join(ROOT, "tests", f), tmp_path / "tests" / f)
+    shutil.copytree(os.path.join(ROOT, "tests", "golden"), tmp_path / "tests" / "golden")
+    env = dict(os.environ, PYTHONPATH=str(tmp_path))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        "tests/test_oracle_pins.py"], cwd=tmp_path, env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
