@@ -1,0 +1,464 @@
+#!/usr/bin/env python
+"""Decode-step benchmark: µs per layer at batch 1 and HBM GB/s over the
+selected bytes, for the Deja Vu contextual-sparsity hot path on GB300.
+
+One step = one decode token through all L stacked layers (predictor look-ahead
+on a side stream, top-k, head-sparse attention with split-K, gather-fused
+sparse MLP), captured once in a CUDA graph and replayed. Weights are seeded
+random draws of the workload's shapes (no trained checkpoints); every step
+reads far more than the 129 MB L2 (inputs larger than L2, no flush needed).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). Multi-GPU: replicas only -- every rank decodes
+its own copy of the workload on its own GPU; no data-path collective.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from contextual_sparsity_gb300 import build as dvbuild  # noqa: E402
+from contextual_sparsity_gb300 import dv, synth, traffic  # noqa: E402
+
+METRIC = "decode µs/layer at batch 1 and HBM GB/s over selected bytes vs 8 TB/s peak"
+UNIT = "µs/layer"
+NOMINAL_HBM = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="opt-175b", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--keep-n", type=float, default=None)
+    ap.add_argument("--keep-h", type=float, default=None)
+    ap.add_argument("--layers", type=int, default=None)
+    ap.add_argument("--n", type=int, default=None, help="cached tokens")
+    ap.add_argument("--sync", action="store_true", help="no look-ahead (predict each layer first)")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--tuning", default=None, help="main,side,main_ring_kb,side_ring_kb,attn")
+    return ap.parse_args()
+
+
+def workload(a):
+    over = {}
+    if a.keep_n is not None:
+        over["keep_N"] = a.keep_n
+    if a.keep_h is not None:
+        over["keep_H"] = a.keep_h
+    if a.layers is not None:
+        over["layers"] = a.layers
+    if a.n is not None:
+        over["n"] = a.n
+    return synth.workload(a.workload, **over)
+
+
+def workload_name(w, lookahead=True):
+    return (f"{w.name} (d {w.d}, {w.h}/{w.h_kv} heads x {w.dh}, FFN {w.F}, rank {w.r}, "
+            f"{w.layers} layers, n {w.n}), neuron keep {w.keep_N:g}, head keep {w.keep_H:g}, "
+            f"batch {w.B}, {'look-ahead' if lookahead else 'sync'} prediction")
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as tdist
+        tdist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch.distributed as tdist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.lines = []
+        self.proc = None
+
+    def _gpu_id(self):
+        try:
+            u = str(torch.cuda.get_device_properties(self.dev).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            return vis.split(",")[self.dev] if vis else str(self.dev)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms",
+                 "100", "-i", self._gpu_id()], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the workload on the GPU
+# ---------------------------------------------------------------------------
+class Model:
+    def __init__(self, w, device, lookahead=True, seed=0):
+        self.w = w
+        self.L = w.layers
+        self.n = w.n
+        self.n_max = w.n + 8
+        self.D = dv.dims(w.d, w.h, w.h_kv, w.dh, w.F, w.r, self.n_max)
+        self.keep = dv.Keep(w.keep_N, w.keep_H, 1.0)
+        self.kN = traffic.k_of(w.keep_N, w.F)
+        self.kH = traffic.k_of(w.keep_H, w.h_kv)
+        self.W = [synth.layer_weights(w, l, seed=seed, device=device) for l in range(self.L)]
+        self.K, self.V = [], []
+        for l in range(self.L):
+            k, v = synth.kv_cache(w, l, self.n_max, seed=seed, device=device)
+            self.K.append(k)
+            self.V.append(v)
+        self.kvs = [dv.kv_cache(self.K[l], self.V[l]) for l in range(self.L)]
+        self.sets = [dv.sets(w.B, w.F, w.h_kv, self.kN, self.kH, device=device) for _ in range(2)]
+        self.ws = dv.workspace(self.D, w.B)
+        self.x = synth.hidden(w, seed=seed, device=device)
+        self.y_tmp = torch.empty(2, w.B, w.d, dtype=torch.float16, device=device)
+        self.y_out = torch.empty(w.B, w.d, dtype=torch.float16, device=device)
+        self.side = torch.cuda.Stream(device=device)
+        self.evf = torch.cuda.Event()
+        self.evj = torch.cuda.Event()
+        self.st = torch.zeros(1, dtype=torch.int32, device=device)
+        flags = dv.DV_LOOKAHEAD if lookahead else 0
+        self.step = dv.Step(self.D, self.keep, self.W, self.kvs, [s for s, _ in self.sets],
+                            self.ws, flags, self.side, self.evf, self.evj, dev_status=self.st)
+
+    def capture(self, stream, profiler=None):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            self.step(self.x, self.y_tmp, self.y_out, self.n, stream=stream)  # warm, outside capture
+            torch.cuda.synchronize()
+            n0 = dv.launch_count()
+            if profiler:
+                profiler.start()
+            with torch.cuda.graph(g, stream=stream):
+                self.step(self.x, self.y_tmp, self.y_out, self.n, stream=stream)
+            if profiler:
+                profiler.stop()
+            per_step = dv.launch_count() - n0
+        return g, per_step
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host (CPU baseline / reference arm)
+# ---------------------------------------------------------------------------
+def oracle_layer_seconds(w, budget_s, W=None, K=None, V=None, x=None, seed=0):
+    """Time the fp64 oracle on one layer of the workload (predictor, top-k and
+    the sparse layer in gather form), repeated until budget_s is spent."""
+    import numpy as np
+
+    import oracle
+
+    oracle.build()
+    if W is None:
+        W = synth.layer_weights(w, 0, seed=seed)
+        K, V = synth.kv_cache(w, 0, w.n + 1, seed=seed)
+        x = synth.hidden(w, seed=seed)
+    h = lambda t: t.detach().cpu().contiguous().numpy()
+    Wh = {k: h(v) for k, v in W.items()}
+    Kh, Vh, xh = h(K[0]), h(V[0]), h(x[0])
+    kN, kH = traffic.k_of(w.keep_N, w.F), traffic.k_of(w.keep_H, w.h_kv)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        s = oracle.predict(xh, Wh["P1"], Wh["P2"])
+        selN = oracle.topk(s[: w.F], kN) if kN < w.F else np.arange(w.F)
+        selH = oracle.topk(s[w.F:], kH) if kH < w.h_kv else np.arange(w.h_kv)
+        oracle.layer(xh, Wh, Kh, Vh, w.n, selH, selN)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return el / reps, reps
+
+
+def run_reference(a):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = workload(a)
+    W = synth.layer_weights(w, 0)
+    K, V = synth.kv_cache(w, 0, w.n + 1)
+    x = synth.hidden(w)
+    if a.warmup:
+        oracle_layer_seconds(w, 0.0, W, K, V, x)
+    steps = max(1, min(a.steps, 3))
+    tot, reps = 0.0, 0
+    for _ in range(steps):
+        s, r = oracle_layer_seconds(w, a.cpu_seconds / steps, W, K, V, x)
+        tot += s
+        reps += r
+    val = tot / steps * 1e6
+    sample = (f"{reps} single-layer samples of {w.name} (predictor, top-k, sparse attention and "
+              f"MLP in gather form), fp64 C oracle, one thread")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(val, 2), "unit": UNIT,
+        "n_gpus": a.gpus, "steps": steps, "warmup": a.warmup,
+        "ms_per_step": round(val * w.layers / 1e3, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(w), "batch": w.B},
+        "cpu_baseline": {"value": round(val, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample, "host_cpus": os.cpu_count()},
+        "e2e": {"value": round(val, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def traffic_record(kernel):
+    """ncu DRAM bytes per launch of `kernel`, if the capture in profiles/ was
+    taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+    except Exception:
+        return None
+    rec = j.get(kernel)
+    if not rec:
+        return None
+    return rec["bytes_per_launch"] if rec.get("source_sha") == source_sha() else None
+
+
+def source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "contextual_sparsity_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def run_ours(a):
+    wsz, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dvbuild.build()
+    dv.lib()
+    if a.tuning:
+        dv.set_tuning(*[int(x) for x in a.tuning.split(",")])
+    w = workload(a)
+    lookahead = not a.sync
+    m = Model(w, dev, lookahead=lookahead)
+    stream = torch.cuda.Stream(device=dev)
+    g, per_step = m.capture(stream)
+    torch.cuda.synchronize()
+
+    for _ in range(max(3, a.warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(wsz)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(a.steps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(wsz)
+    ms_total = max_over_ranks(e0.elapsed_time(e1), wsz)
+    ms_step = ms_total / a.steps
+    us_layer = ms_step * 1e3 / w.layers
+    assert m.st.item() == 0, f"device status {m.st.item()}"
+
+    sel, pred = traffic.layer_bytes(w)
+    gbs_sel = sel / (us_layer * 1e-6) / 1e9
+    gbs_all = (sel + pred) / (us_layer * 1e-6) / 1e9
+
+    # Per-kernel durations: a second graph of the same step with every launch
+    # bracketed by CUDA events on its own stream, replayed after warm-up.
+    prof = dv.Profiler(cap=8 * per_step + 64)
+    gp, _ = m.capture(stream, profiler=prof)
+    for _ in range(max(3, a.warmup)):
+        gp.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(20):
+            gp.replay()
+    torch.cuda.synchronize()
+    per_kind = {}
+    for tag, ms in prof.durations_ms():
+        per_kind.setdefault(tag, []).append(ms * 1e3)
+    kernel_us = {k: round(sum(v) / len(v), 2) for k, v in per_kind.items()}
+    kernel_launches = {k: len(v) for k, v in per_kind.items()}
+    G = w.h // w.h_kv
+    algo = {
+        "qkv": traffic.qkv_bytes(w.d, G, w.dh, m.kH),
+        "wo": traffic.wo_bytes(w.d, G, w.dh, m.kH),
+        "mlp": traffic.mlp_bytes(w.d, m.kN),
+        "splitk": traffic.kv_bytes(w.dh, m.kH, w.n + 1),
+    }
+    totals = {k: sum(v) for k, v in per_kind.items()}
+    dom = max(algo, key=lambda k: totals.get(k, 0.0))
+    peak, peak_src = peaks()
+    ach = algo[dom] / (kernel_us[dom] * 1e-6) / 1e9
+    names = {"qkv": "k_stream<KIND_QKV>", "wo": "k_stream<KIND_WO>", "mlp": "k_stream<KIND_MLP>",
+             "splitk": "k_splitk"}
+    roof = {"bound": "hbm", "kernel": names[dom], "achieved": round(ach, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(ach / peak, 4), "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": algo[dom], "avg_launch_us": kernel_us[dom],
+            "traffic": traffic_record(names[dom])}
+
+    # End to end through the public API: pinned host input -> device, one
+    # dv_decode_step call (eager, all layers), device -> pinned host output.
+    e2e = None
+    if not a.no_e2e:
+        hin = torch.empty(w.B, w.d, dtype=torch.float16).pin_memory()
+        hin.copy_(m.x.cpu())
+        hout = torch.empty(w.B, w.d, dtype=torch.float16).pin_memory()
+        xin = torch.empty_like(m.x)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                xin.copy_(hin, non_blocking=True)
+                m.step(xin, m.y_tmp, m.y_out, m.n, stream=stream)
+                hout.copy_(m.y_out, non_blocking=True)
+            stream.synchronize()
+            barrier(wsz)
+            t0 = time.perf_counter()
+            for _ in range(a.e2e_steps):
+                xin.copy_(hin, non_blocking=True)
+                m.step(xin, m.y_tmp, m.y_out, m.n, stream=stream)
+                hout.copy_(m.y_out, non_blocking=True)
+                stream.synchronize()
+            el = time.perf_counter() - t0
+        el = max_over_ranks(el, wsz)
+        e2e = {"value": round(el / a.e2e_steps * 1e6 / w.layers, 2), "unit": UNIT,
+               "h2d_bytes_per_step": hin.numel() * 2, "d2h_bytes_per_step": hout.numel() * 2,
+               "steps": a.e2e_steps, "api": "dv_decode_step (eager C-ABI call per step)"}
+
+    cpu = None
+    if rank == 0 and wsz == 1 and not a.no_cpu_baseline:
+        W0 = {k: v for k, v in m.W[0].items()}
+        sec, reps = oracle_layer_seconds(w, a.cpu_seconds, W0, m.K[0], m.V[0], m.x)
+        cpu = {"value": round(sec * 1e6, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{reps} repeats of one {w.name} layer (predictor, top-k, sparse "
+                         f"attention and MLP in gather form), fp64 C oracle, one thread",
+               "host_cpus": os.cpu_count()}
+
+    if rank != 0:
+        return
+    out = {
+        "metric": METRIC, "value": round(us_layer, 2), "unit": UNIT, "n_gpus": wsz,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "accumulate": "f32", "data": "synthetic (seeded random weights of the workload's shapes)",
+        "config": {"workload": workload_name(w, lookahead), "layers": w.layers, "batch": w.B,
+                   "n_cached": w.n, "keep_neuron": w.keep_N, "keep_head": w.keep_H,
+                   "parallelism": "replicas" if wsz > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (every step streams ~"
+                         f"{(sel + pred) * w.layers / 1e9:.1f} GB)"},
+        "selected_bytes_per_layer": sel, "predictor_bytes_per_layer": pred,
+        "gbs_selected": round(gbs_sel, 1), "frac_of_8tbs_selected": round(gbs_sel / NOMINAL_HBM, 4),
+        "gbs_all_traffic": round(gbs_all, 1),
+        "frac_of_measured_hbm_selected": round(gbs_sel / peak, 4),
+        "layers_per_s_total": round(wsz * w.layers * a.steps / (ms_total * 1e-3), 1),
+        "roofline": roof, "kernel_us": kernel_us, "kernel_launches_per_step": kernel_launches,
+        "gpu_launches": per_step * a.steps, "launches_per_step": per_step,
+        "clocks": clk.summary(), "e2e": e2e, "cpu_baseline": cpu,
+    }
+    print(json.dumps(out))
+
+
+def main():
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)
+
+
+if __name__ == "__main__":
+    main()

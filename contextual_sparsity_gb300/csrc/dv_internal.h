@@ -1,0 +1,81 @@
+// dv_internal.h -- launchers shared between the libdv translation units.
+#pragma once
+
+#include <algorithm>
+#include <cstddef>
+#include <cstdint>
+
+#include "dv_common.cuh"
+
+namespace dv {
+
+// k_stream.cu ---------------------------------------------------------------
+int launch_mlp(const uint16_t* x, int B, int d, int F, const uint16_t* ln_g, const uint16_t* ln_b,
+               float eps, const uint16_t* fc1, const uint16_t* b1, const uint16_t* fc2T,
+               const uint16_t* b2, const int32_t* idx, int k, const int32_t* dev_count, int flags,
+               uint16_t* out, int* st, float* part, int target_ctas, int ring_budget,
+               cudaStream_t stream);
+
+int launch_qkv(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const uint16_t* ln_g,
+               const uint16_t* ln_b, float eps, const uint16_t* Wq, const uint16_t* bq,
+               const uint16_t* Wk, const uint16_t* bk, const uint16_t* Wv, const uint16_t* bv,
+               const int32_t* idx, int k, const int32_t* dev_count, float scale, float* qbuf,
+               uint16_t* K, uint16_t* V, int n, int n_max, uint16_t* Kr, uint16_t* Vr,
+               const int32_t* kept_count, int b_max, uint16_t* y_side, uint32_t* kv_missing,
+               int* st, int target_ctas, int ring_budget, cudaStream_t stream);
+
+int launch_wo(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const uint16_t* WoT,
+              const uint16_t* bo, const int32_t* idx, int k, const int32_t* dev_count,
+              const float* sk_part, int S, uint16_t* out, int* st, float* part, int target_ctas,
+              int ring_budget, cudaStream_t stream);
+
+int launch_predict(const uint16_t* y, int B, int d, const uint16_t* P1, int r,
+                   const uint16_t* P2, int N, int relu, float* scores, int ld, float* u,
+                   int target_ctas, int ring_budget, cudaStream_t stream);
+
+size_t stream_part_bytes(int d, int B, long long max_rows, int target_ctas);
+
+// k_attn.cu ------------------------------------------------------------------
+struct SplitPlan {
+  int C;  // keys per split
+  int S;  // splits
+};
+SplitPlan split_plan(int max_keys, int units, int B, int target_ctas);
+
+int launch_splitk(const float* q, int B, int dh, int G, int h_kv, const int32_t* idx, int k,
+                  const int32_t* dev_count, const uint16_t* K, const uint16_t* V, int n, int n_max,
+                  const uint16_t* Kr, const uint16_t* Vr, const int32_t* kept_count, int b_max,
+                  int retained, SplitPlan plan, float* part, int* st, cudaStream_t stream);
+
+int launch_combine(const float* part, int B, int units, int G, int dh, int S, float* H,
+                   cudaStream_t stream);
+
+int launch_kv_select(const uint16_t* q_obs, int h, int h_kv, int dh, int W, const uint16_t* K,
+                     const uint16_t* V, int n, int n_max, float scale, int n_sinks, int smooth,
+                     int b, uint16_t* Kr, uint16_t* Vr, int32_t* kept_pos, int32_t* kept_count,
+                     int b_max, float* sel_scores, float* ws_f, size_t ws_floats, int* st,
+                     cudaStream_t stream);
+
+size_t kv_select_ws_floats(int h, int h_kv, int W, int n);
+
+int launch_kv_append(const uint16_t* K, const uint16_t* V, int h_kv, int dh, int n, int n_max,
+                     uint16_t* Kr, uint16_t* Vr, const int32_t* kept_count, int b_max,
+                     cudaStream_t stream);
+
+int launch_kv_advance(int32_t* kept_count, int h_kv, int b_max, cudaStream_t stream);
+
+// k_select.cu ----------------------------------------------------------------
+int launch_topk(const float* scores, int B, int ld, int N, const int* k_per_row, int k,
+                int32_t* idx, int ld_idx, int* st, cudaStream_t stream);
+
+int launch_union(const int32_t* idx, int B, int k, int N, int32_t* out, int32_t* count,
+                 cudaStream_t stream);
+
+// Device properties (cached).
+int sm_count();
+
+// Launch accounting: call with phase 0 just before a kernel launch and phase 1
+// just after it (see dv_profile / dv_launch_count).
+void note_launch(int tag, int phase, cudaStream_t s);
+
+}  // namespace dv

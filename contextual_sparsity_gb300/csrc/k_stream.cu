@@ -1,0 +1,793 @@
+// k_stream.cu -- weight-streaming kernels of the decode step (sm_103a).
+//
+// One engine serves every weight-bound step: a CTA owns a contiguous slice of
+// the selected rows of a matrix whose rows are contiguous in memory (fc1 and
+// fc2^T rows are neurons, Wq/Wk/Wv and Wo^T rows are head dims, P1 rows are
+// predictor units; "Deja Vu", §4.4 / App. D: W2 and W^O stored transposed so
+// that a selected neuron or head is one contiguous read). One elected thread
+// of a producer warp streams those rows into a ring of shared-memory stages
+// with 1-D TMA bulk copies (cp.async.bulk + mbarrier complete_tx, L2
+// evict-first); the consumer warps spread every row across the whole CTA, so
+// each thread keeps its columns of the activation vector in registers:
+//   dot phase   value[row] = z . W[row]           (fc1, QKV, P1)
+//   axpy phase  acc       += coef[row] * W[row]   (fc2^T, Wo^T)
+// The fused MLP runs both phases in one CTA: the producer keeps streaming fc2^T
+// rows while the consumers reduce the fc1 dots, so the pipeline never drains
+// between the two ("Deja Vu", §4.4 kernel fusion). Cross-CTA sums go through
+// fp32 partials in the workspace and a fixed-order reduce kernel, so results
+// are deterministic.
+#include "dv_internal.h"
+
+namespace dv {
+
+// ---------------------------------------------------------------------------
+// Shared-memory layout of a streaming CTA
+// ---------------------------------------------------------------------------
+struct StreamGeom {
+  int T;             // consumer threads (multiple of 32)
+  int R;             // rows per stage
+  int NS;            // stages
+  uint32_t row_bytes;
+  uint32_t stage_bytes;
+  int CH;            // max rows per CTA
+  int B;
+  // byte offsets
+  uint32_t off_bar, off_red, off_coef, off_ln, off_list, total;
+};
+
+__host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline void stream_layout(StreamGeom& g) {
+  const int nwc = g.T / 32;
+  uint32_t off = g.NS * g.stage_bytes;
+  off = align_up(off, 16);
+  g.off_bar = off;
+  off += (2 * g.NS + 2) * 8;
+  off = align_up(off, 16);
+  g.off_red = off;
+  off += g.CH * g.B * nwc * 4;
+  g.off_coef = off;
+  off += g.B * g.CH * 4;
+  g.off_ln = off;
+  off += g.B * nwc * 2 * 4 + g.B * 2 * 4;
+  g.off_list = off;
+  off += (g.CH + 4) * 4;
+  g.total = align_up(off, 128);
+}
+
+// ---------------------------------------------------------------------------
+// Kernel parameters
+// ---------------------------------------------------------------------------
+enum StreamKind { KIND_MLP = 0, KIND_QKV = 1, KIND_P1 = 2, KIND_WO = 3 };
+
+struct StreamParams {
+  StreamGeom g;
+  int d, B;
+  const uint16_t* x;   // [B][d] input of the block (LN applied for MLP / QKV)
+  const uint16_t* ln_g;
+  const uint16_t* ln_b;
+  float eps;
+  // rows
+  const uint16_t* W0;  // fc1 / Wq / P1 / WoT
+  const uint16_t* W1;  // fc2T / Wk
+  const uint16_t* W2;  // Wv
+  const uint16_t* bias0;  // b1 / bq
+  const uint16_t* bias1;  // bk
+  const uint16_t* bias2;  // bv
+  const int32_t* idx;     // selected rows (neurons or units); NULL = identity
+  int k;                  // number of selected entries (upper bound)
+  const int32_t* dev_count;
+  int n_rows_total;       // rows of the addressed matrix (bounds check)
+  int flags;
+  // QKV
+  int G, dh, h_kv, n, n_max;
+  float scale;
+  float* qbuf;            // [B][k][G][dh]
+  uint16_t *K, *V;        // [B][h_kv][n_max][dh]
+  uint16_t *Kr, *Vr;      // retained [h_kv][b_max][dh]
+  const int32_t* kept_count;
+  int b_max;
+  uint16_t* y_side;
+  uint32_t* kv_missing;
+  // P1
+  float* u_out;           // [B][r]
+  int relu;
+  // WO: split-K partials
+  const float* sk_part;   // [B][k][G][S][dh + 2]
+  int S;
+  // partial outputs
+  float* part;            // [gridDim][B][d]
+  int* st;
+};
+
+// Number of selected entries this launch processes.
+DV_DEV int eff_count(const StreamParams& p) {
+  int k = p.k;
+  if (p.dev_count) {
+    int c = *p.dev_count;
+    k = c < k ? (c < 0 ? 0 : c) : k;
+  }
+  return k;
+}
+
+// Rows streamed per selected entry (1 for neurons / predictor rows; (G+2) dh
+// for a QKV unit; G dh for a Wo unit).
+DV_DEV int rows_per_entry(const StreamParams& p, int kind) {
+  if (kind == KIND_QKV) return (p.G + 2) * p.dh;
+  if (kind == KIND_WO) return p.G * p.dh;
+  return 1;
+}
+
+// Global address of virtual row v of the launch's row list (phase: 0 dot
+// phase, 1 axpy phase). Out-of-range indices are replaced by row 0 and
+// reported; the consumers see coef 0 / discard the value.
+DV_DEV const uint16_t* row_addr(const StreamParams& p, int kind, int phase, int v, bool& bad) {
+  const size_t d = (size_t)p.d;
+  if (kind == KIND_MLP || kind == KIND_P1) {
+    int j = p.idx ? p.idx[v] : v;
+    bad = (j < 0 || j >= p.n_rows_total);
+    if (bad) j = 0;
+    const uint16_t* base = (kind == KIND_MLP && phase == 1) ? p.W1 : p.W0;
+    return base + (size_t)j * d;
+  }
+  const int per = rows_per_entry(p, kind);
+  const int e = v / per, r = v % per;
+  int u = p.idx ? p.idx[e] : e;
+  bad = (u < 0 || u >= p.h_kv);
+  if (bad) u = 0;
+  if (kind == KIND_WO) {  // r = g * dh + c ; query head u*G + g
+    return p.W0 + ((size_t)u * p.G * p.dh + r) * d;
+  }
+  const int qrows = p.G * p.dh;
+  if (r < qrows) return p.W0 + ((size_t)u * qrows + r) * d;
+  if (r < qrows + p.dh) return p.W1 + ((size_t)u * p.dh + (r - qrows)) * d;
+  return p.W2 + ((size_t)u * p.dh + (r - qrows - p.dh)) * d;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+template <int KIND, int B, int V>
+__global__ void __launch_bounds__(B == 1 ? 288 : 416, 1) k_stream(const StreamParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const StreamGeom& g = p.g;
+  const int T = g.T, nwc = T / 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nvec = p.d >> 3;
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + g.off_bar);
+  uint64_t* empty = full + g.NS;
+  uint64_t* act_ready = empty + g.NS;
+  float* red = reinterpret_cast<float*>(smem + g.off_red);
+  float* coef = reinterpret_cast<float*>(smem + g.off_coef);
+  float* lnred = reinterpret_cast<float*>(smem + g.off_ln);
+  int* list = reinterpret_cast<int*>(smem + g.off_list);
+  volatile int* abort_flag = list + g.CH;
+  volatile int* list_count = list + g.CH + 1;
+
+  // This CTA's slice of the selected entries.
+  const int kk = eff_count(p);
+  const int per = rows_per_entry(p, KIND);
+  const long long tot_rows = (long long)kk * per;
+  const int r0 = (int)(tot_rows * blockIdx.x / gridDim.x);
+  const int r1 = (int)(tot_rows * (blockIdx.x + 1) / gridDim.x);
+  const int nrows = r1 - r0;
+  const bool has_dot = (KIND != KIND_WO);
+  const bool has_axpy = (KIND == KIND_MLP || KIND == KIND_WO);
+  const bool skip = (KIND == KIND_MLP) && (p.flags & DV_SKIP_INACTIVE);
+
+  if (tid == 0) {
+    for (int s = 0; s < g.NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], nwc);
+    }
+    mbar_init(act_ready, 1);
+    *abort_flag = 0;
+    *list_count = nrows;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // ======================= producer warp =======================
+  if (warp == nwc) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int it = 0;
+      int bad_any = 0;
+      for (int phase = 0; phase < 2; ++phase) {
+        if (phase == 0 && !has_dot) continue;
+        if (phase == 1 && !has_axpy) continue;
+        int n_this = nrows;
+        if (phase == 1 && skip) {
+          if (!mbar_wait(act_ready, 0)) {
+            *abort_flag = 1;
+            flag(p.st, DV_DEV_TIMEOUT);
+          }
+          n_this = *list_count;
+        }
+        for (int q0 = 0; q0 < n_this && !*abort_flag; q0 += g.R, ++it) {
+          const int cnt = min(g.R, n_this - q0);
+          const int s = it % g.NS;
+          const uint32_t ph = (it / g.NS) & 1;
+          if (it >= g.NS && !mbar_wait(&empty[s], ph ^ 1)) {
+            *abort_flag = 1;
+            flag(p.st, DV_DEV_TIMEOUT);
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], cnt * g.row_bytes);
+          for (int c = 0; c < cnt; ++c) {
+            const int local = (phase == 1 && skip) ? list[q0 + c] : (q0 + c);
+            bool bad;
+            const uint16_t* src = row_addr(p, KIND, phase, r0 + local, bad);
+            bad_any |= bad;
+            bulk_g2s(smem + (size_t)s * g.stage_bytes + (size_t)c * g.row_bytes, src, g.row_bytes,
+                     &full[s], pol);
+          }
+        }
+      }
+      if (bad_any) flag(p.st, DV_DEV_BAD_INDEX);
+      // Drain: every issued copy must land before the CTA exits.
+      for (int j = (it > g.NS ? it - g.NS : 0); j < it; ++j)
+        if (!mbar_wait(&full[j % g.NS], (j / g.NS) & 1)) flag(p.st, DV_DEV_TIMEOUT);
+    }
+    __syncthreads();
+    return;
+  }
+
+  // ======================= consumer warps =======================
+  // Activation columns of this thread: vectors v_m = tid + m T (8 columns each).
+  float z[B][V][8];
+  int it = 0;
+  if (has_dot) {
+    // --- load x, optional LayerNorm ("Deja Vu" App. C.3: blocks read LN(y)).
+    float s1[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      s1[b] = 0.f;
+#pragma unroll
+      for (int m = 0; m < V; ++m) {
+        const int v = tid + m * T;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) z[b][m][e] = 0.f;
+        if (v < nvec && b < p.B) {
+          uint4 xv = *reinterpret_cast<const uint4*>(p.x + (size_t)b * p.d + v * 8);
+          h8_to_f8(xv, z[b][m]);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) s1[b] += z[b][m][e];
+        }
+      }
+    }
+    if (KIND != KIND_P1) {
+      float* mean_inv = lnred + B * nwc * 2;
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        float t = warp_sum(s1[b]);
+        if (lane == 0) lnred[b * nwc + warp] = t;
+      }
+      consumer_sync(T);
+      if (tid < B) {
+        float t = 0.f;
+        for (int w = 0; w < nwc; ++w) t += lnred[tid * nwc + w];
+        mean_inv[tid * 2] = t / p.d;
+      }
+      consumer_sync(T);
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const float mu = mean_inv[b * 2];
+        float s2 = 0.f;
+#pragma unroll
+        for (int m = 0; m < V; ++m) {
+          const int v = tid + m * T;
+          if (v < nvec) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float c = z[b][m][e] - mu;
+              s2 = fmaf(c, c, s2);
+            }
+          }
+        }
+        s2 = warp_sum(s2);
+        if (lane == 0) lnred[B * nwc + b * nwc + warp] = s2;
+      }
+      consumer_sync(T);
+      if (tid < B) {
+        float t = 0.f;
+        for (int w = 0; w < nwc; ++w) t += lnred[B * nwc + tid * nwc + w];
+        mean_inv[tid * 2 + 1] = 1.0f / sqrtf(t / p.d + p.eps);
+      }
+      consumer_sync(T);
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const float mu = mean_inv[b * 2], inv = mean_inv[b * 2 + 1];
+#pragma unroll
+        for (int m = 0; m < V; ++m) {
+          const int v = tid + m * T;
+          if (v < nvec) {
+            float gg[8], bb[8];
+            if (p.ln_g) {
+              h8_to_f8(*reinterpret_cast<const uint4*>(p.ln_g + v * 8), gg);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) gg[e] = 1.f;
+            }
+            if (p.ln_b) {
+              h8_to_f8(*reinterpret_cast<const uint4*>(p.ln_b + v * 8), bb);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) bb[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) z[b][m][e] = (z[b][m][e] - mu) * inv * gg[e] + bb[e];
+          }
+        }
+      }
+    }
+
+    // --- dot phase: red[row][b][warp] = warp's share of z . W[row]
+    for (int q0 = 0; q0 < nrows; q0 += g.R, ++it) {
+      const int cnt = min(g.R, nrows - q0);
+      const int s = it % g.NS;
+      const uint32_t ph = (it / g.NS) & 1;
+      bool ok = !*abort_flag;
+      if (ok && !mbar_wait(&full[s], ph)) {
+        *abort_flag = 1;
+        flag(p.st, DV_DEV_TIMEOUT);
+        ok = false;
+      }
+      if (ok) {
+        for (int c = 0; c < cnt; ++c) {
+          const uint8_t* row = smem + (size_t)s * g.stage_bytes + (size_t)c * g.row_bytes;
+          float acc[B], cmp[B];
+#pragma unroll
+          for (int b = 0; b < B; ++b) acc[b] = cmp[b] = 0.f;
+#pragma unroll
+          for (int m = 0; m < V; ++m) {
+            const int v = tid + m * T;
+            if (v < nvec) {
+              float w[8];
+              h8_to_f8(*reinterpret_cast<const uint4*>(row + v * 16), w);
+#pragma unroll
+              for (int b = 0; b < B; ++b) {
+                float t = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) t = fmaf(z[b][m][e], w[e], t);
+                kahan_add(acc[b], cmp[b], t);
+              }
+            }
+          }
+#pragma unroll
+          for (int b = 0; b < B; ++b) {
+            const float t = warp_sum(acc[b]);
+            if (lane == 0) red[((q0 + c) * B + b) * nwc + warp] = t;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    consumer_sync(T);
+
+    // --- finalize the dot values (fixed-order sum over the warps)
+    for (int i = tid; i < nrows; i += T) {
+      const int v = r0 + i;
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        float val = 0.f;
+        for (int w = 0; w < nwc; ++w) val += red[(i * B + b) * nwc + w];
+        if (KIND == KIND_MLP) {
+          int j = p.idx ? p.idx[v] : v;
+          const bool badj = (j < 0 || j >= p.n_rows_total);
+          float a = val + ((p.bias0 && !badj) ? h2f(p.bias0[j]) : 0.f);
+          a = a > 0.f ? a : 0.f;
+          coef[b * g.CH + i] = (badj || b >= p.B) ? 0.f : a;
+        } else if (KIND == KIND_P1) {
+          if (b < p.B) {
+            float u = val;
+            if (p.relu && u < 0.f) u = 0.f;
+            p.u_out[(size_t)b * p.n_rows_total + v] = u;
+          }
+        } else if (KIND == KIND_QKV) {
+          const int e = v / per, r = v % per;
+          const int u = p.idx ? p.idx[e] : e;
+          if (u < 0 || u >= p.h_kv || b >= p.B) continue;
+          const int qrows = p.G * p.dh;
+          if (r < qrows) {
+            const float bq = p.bias0 ? h2f(p.bias0[u * qrows + r]) : 0.f;
+            p.qbuf[((size_t)b * p.k + e) * qrows + r] = (val + bq) * p.scale;
+          } else {
+            const bool isk = r < qrows + p.dh;
+            const int c = isk ? r - qrows : r - qrows - p.dh;
+            const uint16_t* bb = isk ? p.bias1 : p.bias2;
+            const float bv = bb ? h2f(bb[u * p.dh + c]) : 0.f;
+            const uint16_t hv = f2h(val + bv);
+            uint16_t* cache = isk ? p.K : p.V;
+            cache[(((size_t)b * p.h_kv + u) * p.n_max + p.n) * p.dh + c] = hv;
+            if (p.Kr) {
+              uint16_t* rc = isk ? p.Kr : p.Vr;
+              rc[((size_t)u * p.b_max + p.kept_count[u]) * p.dh + c] = hv;
+            }
+          }
+        }
+      }
+    }
+    if (KIND == KIND_QKV && blockIdx.x == 0) {
+      // Missing-KV bookkeeping ("Deja Vu" §4.2): keep a copy of y for the
+      // units that did not get their k, v at this token.
+      const int words = (p.h_kv + 31) / 32;
+      for (int b = 0; b < p.B; ++b) {
+        if (p.y_side)
+          for (int v = tid; v < nvec; v += T)
+            *reinterpret_cast<uint4*>(p.y_side + ((size_t)b * p.n_max + p.n) * p.d + v * 8) =
+                *reinterpret_cast<const uint4*>(p.x + (size_t)b * p.d + v * 8);
+        if (p.kv_missing)
+          for (int w = tid; w < words; w += T) {
+            uint32_t bits = 0;
+            for (int u = w * 32; u < min(p.h_kv, w * 32 + 32); ++u) bits |= 1u << (u - w * 32);
+            if (p.idx) {
+              for (int e = 0; e < kk; ++e) {
+                const int u = p.idx[e];
+                if (u >= w * 32 && u < w * 32 + 32) bits &= ~(1u << (u - w * 32));
+              }
+            } else {
+              bits = 0;
+            }
+            p.kv_missing[((size_t)b * p.n_max + p.n) * words + w] = bits;
+          }
+      }
+    }
+    if (skip) {
+      consumer_sync(T);
+      if (tid == 0) {
+        int c = 0;
+        for (int i = 0; i < nrows; ++i) {
+          float any = 0.f;
+#pragma unroll
+          for (int b = 0; b < B; ++b) any = fmaxf(any, coef[b * g.CH + i]);
+          if (any > 0.f) list[c++] = i;
+        }
+        *list_count = c;
+        mbar_arrive(act_ready);
+      }
+    }
+    consumer_sync(T);
+  }
+
+  if (has_axpy) {
+    if (KIND == KIND_WO) {
+      // Combine the split-K partials of the heads this CTA touches:
+      // H = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+      const int dh = p.dh;
+      for (int i = tid; i < nrows * B; i += T) {
+        const int li = i % nrows, b = i / nrows;
+        const int v = r0 + li;
+        const int e = v / per, r = v % per;  // r = g dh + c
+        const int gq = r / dh, c = r % dh;
+        float H = 0.f;
+        if (b < p.B) {
+          const float* base = p.sk_part + ((((size_t)b * p.k + e) * p.G + gq) * p.S) * (dh + 2);
+          float M = -INFINITY;
+          for (int s = 0; s < p.S; ++s) M = fmaxf(M, base[(size_t)s * (dh + 2)]);
+          float L = 0.f, O = 0.f;
+          for (int s = 0; s < p.S; ++s) {
+            const float* ps = base + (size_t)s * (dh + 2);
+            const float wgt = (ps[1] > 0.f) ? exp2f(ps[0] - M) : 0.f;
+            L += wgt * ps[1];
+            O += wgt * ps[2 + c];
+          }
+          H = L > 0.f ? O / L : 0.f;
+          const int u = p.idx ? p.idx[e] : e;
+          if (u < 0 || u >= p.h_kv) H = 0.f;
+        }
+        coef[b * g.CH + li] = H;
+      }
+      consumer_sync(T);
+    }
+    const int n_ax = skip ? *list_count : nrows;
+    float acc[B][V][8];
+#pragma unroll
+    for (int b = 0; b < B; ++b)
+#pragma unroll
+      for (int m = 0; m < V; ++m)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[b][m][e] = 0.f;
+    for (int q0 = 0; q0 < n_ax; q0 += g.R, ++it) {
+      const int cnt = min(g.R, n_ax - q0);
+      const int s = it % g.NS;
+      const uint32_t ph = (it / g.NS) & 1;
+      bool ok = !*abort_flag;
+      if (ok && !mbar_wait(&full[s], ph)) {
+        *abort_flag = 1;
+        flag(p.st, DV_DEV_TIMEOUT);
+        ok = false;
+      }
+      if (ok) {
+        for (int c = 0; c < cnt; ++c) {
+          const int li = skip ? list[q0 + c] : (q0 + c);
+          const uint8_t* row = smem + (size_t)s * g.stage_bytes + (size_t)c * g.row_bytes;
+          float a[B];
+#pragma unroll
+          for (int b = 0; b < B; ++b) a[b] = coef[b * g.CH + li];
+#pragma unroll
+          for (int m = 0; m < V; ++m) {
+            const int v = tid + m * T;
+            if (v < nvec) {
+              float w[8];
+              h8_to_f8(*reinterpret_cast<const uint4*>(row + v * 16), w);
+#pragma unroll
+              for (int b = 0; b < B; ++b)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[b][m][e] = fmaf(a[b], w[e], acc[b][m][e]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // Partial output of this CTA.
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      if (b >= p.B) break;
+      float* dst = p.part + ((size_t)blockIdx.x * p.B + b) * p.d;
+#pragma unroll
+      for (int m = 0; m < V; ++m) {
+        const int v = tid + m * T;
+        if (v < nvec) {
+          float4* o = reinterpret_cast<float4*>(dst + v * 8);
+          o[0] = make_float4(acc[b][m][0], acc[b][m][1], acc[b][m][2], acc[b][m][3]);
+          o[1] = make_float4(acc[b][m][4], acc[b][m][5], acc[b][m][6], acc[b][m][7]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Fixed-order reduce of the CTA partials: out = x + bias + sum_g part[g].
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_reduce(const float* __restrict__ part, int G, int B, int d,
+                                                const uint16_t* __restrict__ x,
+                                                const uint16_t* __restrict__ bias,
+                                                uint16_t* __restrict__ out) {
+  const int c4 = blockIdx.x * blockDim.x + threadIdx.x;  // group of 4 columns
+  const int b = blockIdx.y;
+  if (c4 * 4 >= d) return;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float* src = part + (size_t)b * d + c4 * 4;
+  const size_t stride = (size_t)B * d;
+  int gi = 0;
+  for (; gi + 4 <= G; gi += 4) {
+    float4 t0 = *reinterpret_cast<const float4*>(src + (gi + 0) * stride);
+    float4 t1 = *reinterpret_cast<const float4*>(src + (gi + 1) * stride);
+    float4 t2 = *reinterpret_cast<const float4*>(src + (gi + 2) * stride);
+    float4 t3 = *reinterpret_cast<const float4*>(src + (gi + 3) * stride);
+    s.x += t0.x; s.y += t0.y; s.z += t0.z; s.w += t0.w;
+    s.x += t1.x; s.y += t1.y; s.z += t1.z; s.w += t1.w;
+    s.x += t2.x; s.y += t2.y; s.z += t2.z; s.w += t2.w;
+    s.x += t3.x; s.y += t3.y; s.z += t3.z; s.w += t3.w;
+  }
+  for (; gi < G; ++gi) {
+    float4 t = *reinterpret_cast<const float4*>(src + gi * stride);
+    s.x += t.x; s.y += t.y; s.z += t.z; s.w += t.w;
+  }
+  const uint16_t* xr = x ? x + (size_t)b * d + c4 * 4 : nullptr;
+  float r[4] = {s.x, s.y, s.z, s.w};
+  uint16_t o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float bb = bias ? h2f(bias[c4 * 4 + e]) : 0.f;
+    o[e] = f2h((x ? h2f(xr[e]) : 0.f) + (r[e] + bb));
+  }
+  uint2 pk;
+  pk.x = (uint32_t)o[0] | ((uint32_t)o[1] << 16);
+  pk.y = (uint32_t)o[2] | ((uint32_t)o[3] << 16);
+  *reinterpret_cast<uint2*>(out + (size_t)b * d + c4 * 4) = pk;
+}
+
+// ---------------------------------------------------------------------------
+// Predictor second layer: scores[b][i] = sum_j u[b][j] P2[i][j] (rows of r).
+// One warp per row, 16-byte loads, Kahan-compensated per-lane sums.
+// ---------------------------------------------------------------------------
+template <int B>
+__global__ void __launch_bounds__(256) k_pred2(const float* __restrict__ u, int r,
+                                               const uint16_t* __restrict__ P2, int N,
+                                               float* __restrict__ scores, int ld, int nB) {
+  extern __shared__ __align__(16) float us[];  // [B][r]
+  for (int i = threadIdx.x; i < nB * r; i += blockDim.x) us[i] = u[i];
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  const int nv = r >> 3;
+  for (int row = blockIdx.x * nw + warp; row < N; row += gridDim.x * nw) {
+    const uint16_t* pr = P2 + (size_t)row * r;
+    float acc[B], cmp[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b) acc[b] = cmp[b] = 0.f;
+    for (int v = lane; v < nv; v += 32) {
+      float w[8];
+      h8_to_f8(ld_nc_v4(pr + v * 8), w);
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        if (b < nB) {
+          const float* ub = us + b * r + v * 8;
+          float t = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t = fmaf(ub[e], w[e], t);
+          kahan_add(acc[b], cmp[b], t);
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      if (b < nB) {
+        const float t = warp_sum(acc[b] - cmp[b]);
+        if (lane == 0) scores[(size_t)b * ld + row] = t;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+static int pick_V(int nvec, int tmax) { return (nvec + tmax - 1) / tmax; }
+
+static bool make_geom(StreamGeom& g, int d, int B, int ring_budget, int CH) {
+  const int nvec = d / 8;
+  const int tmax = (B == 1) ? 256 : 384;
+  const int V = pick_V(nvec, tmax);
+  g.T = ((nvec + V - 1) / V + 31) / 32 * 32;
+  g.B = B;
+  g.row_bytes = (uint32_t)d * 2;
+  g.R = std::max(1, (int)(16384 / g.row_bytes));
+  g.stage_bytes = g.R * g.row_bytes;
+  g.NS = std::min(16, ring_budget / (int)g.stage_bytes);
+  if (g.NS < 2) g.NS = 2;
+  g.CH = CH;
+  stream_layout(g);
+  return g.total <= 227 * 1024;
+}
+
+template <int KIND, int B>
+static void* stream_kernel_for_V(int V) {
+  switch (V) {
+    case 1: return (void*)k_stream<KIND, B, 1>;
+    case 2: return (void*)k_stream<KIND, B, 2>;
+    case 3: return (void*)k_stream<KIND, B, 3>;
+    case 4: return (void*)k_stream<KIND, B, 4>;
+    case 5: return B == 1 ? (void*)k_stream<KIND, 1, 5> : nullptr;
+    case 6: return B == 1 ? (void*)k_stream<KIND, 1, 6> : nullptr;
+    case 8: return B == 1 ? (void*)k_stream<KIND, 1, 8> : nullptr;
+    default: return nullptr;
+  }
+}
+
+template <int KIND>
+static void* stream_kernel(int B, int V) {
+  if (V == 7) V = 8;
+  return B == 1 ? stream_kernel_for_V<KIND, 1>(V) : stream_kernel_for_V<KIND, 4>(V);
+}
+
+int stream_ctas_max(int CH_rows, long long rows, int target) {
+  long long need = (rows + CH_rows - 1) / CH_rows;
+  long long gsz = std::max<long long>(need, std::min<long long>(target, rows));
+  return (int)std::max<long long>(1, gsz);
+}
+
+static int launch_stream(int kind, StreamParams& p, long long rows, int target_ctas,
+                         int ring_budget, cudaStream_t stream, int* grid_out) {
+  const int Bt = p.B == 1 ? 1 : 4;
+  const int CH = (Bt == 1) ? 512 : 256;
+  if (!make_geom(p.g, p.d, Bt, ring_budget, CH)) return DV_ERR_UNSUPPORTED;
+  const int V = pick_V(p.d / 8, Bt == 1 ? 256 : 384);
+  void* fn = nullptr;
+  switch (kind) {
+    case KIND_MLP: fn = stream_kernel<KIND_MLP>(Bt, V); break;
+    case KIND_QKV: fn = stream_kernel<KIND_QKV>(Bt, V); break;
+    case KIND_P1: fn = stream_kernel<KIND_P1>(Bt, V); break;
+    case KIND_WO: fn = stream_kernel<KIND_WO>(Bt, V); break;
+  }
+  if (!fn) return DV_ERR_UNSUPPORTED;
+  int grid = stream_ctas_max(CH, rows, target_ctas);
+  if (rows == 0) grid = 1;
+  if (grid_out) *grid_out = grid;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, p.g.total) !=
+      cudaSuccess)
+    return DV_ERR_LAUNCH;
+  void* args[] = {&p};
+  static const int tags[4] = {DV_TAG_MLP, DV_TAG_QKV, DV_TAG_PRED1, DV_TAG_WO};
+  note_launch(tags[kind], 0, stream);
+  const cudaError_t e = cudaLaunchKernel(fn, dim3(grid), dim3(p.g.T + 32), args, p.g.total, stream);
+  note_launch(tags[kind], 1, stream);
+  return e == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
+}
+
+int reduce_launch(const float* part, int G, int B, int d, const uint16_t* x, const uint16_t* bias,
+                  uint16_t* out, cudaStream_t stream) {
+  const int groups = d / 4;
+  dim3 grid((groups + 255) / 256, B);
+  note_launch(DV_TAG_REDUCE, 0, stream);
+  k_reduce<<<grid, 256, 0, stream>>>(part, G, B, d, x, bias, out);
+  note_launch(DV_TAG_REDUCE, 1, stream);
+  return cudaGetLastError() == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
+}
+
+// ---- public launchers (declared in dv_internal.h) -------------------------
+
+int launch_mlp(const uint16_t* x, int B, int d, int F, const uint16_t* ln_g, const uint16_t* ln_b,
+               float eps, const uint16_t* fc1, const uint16_t* b1, const uint16_t* fc2T,
+               const uint16_t* b2, const int32_t* idx, int k, const int32_t* dev_count, int flags,
+               uint16_t* out, int* st, float* part, int target_ctas, int ring_budget,
+               cudaStream_t stream) {
+  const uint16_t* resid = (flags & DV_NO_RESIDUAL) ? nullptr : x;
+  StreamParams p{};
+  p.d = d; p.B = B; p.x = x; p.ln_g = ln_g; p.ln_b = ln_b; p.eps = eps;
+  p.W0 = fc1; p.W1 = fc2T; p.bias0 = b1; p.idx = idx; p.k = k; p.dev_count = dev_count;
+  p.n_rows_total = F; p.flags = flags; p.part = part; p.st = st;
+  int grid = 0;
+  int rc = launch_stream(KIND_MLP, p, k, target_ctas, ring_budget, stream, &grid);
+  if (rc != DV_OK) return rc;
+  return reduce_launch(part, grid, B, d, resid, b2, out, stream);
+}
+
+int launch_qkv(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const uint16_t* ln_g,
+               const uint16_t* ln_b, float eps, const uint16_t* Wq, const uint16_t* bq,
+               const uint16_t* Wk, const uint16_t* bk, const uint16_t* Wv, const uint16_t* bv,
+               const int32_t* idx, int k, const int32_t* dev_count, float scale, float* qbuf,
+               uint16_t* K, uint16_t* V, int n, int n_max, uint16_t* Kr, uint16_t* Vr,
+               const int32_t* kept_count, int b_max, uint16_t* y_side, uint32_t* kv_missing,
+               int* st, int target_ctas, int ring_budget, cudaStream_t stream) {
+  StreamParams p{};
+  p.d = d; p.B = B; p.x = x; p.ln_g = ln_g; p.ln_b = ln_b; p.eps = eps;
+  p.W0 = Wq; p.W1 = Wk; p.W2 = Wv; p.bias0 = bq; p.bias1 = bk; p.bias2 = bv;
+  p.idx = idx; p.k = k; p.dev_count = dev_count; p.G = G; p.dh = dh; p.h_kv = h_kv;
+  p.scale = scale; p.qbuf = qbuf; p.K = K; p.V = V; p.n = n; p.n_max = n_max;
+  p.Kr = Kr; p.Vr = Vr; p.kept_count = kept_count; p.b_max = b_max;
+  p.y_side = y_side; p.kv_missing = kv_missing; p.st = st;
+  return launch_stream(KIND_QKV, p, (long long)k * (G + 2) * dh, target_ctas, ring_budget, stream,
+                       nullptr);
+}
+
+int launch_wo(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const uint16_t* WoT,
+              const uint16_t* bo, const int32_t* idx, int k, const int32_t* dev_count,
+              const float* sk_part, int S, uint16_t* out, int* st, float* part, int target_ctas,
+              int ring_budget, cudaStream_t stream) {
+  // x: residual added by the reduce (NULL: none)
+  StreamParams p{};
+  p.d = d; p.B = B; p.x = x; p.W0 = WoT; p.idx = idx; p.k = k; p.dev_count = dev_count;
+  p.G = G; p.dh = dh; p.h_kv = h_kv; p.sk_part = sk_part; p.S = S; p.part = part; p.st = st;
+  int grid = 0;
+  int rc = launch_stream(KIND_WO, p, (long long)k * G * dh, target_ctas, ring_budget, stream,
+                         &grid);
+  if (rc != DV_OK) return rc;
+  return reduce_launch(part, grid, B, d, x, bo, out, stream);
+}
+
+int launch_predict(const uint16_t* y, int B, int d, const uint16_t* P1, int r,
+                   const uint16_t* P2, int N, int relu, float* scores, int ld, float* u,
+                   int target_ctas, int ring_budget, cudaStream_t stream) {
+  StreamParams p{};
+  p.d = d; p.B = B; p.x = y; p.W0 = P1; p.idx = nullptr; p.k = r; p.n_rows_total = r;
+  p.u_out = u; p.relu = relu;
+  int rc = launch_stream(KIND_P1, p, r, target_ctas, ring_budget, stream, nullptr);
+  if (rc != DV_OK) return rc;
+  const int threads = 256, nw = threads / 32;
+  int grid = std::min((N + nw - 1) / nw, std::max(1, target_ctas));
+  const size_t smem = (size_t)B * r * sizeof(float);
+  note_launch(DV_TAG_PRED2, 0, stream);
+  if (B == 1)
+    k_pred2<1><<<grid, threads, smem, stream>>>(u, r, P2, N, scores, ld, B);
+  else
+    k_pred2<4><<<grid, threads, smem, stream>>>(u, r, P2, N, scores, ld, B);
+  note_launch(DV_TAG_PRED2, 1, stream);
+  return cudaGetLastError() == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
+}
+
+size_t stream_part_bytes(int d, int B, long long max_rows, int target_ctas) {
+  const int CH = (B == 1) ? 512 : 256;
+  const int grid = stream_ctas_max(CH, max_rows, target_ctas);
+  return (size_t)grid * B * d * sizeof(float);
+}
+
+}  // namespace dv

@@ -1,0 +1,289 @@
+/*
+ * dv.h -- C ABI of libdv.so: the batch-1 decode-step hot path of Deja Vu
+ * contextual sparsity on one NVIDIA GB300 (sm_103a), composed with
+ * attention-scored KV-token selection.
+ *
+ * Pages this interface follows:
+ *   [DV] "Deja Vu: Contextual Sparsity for Efficient LLMs at Inference Time"
+ *        (arXiv 2310.17157): §2.3 Eq. 1 (sparsified MLP), Eq. 2 (sparsified
+ *        MHA) and the keep budget; §4.1 "Design" and §4.2 "Approach"
+ *        (predictors); §4.3 (look-ahead); §4.4 and App. D (fused gather +
+ *        multiply, W2 and W^O stored transposed); App. C.1 (batch union);
+ *        App. C.3 (residual form of a layer).
+ *   [BX] "Where Activation Sparsity and KV-Cache Sparsity Cross in LLM
+ *        Decoding" (arXiv 2609.33889): §3.2 (branches keep all state),
+ *        §4.1 and App. A (attention-scored KV selection, split-K attention).
+ *
+ * Conventions (every entry point):
+ *  - fp16 data are IEEE binary16 bit patterns (uint16_t). Accumulation is fp32.
+ *  - Every pointer is a DEVICE pointer owned by the caller, 16-byte aligned,
+ *    unless stated otherwise. The library allocates no device memory: scratch
+ *    comes from the caller's workspace `ws` of at least dv_workspace_size()
+ *    bytes (256-byte aligned).
+ *  - Every call only enqueues work on the given stream(s) and returns; it
+ *    never synchronises the host, so a sequence of calls can be captured in
+ *    a CUDA graph.
+ *  - Host-side argument errors return a negative dv_status and launch
+ *    nothing. Data-dependent device errors (an index out of range, a bounded
+ *    wait that gave up, a non-finite score) set bits in the caller's
+ *    `dev_status` word (device int, nullable), which the caller reads after
+ *    synchronising; the offending element is skipped, never dereferenced.
+ *  - Matrices are row-major. Layouts: Wq [h*d_h][d] (row j*d_h+c = dim c of
+ *    query head j), Wk / Wv [h_kv*d_h][d], WoT [h*d_h][d] (W^O transposed:
+ *    row j*d_h+c = the output weights of dim c of head j), fc1 [F][d]
+ *    (neuron j's input weights), fc2T [F][d] (W2 transposed: neuron j's output
+ *    weights), P1 [r][d], P2 [F + h_kv][r] (rows 0..F-1 score neurons, rows
+ *    F.. score attention units). KV cache K, V [B][h_kv][n_max][d_h].
+ *  - An attention "unit" is one KV head with the h/h_kv query heads that read
+ *    it; under MHA (h_kv == h) a unit is one head.
+ */
+#ifndef DV_H
+#define DV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (returned) ---------------------------------------- */
+#define DV_OK 0
+#define DV_ERR_NULL (-1)        /* a required pointer is NULL */
+#define DV_ERR_ALIGN (-2)       /* a pointer is not 16-byte aligned (ws: 256) */
+#define DV_ERR_DIMS (-3)        /* a dimension is out of range or inconsistent */
+#define DV_ERR_KEEP (-4)        /* a keep ratio is outside (0, 1] */
+#define DV_ERR_K (-5)           /* k < 1 or k > N */
+#define DV_ERR_WORKSPACE (-6)   /* ws_bytes < dv_workspace_size(...) */
+#define DV_ERR_LAUNCH (-7)      /* a CUDA launch or stream call failed */
+#define DV_ERR_UNSUPPORTED (-8) /* shape outside what the kernels implement */
+
+/* ---- device status bits (written to *dev_status with atomicOr) --------- */
+#define DV_DEV_BAD_INDEX 1      /* an index list held a value out of range */
+#define DV_DEV_TIMEOUT 2        /* a bounded wait inside a kernel gave up */
+#define DV_DEV_NONFINITE 4      /* a non-finite score reached top-k */
+
+/* ---- flags ------------------------------------------------------------- */
+#define DV_PRED_RELU (1u << 0)     /* ReLU between the two predictor layers */
+#define DV_SKIP_INACTIVE (1u << 1) /* MLP: skip fc2T rows with a_j <= 0 (exact) */
+#define DV_LOOKAHEAD (1u << 2)     /* driver: predict layer l+1 on the side stream */
+#define DV_SYNC_PREDICT (1u << 3)  /* driver: predict this layer's sets from y first */
+#define DV_KV_RESELECT (1u << 4)   /* KV: run the scoring pass, rebuild the retained set */
+#define DV_KV_DENSE (1u << 5)      /* attention reads the full cache */
+#define DV_KV_RETAINED (1u << 6)   /* attention reads the retained KV buffer */
+#define DV_KV_ADVANCE (1u << 7)    /* retained counts grow by one after the step */
+#define DV_JOIN (1u << 8)          /* driver: main waits for the previous side work */
+#define DV_NO_RESIDUAL (1u << 9)   /* MLP / attention block: out = block output, without
+                                      the residual x (the parallel form of [DV] App. C.3,
+                                      y + MHA(y) + MLP(y), sums block outputs) */
+
+/* ---- shapes ------------------------------------------------------------ */
+typedef struct {
+  int d;        /* model dim; multiple of 8, 8 <= d <= 16384 */
+  int h;        /* query heads */
+  int h_kv;     /* KV heads; h % h_kv == 0 (h_kv == h: MHA) */
+  int d_h;      /* head dim: 64 or 128; h * d_h need not equal d */
+  int F;        /* FFN width (neurons), >= 1 */
+  int r;        /* predictor rank; multiple of 8, <= 4096 */
+  int n_max;    /* KV cache capacity per KV head, tokens */
+  float ln_eps; /* LayerNorm epsilon (1e-5 for OPT) */
+} dv_dims;
+
+/* Keep ratios ([DV] §2.3: |S| <= (1 - sparsity) N, so k = max(1, floor(keep N))).
+ * keep == 1 skips prediction and selection for that segment (all selected). */
+typedef struct {
+  float neuron; /* MLP neurons */
+  float head;   /* attention units */
+  float kv;     /* KV tokens ([BX] App. A budget b = floor(n kv) per KV head) */
+} dv_keep;
+
+/* One layer's weights. Bias and LayerNorm pointers are nullable (0 bias,
+ * gain 1, shift 0). P1 / P2 are this layer's predictor. */
+typedef struct {
+  const uint16_t *ln1_g, *ln1_b; /* [d] */
+  const uint16_t *Wq, *bq;       /* [h*d_h][d], [h*d_h] */
+  const uint16_t *Wk, *bk;       /* [h_kv*d_h][d], [h_kv*d_h] */
+  const uint16_t *Wv, *bv;       /* [h_kv*d_h][d], [h_kv*d_h] */
+  const uint16_t *WoT, *bo;      /* [h*d_h][d], [d] */
+  const uint16_t *ln2_g, *ln2_b; /* [d] */
+  const uint16_t *fc1, *b1;      /* [F][d], [F] */
+  const uint16_t *fc2T, *b2;     /* [F][d], [d] */
+  const uint16_t *P1, *P2;       /* [r][d], [F + h_kv][r] */
+} dv_layer_weights;
+
+/* One layer's KV state ([BX] §3.2: the full cache stays allocated and keeps
+ * receiving entries; the retained buffer is read instead of it). */
+typedef struct {
+  uint16_t *K, *V;      /* [B][h_kv][n_max][d_h]; slot n receives the new token */
+  uint16_t *y_side;     /* [B][n_max][d] nullable: copy of y per token ([DV] §4.2) */
+  uint32_t *kv_missing; /* [B][n_max][(h_kv+31)/32] nullable: bit u set = unit u's
+                           k, v were not computed for that token ([DV] §4.2) */
+  uint16_t *Kr, *Vr;    /* [h_kv][b_max][d_h] nullable: retained KV (batch 1) */
+  int32_t *kept_pos;    /* [h_kv][b_max]: cache position of each retained row */
+  int32_t *kept_count;  /* [h_kv] device: retained rows before the new token */
+  int b_max;            /* retained capacity per KV head */
+} dv_kv_cache;
+
+/* Index sets of one layer. Per-row sets are ascending. */
+typedef struct {
+  int32_t *idx_N; /* [B][k_N] neuron sets */
+  int32_t *idx_H; /* [B][k_H] attention-unit sets */
+  int32_t *uN;    /* [F] union of the B neuron sets (B > 1), ascending */
+  int32_t *uH;    /* [h_kv] union of the B unit sets (B > 1), ascending */
+  int32_t *ucnt;  /* [2] device: |uN|, |uH| */
+  float *scores;  /* [B][F + h_kv] predictor scores */
+} dv_sets;
+
+/* ---- aux ----------------------------------------------------------------- */
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int dv_version(void);
+
+/* Human-readable text of a dv_status code; never NULL. */
+const char* dv_status_string(int status);
+
+/* Workspace bytes any entry point below needs for these shapes at batch B,
+ * with n_max from dims (split-K partials and KV scoring buffers scale with
+ * it). One workspace of this size serves every entry point and the driver. */
+size_t dv_workspace_size(const dv_dims* dims, int B, int flags);
+
+/* Launch-shape tuning (aux, process-wide; the defaults need no call): CTAs of
+ * the weight-streaming kernels (0: one per SM), CTAs of the side-stream
+ * predictor (>= 1), shared-memory ring budgets in KB (main 16..200, side
+ * 8..200), split-K CTA target (0: four per SM). DV_OK or DV_ERR_DIMS. */
+int dv_set_tuning(int main_ctas, int side_ctas, int main_ring_kb, int side_ring_kb,
+                  int attn_ctas);
+
+/* Kernel-launch accounting (aux). dv_profile(events, tags, cap): from now on
+ * every kernel launch of the library is bracketed by two cudaEventRecord calls
+ * on its stream, using events[2i] (before) and events[2i+1] (after) of the
+ * caller's timing-enabled events, and tags[i] receives the kernel kind
+ * (DV_TAG_*), until cap pairs are used; works inside stream capture (the
+ * records become graph nodes). dv_profile(NULL, NULL, 0) stops and returns the
+ * number of pairs recorded. dv_launch_count() is the number of kernels this
+ * process has launched through the library (captured launches count once). */
+#define DV_TAG_QKV 0
+#define DV_TAG_SPLITK 1
+#define DV_TAG_WO 2
+#define DV_TAG_REDUCE 3
+#define DV_TAG_MLP 4
+#define DV_TAG_PRED1 5
+#define DV_TAG_PRED2 6
+#define DV_TAG_TOPK 7
+#define DV_TAG_UNION 8
+#define DV_TAG_COMBINE 9
+#define DV_TAG_KVSEL 10
+#define DV_TAG_KVAPPEND 11
+#define DV_TAG_KVADVANCE 12
+int dv_profile(cudaEvent_t* events, int* tags, int cap);
+long long dv_launch_count(void);
+
+/* ---- a2: predictor ([DV] §4.1 "Design", §4.2 "Approach") ------------------
+ * scores[b][i] = sum_j act(sum_c y[b][c] P1[j][c]) * P2[i][j] for i < N,
+ * act = identity, or ReLU with DV_PRED_RELU. y [B][d] fp16 is the layer input
+ * y_l ([DV] §4.3); P2 points at the first row to score (e.g. P2 + F*r for the
+ * head rows only). scores [B][N] fp32. B <= 4. ws holds the rank-r vector. */
+int dv_predict(const uint16_t* y, int B, int d, const uint16_t* P1, int r, const uint16_t* P2,
+               int N, int flags, float* scores, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---- a3: top-k selection ([DV] §2.3 budget, §4.1; App. C.1 union) ---------
+ * For each row b < B: the k largest of scores[b*ld + 0 .. b*ld + N-1]; equal
+ * scores go to the lower index, -0 equals +0; idx[b][0..k-1] ascending.
+ * If union_idx != NULL: the ascending union of the B sets is written to
+ * union_idx[0..c-1] and c to *union_count (device int). A NaN score sets
+ * DV_DEV_NONFINITE. B <= 8, N <= 1 << 24. No workspace is needed. */
+int dv_select_topk(const float* scores, int B, int ld, int N, int k, int32_t* idx,
+                   int32_t* union_idx, int32_t* union_count, int* dev_status, void* ws,
+                   size_t ws_bytes, cudaStream_t stream);
+
+/* ---- a4: gather-fused sparse MLP ([DV] §2.3 Eq. 1, §4.4, App. D) ----------
+ * out[b] = x[b] + sum_{j in S} relu(LN2(x[b]) . fc1[j] + b1[j]) fc2T[j] + b2,
+ * S = idx[0..k-1] (shared by the B rows: for B > 1 pass the union), or, if
+ * dev_count != NULL, idx[0..*dev_count-1] with *dev_count <= k read on the
+ * device; idx == NULL means all F neurons (dense). Indices must be distinct
+ * and in [0, F); one out of range is skipped and sets DV_DEV_BAD_INDEX.
+ * x, out [B][d] fp16 (may not alias). B <= 4.
+ * flags: DV_SKIP_INACTIVE, DV_NO_RESIDUAL (out = MLP(x) only). */
+int dv_sparse_mlp(const uint16_t* x, int B, const dv_dims* dims, const dv_layer_weights* w,
+                  const int32_t* idx, int k, const int32_t* dev_count, int flags, uint16_t* out,
+                  int* dev_status, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---- a5-a7: head-sparse attention block ([DV] §2.3 Eq. 2, §4.2, §4.4) ------
+ * For each selected unit u in head_idx[0..k_heads-1] (or *dev_count of them;
+ * head_idx == NULL: all h_kv units): project z = LN1(x[b]) to q (every query
+ * head of u, scaled by softmax_scale), k and v of u (+ biases); write k, v as
+ * fp16 to K/V[b][u][n]; attend over cache positions 0..n (n cached tokens
+ * plus the new one) with split-K flash-decoding and a separate combine; then
+ * out[b] = x[b] + sum_{query heads j of selected units} H_j WoT_j + bo.
+ * Unselected units get no k, v at slot n: their kv_missing bit is set and
+ * y_side[b][n] = x[b] (when those pointers are given).
+ * With DV_KV_RETAINED (batch 1): the new k, v also go to Kr/Vr[u][kept_count[u]]
+ * and attention reads Kr/Vr[u][0..kept_count[u]] instead of the cache; with
+ * DV_KV_ADVANCE the kept counts then grow by one.
+ * 0 <= n < n_max. x, out [B][d]. B <= 4. DV_NO_RESIDUAL: out = MHA(x) only. */
+int dv_sparse_attn(const uint16_t* x, int B, const dv_dims* dims, const dv_layer_weights* w,
+                   const int32_t* head_idx, int k_heads, const int32_t* dev_count,
+                   dv_kv_cache* kv, int n, float softmax_scale, int flags, uint16_t* out,
+                   int* dev_status, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---- a8-a9: attention-scored KV selection + split-K attention --------------
+ * ([BX] §4.1, App. A.) Batch 1. q [h][d_h] fp32: the new token's queries,
+ * already projected and scaled; the new token's k, v are already in K/V[u][n].
+ * With DV_KV_RESELECT: the observation window is the last W = obs_window
+ * cached positions n-W..n-1 with queries q_obs [h][W][d_h] fp16; every
+ * window query t attends causally to positions <= n-W+t (scores scaled by
+ * softmax_scale); the softmax probabilities are summed over the window and
+ * over the query heads of each KV head, smoothed by a centred width-`smooth`
+ * mean (zero padded, divided by smooth); the positions 0..n_sinks-1 and the
+ * window are forced, and the remaining budget b - forced (b = floor(n kv_keep))
+ * is filled by the highest smoothed scores (ties to the lower position).
+ * The kept positions, ascending, go to kept_pos[u][*], their count to
+ * kept_count[u], and their K, V rows to Kr/Vr[u][*] (b <= b_max - 1).
+ * Every call then appends K/V[u][n] at Kr/Vr[u][kept_count[u]] and computes
+ * H[j] = attention of q[j] over Kr/Vr[u][0..kept_count[u]] (or, with
+ * DV_KV_DENSE, over K/V[u][0..n]) by split-K and combine. H [h][d_h] fp32.
+ * sel_scores [h_kv][n] fp32 (nullable) receives the smoothed scores. */
+int dv_kv_select_attn(const float* q, const dv_dims* dims, dv_kv_cache* kv, int n,
+                      const uint16_t* q_obs, int obs_window, int n_sinks, int smooth,
+                      float kv_keep, float softmax_scale, int flags, float* H, float* sel_scores,
+                      int* dev_status, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---- a1 + a10: one decode layer with look-ahead ([DV] §4.3, App. C.3) --------
+ * y_out = h + MLP_{S_M}(h), h = y_in + MHA_{S_A}(y_in), with S_A, S_M taken
+ * from cur (per-row sets; for B > 1 their unions, [DV] App. C.1).
+ * DV_SYNC_PREDICT: first compute cur from y_in with this layer's P1/P2 on
+ *   `main` (used for layer 0 and for sync mode).
+ * DV_LOOKAHEAD: record ev_fork on `main` once y_in is ready, and on `side`
+ *   compute next (the sets of layer l+1) from y_in with P1_next / P2_next,
+ *   then record ev_join ([DV] §4.3: S^{l+1} <- SP(y_l), in parallel with
+ *   layer l). DV_JOIN: `main` first waits on ev_join (pass it for every layer
+ *   after one that looked ahead).
+ * keep->head == 1 uses all units; keep->neuron == 1 all neurons.
+ * DV_KV_RETAINED / DV_KV_ADVANCE as in dv_sparse_attn. y_in, y_out [B][d]. */
+int dv_decode_layer(const dv_dims* dims, const dv_keep* keep, int B, const dv_layer_weights* w,
+                    const uint16_t* P1_next, const uint16_t* P2_next, dv_kv_cache* kv, int n,
+                    float softmax_scale, dv_sets* cur, dv_sets* next, const uint16_t* y_in,
+                    uint16_t* y_out, int flags, int* dev_status, void* ws, size_t ws_bytes,
+                    cudaStream_t main, cudaStream_t side, cudaEvent_t ev_fork,
+                    cudaEvent_t ev_join);
+
+/* One decode step over L stacked layers: layer 0 predicts synchronously, each
+ * layer l looks ahead for l+1 on `side` (when flags has DV_LOOKAHEAD), layer l
+ * reads the sets written by layer l-1's look-ahead. sets[0], sets[1] are used
+ * alternately. y_tmp [2][B][d] holds the intermediate layer outputs.
+ * y_out = layer L-1's output. Same stream / event rules as above. */
+int dv_decode_step(const dv_dims* dims, const dv_keep* keep, int B, int L,
+                   const dv_layer_weights* w /* [L], host array */,
+                   dv_kv_cache* kv /* [L], host array */, int n, float softmax_scale,
+                   dv_sets* sets /* [2], host array */, const uint16_t* y_in, uint16_t* y_tmp,
+                   uint16_t* y_out, int flags, int* dev_status, void* ws, size_t ws_bytes,
+                   cudaStream_t main, cudaStream_t side, cudaEvent_t ev_fork,
+                   cudaEvent_t ev_join);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DV_H */

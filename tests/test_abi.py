@@ -1,0 +1,147 @@
+"""The C ABI: libdv.so builds, exports every symbol include/dv.h declares, and
+host-side validation rejects bad arguments with a status code before anything
+is enqueued. No compute calls: every case here fails validation first (no
+pointer given here is ever dereferenced)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from contextual_sparsity_gb300 import build, dv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return dv.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "dv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w \t*]*?\b(dv_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared()
+    assert "dv_sparse_mlp" in names and "dv_decode_layer" in names and len(names) >= 11
+    out = subprocess.run(["nm", "-D", "--defined-only", dv.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(dv_\w+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    assert sorted(dv.EXPORTED) == names
+
+
+def test_status_strings(L):
+    assert dv.status_string(0) == "ok"
+    for c in range(-8, 0):
+        s = dv.status_string(c)
+        assert s and s != "unknown status"
+    assert dv.status_string(-99) == "unknown status"
+    assert L.dv_version() >= 100
+
+
+def _dims(**kw):
+    base = dict(d=256, h=4, h_kv=4, d_h=64, F=1024, r=32, n_max=80, ln_eps=1e-5)
+    base.update(kw)
+    return dv.Dims(**base)
+
+
+def test_workspace_size_rejects_bad_dims(L):
+    assert dv.workspace_size(_dims()) > 0
+    for bad in (dict(d=250), dict(d=0), dict(h=6, h_kv=4), dict(d_h=96), dict(F=0), dict(r=30),
+                dict(n_max=0)):
+        assert dv.workspace_size(_dims(**bad)) == 0, bad
+    assert L.dv_workspace_size(ctypes.byref(_dims()), 5, 0) == 0
+    assert L.dv_workspace_size(None, 1, 0) == 0
+
+
+FAKE = 0x100000   # aligned, never dereferenced: every call below fails validation first
+MISALIGNED = 0x100002
+
+
+def _w(**kw):
+    w = {n: FAKE for n in ("Wq", "Wk", "Wv", "WoT", "fc1", "fc2T", "P1", "P2")}
+    w.update(kw)
+    return dv.LayerWeights(*[w.get(n) for n in dv._W_FIELDS])
+
+
+def _mlp(L, x=FAKE, B=1, D=None, w=None, idx=None, k=1, out=FAKE + 4096, ws=FAKE * 2, ws_bytes=0):
+    D = D or _dims()
+    w = w or _w()
+    return L.dv_sparse_mlp(x, B, ctypes.byref(D), ctypes.byref(w), idx, k, None, 0, out, None, ws,
+                           ws_bytes, None)
+
+
+def test_sparse_mlp_validation(L):
+    assert _mlp(L, x=None) == dv.DV_ERR_NULL
+    assert _mlp(L, x=MISALIGNED) == dv.DV_ERR_ALIGN
+    assert _mlp(L, D=_dims(d=100)) == dv.DV_ERR_DIMS
+    assert _mlp(L, w=_w(fc1=None)) == dv.DV_ERR_NULL
+    assert _mlp(L, w=_w(fc2T=MISALIGNED)) == dv.DV_ERR_ALIGN
+    assert _mlp(L, B=5) == dv.DV_ERR_DIMS
+    assert _mlp(L, idx=FAKE, k=0) == dv.DV_ERR_K
+    assert _mlp(L, idx=FAKE, k=1025) == dv.DV_ERR_K
+    assert _mlp(L, out=FAKE) == dv.DV_ERR_DIMS           # out aliases x
+    assert _mlp(L, ws=FAKE + 16) == dv.DV_ERR_ALIGN       # workspace wants 256-byte alignment
+    assert _mlp(L, idx=FAKE, k=8, ws_bytes=16) == dv.DV_ERR_WORKSPACE
+
+
+def test_predict_and_topk_validation(L):
+    f = L.dv_predict
+    assert f(None, 1, 256, FAKE, 32, FAKE, 10, 0, FAKE, FAKE, 1 << 20, None) == dv.DV_ERR_NULL
+    assert f(FAKE, 0, 256, FAKE, 32, FAKE, 10, 0, FAKE, FAKE, 1 << 20, None) == dv.DV_ERR_DIMS
+    assert f(FAKE, 1, 256, FAKE, 30, FAKE, 10, 0, FAKE, FAKE, 1 << 20, None) == dv.DV_ERR_DIMS
+    assert f(FAKE, 1, 256, FAKE, 32, FAKE, 10, 0, FAKE, FAKE, 8, None) == dv.DV_ERR_WORKSPACE
+    t = L.dv_select_topk
+    assert t(FAKE, 1, 10, 10, 0, FAKE, None, None, None, None, 0, None) == dv.DV_ERR_K
+    assert t(FAKE, 1, 10, 10, 11, FAKE, None, None, None, None, 0, None) == dv.DV_ERR_K
+    assert t(FAKE, 1, 5, 10, 3, FAKE, None, None, None, None, 0, None) == dv.DV_ERR_DIMS
+    assert t(FAKE, 9, 10, 10, 3, FAKE, None, None, None, None, 0, None) == dv.DV_ERR_DIMS
+    assert t(FAKE, 1, 10, 10, 3, FAKE, FAKE, None, None, None, 0, None) == dv.DV_ERR_NULL
+
+
+def test_attention_and_layer_validation(L):
+    D = _dims()
+    w = _w()
+    kv = dv.KvCache(FAKE, FAKE, None, None, None, None, None, None, 0)
+    a = L.dv_sparse_attn
+    args = lambda n=10, k=2, flags=0, kvp=kv: (FAKE, 1, ctypes.byref(D), ctypes.byref(w), FAKE, k,
+                                                None, ctypes.byref(kvp), n, 0.125, flags,
+                                                FAKE + 4096, None, FAKE * 2, 16, None)
+    assert a(*args(n=80)) == dv.DV_ERR_DIMS          # n must be < n_max
+    assert a(*args(n=-1)) == dv.DV_ERR_DIMS
+    assert a(*args(k=5)) == dv.DV_ERR_K
+    assert a(*args(flags=dv.DV_KV_RETAINED)) == dv.DV_ERR_NULL   # no retained buffers
+    assert a(*args()) == dv.DV_ERR_WORKSPACE
+    keep = dv.Keep(0.0, 0.5, 1.0)
+    lay = L.dv_decode_layer
+    s = dv.Sets(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)
+    call = lambda kp, B=1: lay(ctypes.byref(D), ctypes.byref(kp), B, ctypes.byref(w), None, None,
+                                 ctypes.byref(kv), 10, 0.125, ctypes.byref(s), None, FAKE,
+                                 FAKE + 4096, 0, None, FAKE * 2, 16, None, None, None, None)
+    assert call(keep) == dv.DV_ERR_KEEP
+    assert call(dv.Keep(1.5, 0.5, 1.0)) == dv.DV_ERR_KEEP
+    assert call(dv.Keep(0.25, 0.5, 1.0), B=0) == dv.DV_ERR_DIMS
+    assert call(dv.Keep(0.25, 0.5, 1.0)) == dv.DV_ERR_WORKSPACE
+
+
+def test_kv_select_validation(L):
+    D = _dims(h=8, h_kv=2, n_max=300)
+    kv = dv.KvCache(FAKE, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, 64)
+    f = L.dv_kv_select_attn
+    big = 1 << 40
+    call = lambda n=200, W=64, sinks=4, sm=7, keep=0.125, flags=dv.DV_KV_RESELECT: f(
+        FAKE, ctypes.byref(D), ctypes.byref(kv), n, FAKE, W, sinks, sm, keep, 0.1, flags, FAKE,
+        None, None, FAKE * 2, big, None)
+    assert call(W=0) == dv.DV_ERR_DIMS
+    assert call(W=201) == dv.DV_ERR_DIMS
+    assert call(sm=6) == dv.DV_ERR_DIMS
+    assert call(keep=0.0) == dv.DV_ERR_KEEP
+    assert call(keep=1.5) == dv.DV_ERR_KEEP
+    assert call(n=300) == dv.DV_ERR_DIMS
