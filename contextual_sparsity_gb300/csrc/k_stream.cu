@@ -403,8 +403,9 @@ __global__ void __launch_bounds__(B == 1 ? 288 : 416, 1) k_stream(const StreamPa
             uint16_t* cache = isk ? p.K : p.V;
             cache[(((size_t)b * p.h_kv + u) * p.n_max + p.n) * p.dh + c] = hv;
             if (p.Kr) {
+              const int slot = p.kept_count[u];
               uint16_t* rc = isk ? p.Kr : p.Vr;
-              rc[((size_t)u * p.b_max + p.kept_count[u]) * p.dh + c] = hv;
+              if (slot >= 0 && slot < p.b_max) rc[((size_t)u * p.b_max + slot) * p.dh + c] = hv;
             }
           }
         }
@@ -775,6 +776,10 @@ int launch_predict(const uint16_t* y, int B, int d, const uint16_t* P1, int r,
   const int threads = 256, nw = threads / 32;
   int grid = std::min((N + nw - 1) / nw, std::max(1, target_ctas));
   const size_t smem = (size_t)B * r * sizeof(float);
+  if (smem > 48 * 1024) {
+    cudaFuncSetAttribute(k_pred2<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncSetAttribute(k_pred2<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  }
   note_launch(DV_TAG_PRED2, 0, stream);
   if (B == 1)
     k_pred2<1><<<grid, threads, smem, stream>>>(u, r, P2, N, scores, ld, B);
