@@ -99,7 +99,9 @@ DV_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar, 
 }
 
 // ---- named barrier among the consumer warps (id 1) ------------------------
+// The warp reconverges first: bar.sync is executed per warp.
 DV_DEV void consumer_sync(int nthreads) {
+  __syncwarp();
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 

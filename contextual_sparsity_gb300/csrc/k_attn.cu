@@ -98,12 +98,14 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
   }
 
   const int step = 4 * KPW;  // keys per CTA step
-  for (int base = t0 + warp * KPW + grp; base < t1; base += step * U) {
+  // The loop bound is warp-uniform (the shuffles below need every lane);
+  // lanes whose key lies past the split's end carry a zero weight.
+  for (int wbase = t0 + warp * KPW; wbase < t1; wbase += step * U) {
     uint4 kv[U], vv[U];
     bool valid[U];
 #pragma unroll
     for (int j = 0; j < U; ++j) {
-      const int t = base + j * step;
+      const int t = wbase + grp + j * step;
       valid[j] = t < t1;
       if (valid[j]) {
         kv[j] = ld_nc_v4(Kb + (size_t)t * DH + sub * 8);

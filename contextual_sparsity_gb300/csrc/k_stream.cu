@@ -148,6 +148,13 @@ DV_DEV const uint16_t* row_addr(const StreamParams& p, int kind, int phase, int 
 // The kernel
 // ---------------------------------------------------------------------------
 template <int KIND, int B, int V>
+DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                    uint64_t* act_ready, float* red, float* coef, float* lnred, int* list,
+                    volatile int* abort_flag, volatile int* list_count, const int kk,
+                    const int per, const int r0, const int nrows, const bool has_dot,
+                    const bool has_axpy, const bool skip);
+
+template <int KIND, int B, int V>
 __global__ void __launch_bounds__(B == 1 ? 288 : 416, 1) k_stream(const StreamParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const StreamGeom& g = p.g;
@@ -230,11 +237,26 @@ __global__ void __launch_bounds__(B == 1 ? 288 : 416, 1) k_stream(const StreamPa
       for (int j = (it > g.NS ? it - g.NS : 0); j < it; ++j)
         if (!mbar_wait(&full[j % g.NS], (j / g.NS) & 1)) flag(p.st, DV_DEV_TIMEOUT);
     }
-    __syncthreads();
-    return;
+    __syncwarp();
+  } else {
+    consume<KIND, B, V>(p, smem, full, empty, act_ready, red, coef, lnred, list, abort_flag,
+                        list_count, kk, per, r0, nrows, has_dot, has_axpy, skip);
   }
+  // Both roles meet here once, with converged warps.
+  __syncthreads();
+}
 
-  // ======================= consumer warps =======================
+// ======================= consumer warps =======================
+template <int KIND, int B, int V>
+DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                    uint64_t* act_ready, float* red, float* coef, float* lnred, int* list,
+                    volatile int* abort_flag, volatile int* list_count, const int kk,
+                    const int per, const int r0, const int nrows, const bool has_dot,
+                    const bool has_axpy, const bool skip) {
+  const StreamGeom& g = p.g;
+  const int T = g.T, nwc = T / 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nvec = p.d >> 3;
   // Activation columns of this thread: vectors v_m = tid + m T (8 columns each).
   float z[B][V][8];
   int it = 0;
@@ -334,6 +356,7 @@ __global__ void __launch_bounds__(B == 1 ? 288 : 416, 1) k_stream(const StreamPa
         flag(p.st, DV_DEV_TIMEOUT);
         ok = false;
       }
+      ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the row sums below shuffle
       if (ok) {
         for (int c = 0; c < cnt; ++c) {
           const uint8_t* row = smem + (size_t)s * g.stage_bytes + (size_t)c * g.row_bytes;
@@ -501,6 +524,7 @@ __global__ void __launch_bounds__(B == 1 ? 288 : 416, 1) k_stream(const StreamPa
         flag(p.st, DV_DEV_TIMEOUT);
         ok = false;
       }
+      ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the row sums below shuffle
       if (ok) {
         for (int c = 0; c < cnt; ++c) {
           const int li = skip ? list[q0 + c] : (q0 + c);
@@ -541,7 +565,7 @@ __global__ void __launch_bounds__(B == 1 ? 288 : 416, 1) k_stream(const StreamPa
       }
     }
   }
-  __syncthreads();
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
