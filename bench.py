@@ -198,8 +198,8 @@ class Model:
         self.y_tmp = torch.empty(2, w.B, w.d, dtype=torch.float16, device=device)
         self.y_out = torch.empty(w.B, w.d, dtype=torch.float16, device=device)
         self.side = torch.cuda.Stream(device=device)
-        self.evf = torch.cuda.Event()
-        self.evj = torch.cuda.Event()
+        self.evf = dv.event()
+        self.evj = dv.event()
         self.st = torch.zeros(1, dtype=torch.int32, device=device)
         flags = dv.DV_LOOKAHEAD if lookahead else 0
         self.step = dv.Step(self.D, self.keep, self.W, self.kvs, [s for s, _ in self.sets],
@@ -358,6 +358,8 @@ def run_ours(a):
     sel, pred = traffic.layer_bytes(w)
     gbs_sel = sel / (us_layer * 1e-6) / 1e9
     gbs_all = (sel + pred) / (us_layer * 1e-6) / 1e9
+    print(f"[bench] {us_layer:.2f} us/layer, {gbs_sel:.0f} GB/s selected, {gbs_all:.0f} GB/s all, "
+          f"{per_step} launches/step", file=sys.stderr, flush=True)
 
     # Per-kernel durations: a second graph of the same step with every launch
     # bracketed by CUDA events on its own stream, replayed after warm-up.

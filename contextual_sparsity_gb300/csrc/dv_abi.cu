@@ -42,7 +42,9 @@ static long long g_launches = 0;
 void note_launch(int tag, int phase, cudaStream_t s) {
   if (phase == 0) ++g_launches;
   if (!g_prof_ev || g_prof_n >= g_prof_cap) return;
-  cudaEventRecord(g_prof_ev[2 * g_prof_n + phase], s);
+  // External records become event nodes under stream capture (a plain record
+  // would only express a dependency), so graph replays leave timestamps.
+  cudaEventRecordWithFlags(g_prof_ev[2 * g_prof_n + phase], s, cudaEventRecordExternal);
   if (phase == 0) {
     g_prof_tags[g_prof_n] = tag;
   } else {

@@ -136,6 +136,23 @@ def _stream(stream=None):
     return s.cuda_stream
 
 
+def event(timing=False) -> "torch.cuda.Event":
+    """A CUDA event whose handle exists now (torch creates handles lazily, on
+    the first record), usable as ev_fork / ev_join or for profiling."""
+    e = torch.cuda.Event(enable_timing=timing)
+    e.record()
+    return e
+
+
+def _ev(e):
+    if e is None:
+        return None
+    h = e.cuda_event
+    if not h:
+        raise ValueError("CUDA event has no handle yet; create it with dv.event()")
+    return h
+
+
 def dims(d, h, h_kv, d_h, F, r, n_max, ln_eps=1e-5) -> Dims:
     return Dims(d, h, h_kv, d_h, F, r, n_max, ln_eps)
 
@@ -246,8 +263,7 @@ def decode_layer(D: Dims, keep: Keep, W: dict, P_next, kv: KvCache, n, cur: Sets
                                  ptr(y_in), ptr(y_out), flags, ptr(dev_status), ptr(ws),
                                  ws.numel(), _stream(stream),
                                  side.cuda_stream if side is not None else None,
-                                 ev_fork.cuda_event if ev_fork is not None else None,
-                                 ev_join.cuda_event if ev_join is not None else None),
+                                 _ev(ev_fork), _ev(ev_join)),
            "dv_decode_layer")
 
 
@@ -262,7 +278,7 @@ def decode_step(D: Dims, keep: Keep, Ws: list, kvs: list, n, sets2: list, y_in, 
     _check(lib().dv_decode_step(ctypes.byref(D), ctypes.byref(keep), y_in.shape[0], L, warr, karr,
                                 n, scale, sarr, ptr(y_in), ptr(y_tmp), ptr(y_out), flags,
                                 ptr(dev_status), ptr(ws), ws.numel(), _stream(stream),
-                                side.cuda_stream, ev_fork.cuda_event, ev_join.cuda_event),
+                                side.cuda_stream, _ev(ev_fork), _ev(ev_join)),
            "dv_decode_step")
 
 
@@ -280,7 +296,7 @@ class Profiler:
 
     def __init__(self, cap=4096):
         self.cap = cap
-        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * cap)]
+        self.events = [event(timing=True) for _ in range(2 * cap)]
         self._ev = (ctypes.c_void_p * (2 * cap))(*[e.cuda_event for e in self.events])
         self._tags = (ctypes.c_int * cap)()
         self.n = 0
@@ -326,5 +342,5 @@ class Step:
                                     ptr(y_in), ptr(y_tmp), ptr(y_out), self.flags,
                                     ptr(self.dev_status), ptr(self.ws), self.ws.numel(),
                                     _stream(stream), self.side.cuda_stream,
-                                    self.ev_fork.cuda_event, self.ev_join.cuda_event),
+                                    _ev(self.ev_fork), _ev(self.ev_join)),
                "dv_decode_step")

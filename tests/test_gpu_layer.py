@@ -49,7 +49,7 @@ class Stack:
 def _layer_by_layer(S: Stack, lookahead=True):
     kvs = S.fresh_kv()
     side = torch.cuda.Stream()
-    evf, evj = torch.cuda.Event(), torch.cuda.Event()
+    evf, evj = dv.event(), dv.event()
     ys = [S.x.cuda()]
     used_sets = []
     for l in range(S.L):
@@ -126,7 +126,7 @@ def test_driver_matches_layers_and_graph_replay():
     S = Stack(synth.workload("tiny", d=512, h=8, h_kv=8, F=2048, r=64, n=96), 4)
     ys, _ = _layer_by_layer(S)
     side = torch.cuda.Stream()
-    evf, evj = torch.cuda.Event(), torch.cuda.Event()
+    evf, evj = dv.event(), dv.event()
     y_tmp = torch.empty(2, 1, S.w.d, dtype=torch.float16, device="cuda")
     y_out = torch.empty(1, S.w.d, dtype=torch.float16, device="cuda")
     kvs = S.fresh_kv()
