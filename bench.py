@@ -54,7 +54,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--tuning", default=None, help="main,side,main_ring_kb,side_ring_kb,attn")
+    ap.add_argument("--tuning", default=None,
+                    help="main,side,main_ring_kb,side_ring_kb,attn,pdl,stage_kb (see dv_set_tuning)")
+    ap.add_argument("--timeline", type=int, default=0,
+                    help="print start/end of the first N launches of a profiled step to stderr")
     return ap.parse_args()
 
 
@@ -371,6 +374,13 @@ def run_ours(a):
         for _ in range(20):
             gp.replay()
     torch.cuda.synchronize()
+    if a.timeline:
+        t0 = prof.events[0]
+        for i in range(min(a.timeline, prof.n)):
+            tag = dv.TAGS.get(prof._tags[i], "?")
+            b, e = t0.elapsed_time(prof.events[2 * i]), t0.elapsed_time(prof.events[2 * i + 1])
+            print(f"[timeline] {i:4d} {tag:9s} {b * 1e3:9.2f} {e * 1e3:9.2f} {(e - b) * 1e3:8.2f}",
+                  file=sys.stderr)
     per_kind = {}
     for tag, ms in prof.durations_ms():
         per_kind.setdefault(tag, []).append(ms * 1e3)

@@ -15,7 +15,7 @@ namespace dv {
 
 struct Tuning {
   int main_ctas = 0;        // 0: one per SM
-  int side_ctas = 16;       // predictor CTAs on the side stream
+  int side_ctas = 0;        // predictor CTAs on the side stream; 0: two per SM
   int main_ring = 160 * 1024;
   int side_ring = 32 * 1024;
   int attn_ctas = 0;        // split-K CTA target; 0: 4 per SM
@@ -44,7 +44,12 @@ void note_launch(int tag, int phase, cudaStream_t s) {
   if (!g_prof_ev || g_prof_n >= g_prof_cap) return;
   // External records become event nodes under stream capture (a plain record
   // would only express a dependency), so graph replays leave timestamps.
-  cudaEventRecordWithFlags(g_prof_ev[2 * g_prof_n + phase], s, cudaEventRecordExternal);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(g_prof_ev[2 * g_prof_n + phase], s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(g_prof_ev[2 * g_prof_n + phase], s);
   if (phase == 0) {
     g_prof_tags[g_prof_n] = tag;
   } else {
@@ -52,8 +57,26 @@ void note_launch(int tag, int phase, cudaStream_t s) {
   }
 }
 
+static int side_ctas() { return g_tune.side_ctas > 0 ? g_tune.side_ctas : 2 * sm_count(); }
 static int main_ctas() { return g_tune.main_ctas > 0 ? g_tune.main_ctas : sm_count(); }
-static int attn_ctas() { return g_tune.attn_ctas > 0 ? g_tune.attn_ctas : 4 * sm_count(); }
+
+static bool g_pdl = true;
+
+cudaError_t launch_k(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     void** args, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = (pdl && g_pdl) ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+static int attn_ctas() { return g_tune.attn_ctas > 0 ? g_tune.attn_ctas : 2 * sm_count(); }
 
 static int k_from_keep(float keep, int N) {
   const double k = std::floor((double)keep * (double)N + 1e-9);
@@ -92,7 +115,7 @@ static int check_dims(const dv_dims* D) {
 
 // ---- workspace layout ------------------------------------------------------
 struct WsLayout {
-  size_t part, qbuf, sk, hmid, u_main, u_side, kvsel, total;
+  size_t part, qbuf, sk, hcomb, cnt, hmid, u_main, u_side, kvsel, total;
   size_t kvsel_floats;
   int S_max;
 };
@@ -113,6 +136,10 @@ static WsLayout ws_layout(const dv_dims* D, int B, int flags) {
   off += al((size_t)B * D->h * D->d_h * 4);
   L.sk = off;
   off += al((size_t)B * D->h_kv * G * L.S_max * (D->d_h + 2) * 4);
+  L.hcomb = off;
+  off += al((size_t)B * D->h * D->d_h * 4);
+  L.cnt = off;
+  off += al((size_t)B * D->h_kv * 4);
   L.hmid = off;
   off += al((size_t)B * D->d * 2);
   L.u_main = off;
@@ -135,54 +162,75 @@ static T* at(void* ws, size_t off) {
 }
 
 // ---- the attention block and the MLP block (shared by the entry points) ----
-static int run_attn(const uint16_t* x, int B, const dv_dims* D, const dv_layer_weights* w,
+// QKV gather-GEMV (+ KV append; optionally the look-ahead predictor's first
+// layer on the same input, written to u_out).
+static int attn_qkv(const uint16_t* x, int B, const dv_dims* D, const dv_layer_weights* w,
                     const int32_t* sel, int k, const int32_t* dev_count, dv_kv_cache* kv, int n,
-                    float scale, int flags, uint16_t* out, int* st, void* ws, const WsLayout& L,
-                    cudaStream_t s) {
+                    float scale, int flags, const uint16_t* P1n, float* u_out, int* st, void* ws,
+                    const WsLayout& L, cudaStream_t s, bool pdl) {
   const int G = D->h / D->h_kv;
   const bool ret = (flags & DV_KV_RETAINED) != 0;
-  int rc = launch_qkv(x, B, D->d, G, D->d_h, D->h_kv, w->ln1_g, w->ln1_b, D->ln_eps, w->Wq, w->bq,
-                      w->Wk, w->bk, w->Wv, w->bv, sel, k, dev_count, scale, at<float>(ws, L.qbuf),
-                      kv->K, kv->V, n, D->n_max, ret ? kv->Kr : nullptr, ret ? kv->Vr : nullptr,
-                      kv->kept_count, kv->b_max, kv->y_side, kv->kv_missing, st, main_ctas(),
-                      g_tune.main_ring, s);
-  if (rc != DV_OK) return rc;
+  return launch_qkv(x, B, D->d, G, D->d_h, D->h_kv, w->ln1_g, w->ln1_b, D->ln_eps, w->Wq, w->bq,
+                    w->Wk, w->bk, w->Wv, w->bv, sel, k, dev_count, scale, at<float>(ws, L.qbuf),
+                    kv->K, kv->V, n, D->n_max, ret ? kv->Kr : nullptr, ret ? kv->Vr : nullptr,
+                    kv->kept_count, kv->b_max, kv->y_side, kv->kv_missing, at<int>(ws, L.cnt),
+                    B * D->h_kv, P1n, D->r, (flags & DV_PRED_RELU) ? 1 : 0, u_out, st,
+                    main_ctas(), g_tune.main_ring, s, pdl);
+}
+
+// Split-K attention with the combine fused, then the Wo^T gather-axpy and the
+// residual.
+static int attn_rest(const uint16_t* x, int B, const dv_dims* D, const dv_layer_weights* w,
+                     const int32_t* sel, int k, const int32_t* dev_count, dv_kv_cache* kv, int n,
+                     int flags, uint16_t* out, int* st, void* ws, const WsLayout& L,
+                     cudaStream_t s) {
+  const int G = D->h / D->h_kv;
+  const bool ret = (flags & DV_KV_RETAINED) != 0;
   const int max_keys = ret ? kv->b_max : n + 1;
   SplitPlan plan = split_plan(max_keys, k, B, attn_ctas());
   if (plan.S > L.S_max) return DV_ERR_WORKSPACE;
-  rc = launch_splitk(at<float>(ws, L.qbuf), B, D->d_h, G, D->h_kv, sel, k, dev_count, kv->K, kv->V,
-                     n, D->n_max, kv->Kr, kv->Vr, kv->kept_count, kv->b_max, ret ? 1 : 0, plan,
-                     at<float>(ws, L.sk), st, s);
+  int rc = launch_splitk(at<float>(ws, L.qbuf), B, D->d_h, G, D->h_kv, sel, k, dev_count, kv->K,
+                         kv->V, n, D->n_max, kv->Kr, kv->Vr, kv->kept_count, kv->b_max,
+                         ret ? 1 : 0, plan, at<float>(ws, L.sk), at<float>(ws, L.hcomb),
+                         at<int>(ws, L.cnt), st, s, true);
   if (rc != DV_OK) return rc;
   rc = launch_wo((flags & DV_NO_RESIDUAL) ? nullptr : x, B, D->d, G, D->d_h, D->h_kv, w->WoT,
-                 w->bo, sel, k, dev_count,
-                 at<float>(ws, L.sk), plan.S, out, st, at<float>(ws, L.part), main_ctas(),
-                 g_tune.main_ring, s);
+                 w->bo, sel, k, dev_count, at<float>(ws, L.hcomb), out, st, at<float>(ws, L.part),
+                 main_ctas(), g_tune.main_ring, s);
   if (rc != DV_OK) return rc;
   if (ret && (flags & DV_KV_ADVANCE)) rc = launch_kv_advance(kv->kept_count, D->h_kv, kv->b_max, s);
   return rc;
 }
 
+static int run_attn(const uint16_t* x, int B, const dv_dims* D, const dv_layer_weights* w,
+                    const int32_t* sel, int k, const int32_t* dev_count, dv_kv_cache* kv, int n,
+                    float scale, int flags, uint16_t* out, int* st, void* ws, const WsLayout& L,
+                    cudaStream_t s) {
+  int rc = attn_qkv(x, B, D, w, sel, k, dev_count, kv, n, scale, flags, nullptr, nullptr, st, ws, L,
+                    s, false);
+  if (rc != DV_OK) return rc;
+  return attn_rest(x, B, D, w, sel, k, dev_count, kv, n, flags, out, st, ws, L, s);
+}
+
 static int run_mlp(const uint16_t* x, int B, const dv_dims* D, const dv_layer_weights* w,
                    const int32_t* sel, int k, const int32_t* dev_count, int flags, uint16_t* out,
-                   int* st, void* ws, const WsLayout& L, cudaStream_t s) {
+                   int* st, void* ws, const WsLayout& L, cudaStream_t s, bool pdl) {
   return launch_mlp(x, B, D->d, D->F, w->ln2_g, w->ln2_b, D->ln_eps, w->fc1, w->b1, w->fc2T, w->b2,
                     sel, k, dev_count, flags & (DV_SKIP_INACTIVE | DV_NO_RESIDUAL), out, st,
                     at<float>(ws, L.part),
-                    main_ctas(), g_tune.main_ring, s);
+                    main_ctas(), g_tune.main_ring, s, pdl);
 }
 
-// Predict the sets of one layer from y into `sets` (per-row top-k, unions).
-static int run_sets(const dv_dims* D, int B, const uint16_t* y, const uint16_t* P1,
-                    const uint16_t* P2, int kN, bool neuron_dense, int kH, bool head_dense,
-                    int flags, dv_sets* sets, int* st, float* u, int ctas, int ring,
-                    cudaStream_t s) {
+// Second predictor layer on u, then per-row top-k and (B > 1) unions.
+static int sets_from_u(const dv_dims* D, int B, const float* u, const uint16_t* P2, int kN,
+                       bool neuron_dense, int kH, bool head_dense, dv_sets* sets, int* st,
+                       int ctas, cudaStream_t s) {
   const int ld = D->F + D->h_kv;
   const int row0 = neuron_dense ? D->F : 0;
   const int row1 = head_dense ? D->F : ld;
   if (row1 <= row0) return DV_OK;
-  int rc = launch_predict(y, B, D->d, P1, D->r, P2 + (size_t)row0 * D->r, row1 - row0,
-                          (flags & DV_PRED_RELU) ? 1 : 0, sets->scores + row0, ld, u, ctas, ring, s);
+  int rc = launch_pred2(u, B, D->r, P2 + (size_t)row0 * D->r, row1 - row0, sets->scores + row0, ld,
+                        ctas, s);
   if (rc != DV_OK) return rc;
   if (!neuron_dense) {
     rc = launch_topk(sets->scores, B, ld, D->F, nullptr, kN, sets->idx_N, kN, st, s);
@@ -196,6 +244,17 @@ static int run_sets(const dv_dims* D, int B, const uint16_t* y, const uint16_t* 
     if (rc != DV_OK) return rc;
   }
   return DV_OK;
+}
+
+// Predict the sets of one layer from y (both predictor layers, top-k, unions).
+static int run_sets(const dv_dims* D, int B, const uint16_t* y, const uint16_t* P1,
+                    const uint16_t* P2, int kN, bool neuron_dense, int kH, bool head_dense,
+                    int flags, dv_sets* sets, int* st, float* u, int ctas, int ring,
+                    cudaStream_t s) {
+  if (neuron_dense && head_dense) return DV_OK;
+  int rc = launch_pred1(y, B, D->d, P1, D->r, (flags & DV_PRED_RELU) ? 1 : 0, u, ctas, ring, s);
+  if (rc != DV_OK) return rc;
+  return sets_from_u(D, B, u, P2, kN, neuron_dense, kH, head_dense, sets, st, ctas, s);
 }
 
 static int check_weights_attn(const dv_layer_weights* w) {
@@ -278,15 +337,18 @@ long long dv_launch_count(void) { return g_launches; }
 
 // Tuning knobs for launch shapes (aux; defaults need no call).
 int dv_set_tuning(int main_ctas, int side_ctas, int main_ring_kb, int side_ring_kb,
-                  int attn_ctas) {
-  if (main_ctas < 0 || side_ctas < 1 || main_ring_kb < 16 || main_ring_kb > 200 ||
-      side_ring_kb < 8 || side_ring_kb > 200 || attn_ctas < 0)
+                  int attn_ctas, int pdl, int stage_kb) {
+  if (main_ctas < 0 || side_ctas < 0 || main_ring_kb < 16 || main_ring_kb > 200 ||
+      side_ring_kb < 8 || side_ring_kb > 200 || attn_ctas < 0 || stage_kb < 4 ||
+      stage_kb > 100)
     return DV_ERR_DIMS;
+  g_stage_target = stage_kb * 1024;
   g_tune.main_ctas = main_ctas;
   g_tune.side_ctas = side_ctas;
   g_tune.main_ring = main_ring_kb * 1024;
   g_tune.side_ring = side_ring_kb * 1024;
   g_tune.attn_ctas = attn_ctas;
+  g_pdl = pdl != 0;
   return DV_OK;
 }
 
@@ -331,7 +393,7 @@ int dv_sparse_mlp(const uint16_t* x, int B, const dv_dims* dims, const dv_layer_
   REQ(x != out, DV_ERR_DIMS);
   const WsLayout L = ws_layout(dims, B, 0);
   REQ(ws_bytes >= L.total, DV_ERR_WORKSPACE);
-  return run_mlp(x, B, dims, w, idx, k, dev_count, flags, out, dev_status, ws, L, stream);
+  return run_mlp(x, B, dims, w, idx, k, dev_count, flags, out, dev_status, ws, L, stream, false);
 }
 
 int dv_sparse_attn(const uint16_t* x, int B, const dv_dims* dims, const dv_layer_weights* w,
@@ -392,11 +454,11 @@ int dv_kv_select_attn(const float* q, const dv_dims* dims, dv_kv_cache* kv, int 
   const int max_keys = dense ? n + 1 : kv->b_max;
   SplitPlan plan = split_plan(max_keys, dims->h_kv, 1, attn_ctas());
   if (plan.S > L.S_max) return DV_ERR_WORKSPACE;
+  if (cudaMemsetAsync(at<int>(ws, L.cnt), 0, sizeof(int) * dims->h_kv, stream) != cudaSuccess)
+    return DV_ERR_LAUNCH;
   rc = launch_splitk(q, 1, dims->d_h, G, dims->h_kv, nullptr, dims->h_kv, nullptr, kv->K, kv->V, n,
                      dims->n_max, kv->Kr, kv->Vr, kv->kept_count, kv->b_max, dense ? 0 : 1, plan,
-                     at<float>(ws, L.sk), dev_status, stream);
-  if (rc != DV_OK) return rc;
-  rc = launch_combine(at<float>(ws, L.sk), 1, dims->h_kv, G, dims->d_h, plan.S, H, stream);
+                     at<float>(ws, L.sk), H, at<int>(ws, L.cnt), dev_status, stream, false);
   if (rc != DV_OK) return rc;
   if (!dense && (flags & DV_KV_ADVANCE))
     rc = launch_kv_advance(kv->kept_count, dims->h_kv, kv->b_max, stream);
@@ -438,6 +500,8 @@ int dv_decode_layer(const dv_dims* dims, const dv_keep* keep, int B, const dv_la
     REQ(next && next->scores && next->idx_N && next->idx_H, DV_ERR_NULL);
     if (B > 1) REQ(next->uN && next->uH && next->ucnt, DV_ERR_NULL);
     REQ(side && ev_fork && ev_join, DV_ERR_NULL);
+    REQ_PTR(P1_next);
+    REQ_PTR(P2_next);
   }
 
   if ((flags & DV_JOIN) && ev_join)
@@ -448,28 +512,35 @@ int dv_decode_layer(const dv_dims* dims, const dv_keep* keep, int B, const dv_la
                   at<float>(ws, L.u_main), main_ctas(), g_tune.main_ring, main);
     if (rc != DV_OK) return rc;
   }
-  if (look) {
-    if (cudaEventRecord(ev_fork, main) != cudaSuccess) return DV_ERR_LAUNCH;
-    if (cudaStreamWaitEvent(side, ev_fork, 0) != cudaSuccess) return DV_ERR_LAUNCH;
-    rc = run_sets(dims, B, y_in, P1_next, P2_next, kN, nd, kH, hd, flags, next, dev_status,
-                  at<float>(ws, L.u_side), g_tune.side_ctas, g_tune.side_ring, side);
-    if (rc != DV_OK) return rc;
-    if (cudaEventRecord(ev_join, side) != cudaSuccess) return DV_ERR_LAUNCH;
-  }
-
-  // Attention block: h = y + MHA_{S_A}(y).
+  // Attention block: h = y + MHA_{S_A}(y). The QKV kernel also streams the
+  // next layer's first predictor layer on y ([DV] 4.3: S^{l+1} <- SP(y_l));
+  // the rest of the prediction runs on the side stream alongside this layer.
   const int32_t* selH = hd ? nullptr : (B == 1 ? cur->idx_H : cur->uH);
   const int32_t* cntH = (hd || B == 1) ? nullptr : cur->ucnt + 1;
   const int kHe = (hd || B == 1) ? kH : std::min(dims->h_kv, B * kH);
   uint16_t* hmid = at<uint16_t>(ws, L.hmid);
-  rc = run_attn(y_in, B, dims, w, selH, kHe, cntH, kv, n, softmax_scale, flags, hmid, dev_status,
-                ws, L, main);
+  // PDL for the QKV kernel only when its index list was not produced by the
+  // kernel right before it (a synchronous prediction on this stream).
+  const bool pdl_qkv = !((flags & DV_SYNC_PREDICT) && need_pred) && (flags & DV_JOIN);
+  rc = attn_qkv(y_in, B, dims, w, selH, kHe, cntH, kv, n, softmax_scale, flags,
+                look ? P1_next : nullptr, at<float>(ws, L.u_side), dev_status, ws, L, main,
+                pdl_qkv);
+  if (rc != DV_OK) return rc;
+  if (look) {
+    if (cudaEventRecord(ev_fork, main) != cudaSuccess) return DV_ERR_LAUNCH;
+    if (cudaStreamWaitEvent(side, ev_fork, 0) != cudaSuccess) return DV_ERR_LAUNCH;
+    rc = sets_from_u(dims, B, at<float>(ws, L.u_side), P2_next, kN, nd, kH, hd, next, dev_status,
+                     side_ctas(), side);
+    if (rc != DV_OK) return rc;
+    if (cudaEventRecord(ev_join, side) != cudaSuccess) return DV_ERR_LAUNCH;
+  }
+  rc = attn_rest(y_in, B, dims, w, selH, kHe, cntH, kv, n, flags, hmid, dev_status, ws, L, main);
   if (rc != DV_OK) return rc;
   // MLP block: y' = h + MLP_{S_M}(h).
   const int32_t* selN = nd ? nullptr : (B == 1 ? cur->idx_N : cur->uN);
   const int32_t* cntN = (nd || B == 1) ? nullptr : cur->ucnt;
   const int kNe = (nd || B == 1) ? kN : std::min(dims->F, B * kN);
-  rc = run_mlp(hmid, B, dims, w, selN, kNe, cntN, flags, y_out, dev_status, ws, L, main);
+  rc = run_mlp(hmid, B, dims, w, selN, kNe, cntN, flags, y_out, dev_status, ws, L, main, true);
   if (rc != DV_OK) return rc;
   return launch_status();
 }

@@ -98,6 +98,13 @@ DV_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar, 
       : "memory");
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// launch_dependents lets the next kernel of the stream be scheduled before this
+// one ends; wait blocks until the previous kernel has completed and its memory
+// is visible (a no-op when the launch carried no programmatic dependency).
+DV_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+DV_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- named barrier among the consumer warps (id 1) ------------------------
 // The warp reconverges first: bar.sync is executed per warp.
 DV_DEV void consumer_sync(int nthreads) {

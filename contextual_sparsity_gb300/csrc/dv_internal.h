@@ -14,7 +14,7 @@ int launch_mlp(const uint16_t* x, int B, int d, int F, const uint16_t* ln_g, con
                float eps, const uint16_t* fc1, const uint16_t* b1, const uint16_t* fc2T,
                const uint16_t* b2, const int32_t* idx, int k, const int32_t* dev_count, int flags,
                uint16_t* out, int* st, float* part, int target_ctas, int ring_budget,
-               cudaStream_t stream);
+               cudaStream_t stream, bool pdl);
 
 int launch_qkv(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const uint16_t* ln_g,
                const uint16_t* ln_b, float eps, const uint16_t* Wq, const uint16_t* bq,
@@ -22,16 +22,23 @@ int launch_qkv(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const u
                const int32_t* idx, int k, const int32_t* dev_count, float scale, float* qbuf,
                uint16_t* K, uint16_t* V, int n, int n_max, uint16_t* Kr, uint16_t* Vr,
                const int32_t* kept_count, int b_max, uint16_t* y_side, uint32_t* kv_missing,
-               int* st, int target_ctas, int ring_budget, cudaStream_t stream);
+               int* zero_cnt, int n_zero, const uint16_t* P1, int n_pred, int relu, float* u_out,
+               int* st, int target_ctas, int ring_budget, cudaStream_t stream, bool pdl);
 
 int launch_wo(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const uint16_t* WoT,
               const uint16_t* bo, const int32_t* idx, int k, const int32_t* dev_count,
-              const float* sk_part, int S, uint16_t* out, int* st, float* part, int target_ctas,
+              const float* H, uint16_t* out, int* st, float* part, int target_ctas,
               int ring_budget, cudaStream_t stream);
 
 int launch_predict(const uint16_t* y, int B, int d, const uint16_t* P1, int r,
                    const uint16_t* P2, int N, int relu, float* scores, int ld, float* u,
                    int target_ctas, int ring_budget, cudaStream_t stream);
+
+int launch_pred1(const uint16_t* y, int B, int d, const uint16_t* P1, int r, int relu, float* u,
+                 int target_ctas, int ring_budget, cudaStream_t stream);
+
+int launch_pred2(const float* u, int B, int r, const uint16_t* P2, int N, float* scores, int ld,
+                 int target_ctas, cudaStream_t stream);
 
 size_t stream_part_bytes(int d, int B, long long max_rows, int target_ctas);
 
@@ -45,10 +52,8 @@ SplitPlan split_plan(int max_keys, int units, int B, int target_ctas);
 int launch_splitk(const float* q, int B, int dh, int G, int h_kv, const int32_t* idx, int k,
                   const int32_t* dev_count, const uint16_t* K, const uint16_t* V, int n, int n_max,
                   const uint16_t* Kr, const uint16_t* Vr, const int32_t* kept_count, int b_max,
-                  int retained, SplitPlan plan, float* part, int* st, cudaStream_t stream);
-
-int launch_combine(const float* part, int B, int units, int G, int dh, int S, float* H,
-                   cudaStream_t stream);
+                  int retained, SplitPlan plan, float* part, float* H, int* cnt, int* st,
+                  cudaStream_t stream, bool pdl);
 
 int launch_kv_select(const uint16_t* q_obs, int h, int h_kv, int dh, int W, const uint16_t* K,
                      const uint16_t* V, int n, int n_max, float scale, int n_sinks, int smooth,
@@ -71,8 +76,15 @@ int launch_topk(const float* scores, int B, int ld, int N, const int* k_per_row,
 int launch_union(const int32_t* idx, int B, int k, int N, int32_t* out, int32_t* count,
                  cudaStream_t stream);
 
+extern int g_stage_target;  // bytes per weight-stream ring stage
+
 // Device properties (cached).
 int sm_count();
+
+// Launch with (pdl) or without a programmatic dependency on the previous
+// kernel of the stream.
+cudaError_t launch_k(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     void** args, bool pdl);
 
 // Launch accounting: call with phase 0 just before a kernel launch and phase 1
 // just after it (see dv_profile / dv_launch_count).

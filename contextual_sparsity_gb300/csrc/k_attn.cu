@@ -31,6 +31,8 @@ struct SplitParams {
   const int32_t* dev_count;
   int k, h_kv, n, n_max, b_max, retained, C, S;
   float* part;  // [B][k][G][S][DH + 2]
+  float* H;     // [B][k][G][DH] combined head outputs
+  int* cnt;     // [B][k] splits finished per unit (zero between launches)
   int* st;
 };
 
@@ -47,16 +49,25 @@ DV_DEV void merge(float& m, float& l, float* o, float m2, float l2, const float*
   m = M;
 }
 
+// The CTA's contiguous K and V rows (at most kSplitMax keys) are brought into
+// shared memory by two 1-D bulk copies (one round trip to memory), then the
+// online softmax runs from shared memory.
+constexpr int kSplitMax = 128;
+
 template <int DH, int G>
 __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
   constexpr int LPK = DH / 8;        // lanes per key (8 dims each)
   constexpr int KPW = 32 / LPK;      // keys per warp step
-  constexpr int U = 4;               // unrolled steps
+  constexpr int U = 8;               // unrolled steps
   __shared__ float red[4][G][DH + 2];
+  __shared__ __align__(8) uint64_t kv_bar;
+  extern __shared__ __align__(128) uint16_t kv_smem[];  // [C][DH] K, then [C][DH] V
 
   const int s = blockIdx.x, e = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane % LPK, grp = lane / LPK;
+  pdl_wait();  // q and the new key/value come from the previous kernel
+  if (threadIdx.x == 0) pdl_launch_dependents();
 
   int kk = p.k;
   if (p.dev_count) kk = min(kk, *p.dev_count);
@@ -80,6 +91,29 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
   }
   const int t0 = s * p.C;
   const int t1 = min(count, t0 + p.C);
+  uint16_t* sK = kv_smem;
+  uint16_t* sV = kv_smem + (size_t)p.C * DH;
+  const uint32_t bytes = t1 > t0 ? (uint32_t)(t1 - t0) * DH * 2 : 0u;
+  if (threadIdx.x == 0) {
+    mbar_init(&kv_bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  bool staged = true;
+  if (bytes) {
+    if (threadIdx.x == 0) {
+      // K/V rows were written by generic stores (the new token, by the QKV
+      // kernel); order them before the async-proxy reads.
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      const uint64_t pol = policy_evict_first();
+      mbar_arrive_expect_tx(&kv_bar, 2 * bytes);
+      bulk_g2s(sK, Kb + (size_t)t0 * DH, bytes, &kv_bar, pol);
+      bulk_g2s(sV, Vb + (size_t)t0 * DH, bytes, &kv_bar, pol);
+    }
+    staged = mbar_wait(&kv_bar, 0);
+    if (!staged && (threadIdx.x & 31) == 0) flag(p.st, DV_DEV_TIMEOUT);
+  }
+  staged = __syncthreads_and(staged);
 
   float q[G][8];
 #pragma unroll
@@ -106,10 +140,10 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
 #pragma unroll
     for (int j = 0; j < U; ++j) {
       const int t = wbase + grp + j * step;
-      valid[j] = t < t1;
+      valid[j] = staged && t < t1;
       if (valid[j]) {
-        kv[j] = ld_nc_v4(Kb + (size_t)t * DH + sub * 8);
-        vv[j] = ld_nc_v4(Vb + (size_t)t * DH + sub * 8);
+        kv[j] = *reinterpret_cast<const uint4*>(sK + (size_t)(t - t0) * DH + sub * 8);
+        vv[j] = *reinterpret_cast<const uint4*>(sV + (size_t)(t - t0) * DH + sub * 8);
       } else {
         kv[j] = make_uint4(0, 0, 0, 0);
         vv[j] = kv[j];
@@ -198,13 +232,39 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
     }
     p.part[((((size_t)b * p.k + e) * G + g) * p.S + s) * (DH + 2) + c] = val;
   }
+  // The last split of this unit to finish combines all splits (no waiting:
+  // the others have already published their partials):
+  // H = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = (atomicAdd(&p.cnt[(size_t)b * p.k + e], 1) == p.S - 1);
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < G * DH; i += blockDim.x) {
+    const int g = i / DH, c = i % DH;
+    const float* base = p.part + ((((size_t)b * p.k + e) * G + g) * p.S) * (DH + 2);
+    float M = -INFINITY;
+    for (int t = 0; t < p.S; ++t) M = fmaxf(M, __ldcg(base + (size_t)t * (DH + 2)));
+    float L = 0.f, O = 0.f;
+    for (int t = 0; t < p.S; ++t) {
+      const float* ps = base + (size_t)t * (DH + 2);
+      const float mt = __ldcg(ps), lt = __ldcg(ps + 1);
+      const float w = (lt > 0.f) ? exp2f(mt - M) : 0.f;
+      L += w * lt;
+      O += w * __ldcg(ps + 2 + c);
+    }
+    p.H[(((size_t)b * p.k + e) * G + g) * DH + c] = L > 0.f ? O / L : 0.f;
+  }
+  if (threadIdx.x == 0) p.cnt[(size_t)b * p.k + e] = 0;
 }
 
 SplitPlan split_plan(int max_keys, int units, int B, int target_ctas) {
   SplitPlan pl;
   const long long want = std::max(1, target_ctas);
   long long per = ((long long)max_keys * units * B + want - 1) / want;
-  per = std::max<long long>(per, 64);
+  per = std::max<long long>(32, std::min<long long>(per, kSplitMax));
   per = (per + 31) / 32 * 32;
   pl.C = (int)per;
   pl.S = (int)((max_keys + per - 1) / per);
@@ -225,43 +285,21 @@ static void* splitk_fn(int G) {
 int launch_splitk(const float* q, int B, int dh, int G, int h_kv, const int32_t* idx, int k,
                   const int32_t* dev_count, const uint16_t* K, const uint16_t* V, int n, int n_max,
                   const uint16_t* Kr, const uint16_t* Vr, const int32_t* kept_count, int b_max,
-                  int retained, SplitPlan plan, float* part, int* st, cudaStream_t stream) {
+                  int retained, SplitPlan plan, float* part, float* H, int* cnt, int* st,
+                  cudaStream_t stream, bool pdl) {
   void* fn = dh == 128 ? splitk_fn<128>(G) : (dh == 64 ? splitk_fn<64>(G) : nullptr);
   if (!fn) return DV_ERR_UNSUPPORTED;
   SplitParams p{q, K, V, Kr, Vr, kept_count, idx, dev_count, k, h_kv, n, n_max, b_max,
-                retained, plan.C, plan.S, part, st};
+                retained, plan.C, plan.S, part, H, cnt, st};
   void* args[] = {&p};
+  const size_t smem = (size_t)2 * plan.C * dh * 2;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return DV_ERR_LAUNCH;
   note_launch(DV_TAG_SPLITK, 0, stream);
-  const cudaError_t e = cudaLaunchKernel(fn, dim3(plan.S, k, B), dim3(128), args, 0, stream);
+  const cudaError_t e = launch_k(fn, dim3(plan.S, k, B), dim3(128), smem, stream, args, pdl);
   note_launch(DV_TAG_SPLITK, 1, stream);
   return e == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
-}
-
-// Combine of the split partials into H [B][units*G][dh] (fp32).
-__global__ void k_combine(const float* __restrict__ part, int units, int G, int dh, int S,
-                          float* __restrict__ H) {
-  const int hq = blockIdx.x, b = blockIdx.y;  // query head slot = e*G + g
-  const float* base = part + (((size_t)b * units * G + hq) * S) * (dh + 2);
-  float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, base[(size_t)s * (dh + 2)]);
-  for (int c = threadIdx.x; c < dh; c += blockDim.x) {
-    float L = 0.f, O = 0.f;
-    for (int s = 0; s < S; ++s) {
-      const float* ps = base + (size_t)s * (dh + 2);
-      const float w = (ps[1] > 0.f) ? exp2f(ps[0] - M) : 0.f;
-      L += w * ps[1];
-      O += w * ps[2 + c];
-    }
-    H[((size_t)b * units * G + hq) * dh + c] = L > 0.f ? O / L : 0.f;
-  }
-}
-
-int launch_combine(const float* part, int B, int units, int G, int dh, int S, float* H,
-                   cudaStream_t stream) {
-  note_launch(DV_TAG_COMBINE, 0, stream);
-  k_combine<<<dim3(units * G, B), 128, 0, stream>>>(part, units, G, dh, S, H);
-  note_launch(DV_TAG_COMBINE, 1, stream);
-  return cudaGetLastError() == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
 }
 
 // ---------------------------------------------------------------------------

@@ -37,6 +37,9 @@ struct StreamGeom {
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
+// Rows per ring stage a consumer holds in registers: at most 8 vectors of 16 B.
+__host__ __device__ constexpr int rows_max(int V) { return V >= 8 ? 1 : 8 / V; }
+
 __host__ __device__ inline void stream_layout(StreamGeom& g) {
   const int nwc = g.T / 32;
   uint32_t off = g.NS * g.stage_bytes;
@@ -89,12 +92,17 @@ struct StreamParams {
   int b_max;
   uint16_t* y_side;
   uint32_t* kv_missing;
-  // P1
+  // predictor first layer: P1 rows streamed after the QKV rows (look-ahead,
+  // on the raw layer input) or alone (KIND_P1)
+  const uint16_t* P1;
+  int n_pred;             // P1 rows appended to a QKV launch
   float* u_out;           // [B][r]
   int relu;
-  // WO: split-K partials
-  const float* sk_part;   // [B][k][G][S][dh + 2]
-  int S;
+  // WO: combined head outputs [B][k][G][dh]
+  const float* Hc;
+  // QKV: split-K counters to clear for the attention launch that follows
+  int* zero_cnt;
+  int n_zero;
   // partial outputs
   float* part;            // [gridDim][B][d]
   int* st;
@@ -121,8 +129,13 @@ DV_DEV int rows_per_entry(const StreamParams& p, int kind) {
 // Global address of virtual row v of the launch's row list (phase: 0 dot
 // phase, 1 axpy phase). Out-of-range indices are replaced by row 0 and
 // reported; the consumers see coef 0 / discard the value.
-DV_DEV const uint16_t* row_addr(const StreamParams& p, int kind, int phase, int v, bool& bad) {
+DV_DEV const uint16_t* row_addr(const StreamParams& p, int kind, int phase, int v, int qkv_rows,
+                                bool& bad) {
   const size_t d = (size_t)p.d;
+  if (kind == KIND_QKV && v >= qkv_rows) {  // appended predictor rows
+    bad = false;
+    return p.P1 + (size_t)(v - qkv_rows) * d;
+  }
   if (kind == KIND_MLP || kind == KIND_P1) {
     int j = p.idx ? p.idx[v] : v;
     bad = (j < 0 || j >= p.n_rows_total);
@@ -151,11 +164,11 @@ template <int KIND, int B, int V>
 DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                     uint64_t* act_ready, float* red, float* coef, float* lnred, int* list,
                     volatile int* abort_flag, volatile int* list_count, const int kk,
-                    const int per, const int r0, const int nrows, const bool has_dot,
-                    const bool has_axpy, const bool skip);
+                    const int per, const int qkv_rows, const int r0, const int nrows,
+                    const bool has_dot, const bool has_axpy, const bool skip);
 
 template <int KIND, int B, int V>
-__global__ void __launch_bounds__(B == 1 ? 288 : 416, 1) k_stream(const StreamParams p) {
+__global__ void __launch_bounds__(B == 1 ? 544 : 416, 1) k_stream(const StreamParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const StreamGeom& g = p.g;
   const int T = g.T, nwc = T / 32;
@@ -175,7 +188,8 @@ __global__ void __launch_bounds__(B == 1 ? 288 : 416, 1) k_stream(const StreamPa
   // This CTA's slice of the selected entries.
   const int kk = eff_count(p);
   const int per = rows_per_entry(p, KIND);
-  const long long tot_rows = (long long)kk * per;
+  const int qkv_rows = (KIND == KIND_QKV) ? kk * per : 0;
+  const long long tot_rows = (long long)kk * per + (KIND == KIND_QKV ? p.n_pred : 0);
   const int r0 = (int)(tot_rows * blockIdx.x / gridDim.x);
   const int r1 = (int)(tot_rows * (blockIdx.x + 1) / gridDim.x);
   const int nrows = r1 - r0;
@@ -225,7 +239,7 @@ __global__ void __launch_bounds__(B == 1 ? 288 : 416, 1) k_stream(const StreamPa
           for (int c = 0; c < cnt; ++c) {
             const int local = (phase == 1 && skip) ? list[q0 + c] : (q0 + c);
             bool bad;
-            const uint16_t* src = row_addr(p, KIND, phase, r0 + local, bad);
+            const uint16_t* src = row_addr(p, KIND, phase, r0 + local, qkv_rows, bad);
             bad_any |= bad;
             bulk_g2s(smem + (size_t)s * g.stage_bytes + (size_t)c * g.row_bytes, src, g.row_bytes,
                      &full[s], pol);
@@ -240,7 +254,7 @@ __global__ void __launch_bounds__(B == 1 ? 288 : 416, 1) k_stream(const StreamPa
     __syncwarp();
   } else {
     consume<KIND, B, V>(p, smem, full, empty, act_ready, red, coef, lnred, list, abort_flag,
-                        list_count, kk, per, r0, nrows, has_dot, has_axpy, skip);
+                        list_count, kk, per, qkv_rows, r0, nrows, has_dot, has_axpy, skip);
   }
   // Both roles meet here once, with converged warps.
   __syncthreads();
@@ -251,14 +265,20 @@ template <int KIND, int B, int V>
 DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
                     uint64_t* act_ready, float* red, float* coef, float* lnred, int* list,
                     volatile int* abort_flag, volatile int* list_count, const int kk,
-                    const int per, const int r0, const int nrows, const bool has_dot,
-                    const bool has_axpy, const bool skip) {
+                    const int per, const int qkv_rows, const int r0, const int nrows,
+                    const bool has_dot, const bool has_axpy, const bool skip) {
   const StreamGeom& g = p.g;
   const int T = g.T, nwc = T / 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nvec = p.d >> 3;
+  constexpr int RM = rows_max(V);  // rows per stage held in registers
+  // The weight stream may already be running; activations and every global
+  // write wait until the previous kernel of the stream has completed.
+  pdl_wait();
+  if (tid == 0) pdl_launch_dependents();
   // Activation columns of this thread: vectors v_m = tid + m T (8 columns each).
   float z[B][V][8];
+  uint4 xraw[B][V];  // the raw fp16 input (predictor rows read y, not LN(y))
   int it = 0;
   if (has_dot) {
     // --- load x, optional LayerNorm ("Deja Vu" App. C.3: blocks read LN(y)).
@@ -271,8 +291,10 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         const int v = tid + m * T;
 #pragma unroll
         for (int e = 0; e < 8; ++e) z[b][m][e] = 0.f;
+        xraw[b][m] = make_uint4(0, 0, 0, 0);
         if (v < nvec && b < p.B) {
           uint4 xv = *reinterpret_cast<const uint4*>(p.x + (size_t)b * p.d + v * 8);
+          xraw[b][m] = xv;
           h8_to_f8(xv, z[b][m]);
 #pragma unroll
           for (int e = 0; e < 8; ++e) s1[b] += z[b][m][e];
@@ -345,7 +367,9 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
       }
     }
 
-    // --- dot phase: red[row][b][warp] = warp's share of z . W[row]
+    // --- dot phase: red[row][b][warp] = warp's share of z . W[row]. A warp
+    // copies its columns of the stage's rows into registers, releases the
+    // slot, then computes (the slot is held only for the shared-memory reads).
     for (int q0 = 0; q0 < nrows; q0 += g.R, ++it) {
       const int cnt = min(g.R, nrows - q0);
       const int s = it % g.NS;
@@ -357,25 +381,46 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         ok = false;
       }
       ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the row sums below shuffle
+      uint4 wv[RM][V];
       if (ok) {
-        for (int c = 0; c < cnt; ++c) {
-          const uint8_t* row = smem + (size_t)s * g.stage_bytes + (size_t)c * g.row_bytes;
-          float acc[B], cmp[B];
+        const uint8_t* st0 = smem + (size_t)s * g.stage_bytes;
 #pragma unroll
-          for (int b = 0; b < B; ++b) acc[b] = cmp[b] = 0.f;
+        for (int c = 0; c < RM; ++c)
 #pragma unroll
           for (int m = 0; m < V; ++m) {
             const int v = tid + m * T;
-            if (v < nvec) {
-              float w[8];
-              h8_to_f8(*reinterpret_cast<const uint4*>(row + v * 16), w);
+            wv[c][m] = (c < cnt && v < nvec)
+                           ? *reinterpret_cast<const uint4*>(st0 + (size_t)c * g.row_bytes + v * 16)
+                           : make_uint4(0, 0, 0, 0);
+          }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < RM; ++c) {
+          if (c >= cnt) break;
+          const bool raw = (KIND == KIND_QKV) && (r0 + q0 + c >= qkv_rows);
+          float acc[B];
+#pragma unroll
+          for (int b = 0; b < B; ++b) acc[b] = 0.f;
+#pragma unroll
+          for (int m = 0; m < V; ++m) {
+            float w[8];
+            h8_to_f8(wv[c][m], w);
+            if (raw) {
 #pragma unroll
               for (int b = 0; b < B; ++b) {
-                float t = 0.f;
+                float xf[8];
+                h8_to_f8(xraw[b][m], xf);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) t = fmaf(z[b][m][e], w[e], t);
-                kahan_add(acc[b], cmp[b], t);
+                for (int e = 0; e < 8; ++e) acc[b] = fmaf(xf[e], w[e], acc[b]);
               }
+            } else {
+#pragma unroll
+              for (int b = 0; b < B; ++b)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[b] = fmaf(z[b][m][e], w[e], acc[b]);
             }
           }
 #pragma unroll
@@ -385,8 +430,6 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
     }
     consumer_sync(T);
 
@@ -408,6 +451,12 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
             float u = val;
             if (p.relu && u < 0.f) u = 0.f;
             p.u_out[(size_t)b * p.n_rows_total + v] = u;
+          }
+        } else if (KIND == KIND_QKV && v >= qkv_rows) {
+          if (b < p.B) {
+            float u = val;
+            if (p.relu && u < 0.f) u = 0.f;
+            p.u_out[(size_t)b * p.n_pred + (v - qkv_rows)] = u;
           }
         } else if (KIND == KIND_QKV) {
           const int e = v / per, r = v % per;
@@ -434,6 +483,8 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         }
       }
     }
+    if (KIND == KIND_QKV && blockIdx.x == 0)
+      for (int i = tid; i < p.n_zero; i += T) p.zero_cnt[i] = 0;
     if (KIND == KIND_QKV && blockIdx.x == 0) {
       // Missing-KV bookkeeping ("Deja Vu" §4.2): keep a copy of y for the
       // units that did not get their k, v at this token.
@@ -478,29 +529,15 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
 
   if (has_axpy) {
     if (KIND == KIND_WO) {
-      // Combine the split-K partials of the heads this CTA touches:
-      // H = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
-      const int dh = p.dh;
+      // Coefficients: the combined attention output of each row's (head, dim).
       for (int i = tid; i < nrows * B; i += T) {
         const int li = i % nrows, b = i / nrows;
         const int v = r0 + li;
         const int e = v / per, r = v % per;  // r = g dh + c
-        const int gq = r / dh, c = r % dh;
         float H = 0.f;
         if (b < p.B) {
-          const float* base = p.sk_part + ((((size_t)b * p.k + e) * p.G + gq) * p.S) * (dh + 2);
-          float M = -INFINITY;
-          for (int s = 0; s < p.S; ++s) M = fmaxf(M, base[(size_t)s * (dh + 2)]);
-          float L = 0.f, O = 0.f;
-          for (int s = 0; s < p.S; ++s) {
-            const float* ps = base + (size_t)s * (dh + 2);
-            const float wgt = (ps[1] > 0.f) ? exp2f(ps[0] - M) : 0.f;
-            L += wgt * ps[1];
-            O += wgt * ps[2 + c];
-          }
-          H = L > 0.f ? O / L : 0.f;
           const int u = p.idx ? p.idx[e] : e;
-          if (u < 0 || u >= p.h_kv) H = 0.f;
+          if (u >= 0 && u < p.h_kv) H = p.Hc[((size_t)b * p.k + e) * per + r];
         }
         coef[b * g.CH + li] = H;
       }
@@ -524,30 +561,41 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         flag(p.st, DV_DEV_TIMEOUT);
         ok = false;
       }
-      ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the row sums below shuffle
+      ok = __all_sync(0xffffffffu, ok);
+      uint4 wv[RM][V];
       if (ok) {
-        for (int c = 0; c < cnt; ++c) {
+        const uint8_t* st0 = smem + (size_t)s * g.stage_bytes;
+#pragma unroll
+        for (int c = 0; c < RM; ++c)
+#pragma unroll
+          for (int m = 0; m < V; ++m) {
+            const int v = tid + m * T;
+            wv[c][m] = (c < cnt && v < nvec)
+                           ? *reinterpret_cast<const uint4*>(st0 + (size_t)c * g.row_bytes + v * 16)
+                           : make_uint4(0, 0, 0, 0);
+          }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < RM; ++c) {
+          if (c >= cnt) break;
           const int li = skip ? list[q0 + c] : (q0 + c);
-          const uint8_t* row = smem + (size_t)s * g.stage_bytes + (size_t)c * g.row_bytes;
           float a[B];
 #pragma unroll
           for (int b = 0; b < B; ++b) a[b] = coef[b * g.CH + li];
 #pragma unroll
           for (int m = 0; m < V; ++m) {
-            const int v = tid + m * T;
-            if (v < nvec) {
-              float w[8];
-              h8_to_f8(*reinterpret_cast<const uint4*>(row + v * 16), w);
+            float w[8];
+            h8_to_f8(wv[c][m], w);
 #pragma unroll
-              for (int b = 0; b < B; ++b)
+            for (int b = 0; b < B; ++b)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[b][m][e] = fmaf(a[b], w[e], acc[b][m][e]);
-            }
+              for (int e = 0; e < 8; ++e) acc[b][m][e] = fmaf(a[b], w[e], acc[b][m][e]);
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
     }
     // Partial output of this CTA.
 #pragma unroll
@@ -570,39 +618,53 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
 
 // ---------------------------------------------------------------------------
 // Fixed-order reduce of the CTA partials: out = x + bias + sum_g part[g].
+// A CTA covers 64 columns: 16 slices of 16 lanes, each lane a float4 of
+// columns; slice j sums partials j, j+16, ... with all its loads in flight,
+// then slice 0 adds the 16 slices in order.
 // ---------------------------------------------------------------------------
+constexpr int kRedSlices = 16;
+
 __global__ void __launch_bounds__(256) k_reduce(const float* __restrict__ part, int G, int B, int d,
                                                 const uint16_t* __restrict__ x,
                                                 const uint16_t* __restrict__ bias,
                                                 uint16_t* __restrict__ out) {
-  const int c4 = blockIdx.x * blockDim.x + threadIdx.x;  // group of 4 columns
+  __shared__ float4 sl[kRedSlices][16];
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  const int cg = threadIdx.x & 15, slice = threadIdx.x >> 4;
+  const int c4 = blockIdx.x * 16 + cg;  // group of 4 columns
   const int b = blockIdx.y;
-  if (c4 * 4 >= d) return;
+  const bool on = c4 * 4 < d;
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float* src = part + (size_t)b * d + c4 * 4;
-  const size_t stride = (size_t)B * d;
-  int gi = 0;
-  for (; gi + 4 <= G; gi += 4) {
-    float4 t0 = *reinterpret_cast<const float4*>(src + (gi + 0) * stride);
-    float4 t1 = *reinterpret_cast<const float4*>(src + (gi + 1) * stride);
-    float4 t2 = *reinterpret_cast<const float4*>(src + (gi + 2) * stride);
-    float4 t3 = *reinterpret_cast<const float4*>(src + (gi + 3) * stride);
-    s.x += t0.x; s.y += t0.y; s.z += t0.z; s.w += t0.w;
-    s.x += t1.x; s.y += t1.y; s.z += t1.z; s.w += t1.w;
-    s.x += t2.x; s.y += t2.y; s.z += t2.z; s.w += t2.w;
-    s.x += t3.x; s.y += t3.y; s.z += t3.z; s.w += t3.w;
+  if (on) {
+    const size_t stride = (size_t)B * d;
+    const float* src = part + (size_t)b * d + c4 * 4;
+    for (int g0 = slice; g0 < G; g0 += kRedSlices * 12) {
+      float4 t[12];
+#pragma unroll
+      for (int j = 0; j < 12; ++j) {
+        const int gi = g0 + kRedSlices * j;
+        t[j] = gi < G ? __ldcg(reinterpret_cast<const float4*>(src + gi * stride))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < 12; ++j) { s.x += t[j].x; s.y += t[j].y; s.z += t[j].z; s.w += t[j].w; }
+    }
   }
-  for (; gi < G; ++gi) {
-    float4 t = *reinterpret_cast<const float4*>(src + gi * stride);
-    s.x += t.x; s.y += t.y; s.z += t.z; s.w += t.w;
+  sl[slice][cg] = s;
+  __syncthreads();
+  if (slice != 0 || !on) return;
+  float r[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < kRedSlices; ++k) {
+    r[0] += sl[k][cg].x; r[1] += sl[k][cg].y; r[2] += sl[k][cg].z; r[3] += sl[k][cg].w;
   }
   const uint16_t* xr = x ? x + (size_t)b * d + c4 * 4 : nullptr;
-  float r[4] = {s.x, s.y, s.z, s.w};
   uint16_t o[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const float bb = bias ? h2f(bias[c4 * 4 + e]) : 0.f;
-    o[e] = f2h((x ? h2f(xr[e]) : 0.f) + (r[e] + bb));
+    o[e] = f2h((xr ? h2f(xr[e]) : 0.f) + (r[e] + bb));
   }
   uint2 pk;
   pk.x = (uint32_t)o[0] | ((uint32_t)o[1] << 16);
@@ -611,45 +673,82 @@ __global__ void __launch_bounds__(256) k_reduce(const float* __restrict__ part, 
 }
 
 // ---------------------------------------------------------------------------
-// Predictor second layer: scores[b][i] = sum_j u[b][j] P2[i][j] (rows of r).
-// One warp per row, 16-byte loads, Kahan-compensated per-lane sums.
+// Predictor GEMVs ("Deja Vu" §4.1 "Design": a small two-layer fully connected
+// network; low-rank chain y -> P1 -> r -> P2 -> scores). Dense, contiguous
+// rows, so plain 16-byte loads: one warp per row (two rows per step for short
+// rows), each lane keeping U independent loads in flight. These kernels are
+// small (256 threads, no dynamic shared memory) so that, launched on the side
+// stream, their CTAs fit next to a weight-streaming CTA on every SM.
+// out[b][row] = act(sum_c in[b][c] W[row][c]); `in` is fp16 (first layer) or
+// fp32 (second layer); Kahan-compensated per-lane sums of 8-term chunks.
 // ---------------------------------------------------------------------------
-template <int B>
-__global__ void __launch_bounds__(256) k_pred2(const float* __restrict__ u, int r,
-                                               const uint16_t* __restrict__ P2, int N,
-                                               float* __restrict__ scores, int ld, int nB) {
-  extern __shared__ __align__(16) float us[];  // [B][r]
-  for (int i = threadIdx.x; i < nB * r; i += blockDim.x) us[i] = u[i];
-  __syncthreads();
+template <typename TIn>
+DV_DEV void load_in8(const TIn* p, float* f);
+template <>
+DV_DEV void load_in8<uint16_t>(const uint16_t* p, float* f) {
+  h8_to_f8(*reinterpret_cast<const uint4*>(p), f);
+}
+template <>
+DV_DEV void load_in8<float>(const float* p, float* f) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+template <typename TIn, int B, int RPW>
+__global__ void __launch_bounds__(256) k_gemv(const TIn* __restrict__ in, int nB, int len,
+                                              const uint16_t* __restrict__ W, int N,
+                                              float* __restrict__ out, int ld, int relu) {
+  constexpr int U = 8;  // loads in flight per lane and row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
-  const int nv = r >> 3;
-  for (int row = blockIdx.x * nw + warp; row < N; row += gridDim.x * nw) {
-    const uint16_t* pr = P2 + (size_t)row * r;
-    float acc[B], cmp[B];
+  const int nv = len >> 3;
+  for (int row0 = (blockIdx.x * nw + warp) * RPW; row0 < N; row0 += gridDim.x * nw * RPW) {
+    float acc[RPW][B], cmp[RPW][B];
 #pragma unroll
-    for (int b = 0; b < B; ++b) acc[b] = cmp[b] = 0.f;
-    for (int v = lane; v < nv; v += 32) {
-      float w[8];
-      h8_to_f8(ld_nc_v4(pr + v * 8), w);
+    for (int q = 0; q < RPW; ++q)
 #pragma unroll
-      for (int b = 0; b < B; ++b) {
-        if (b < nB) {
-          const float* ub = us + b * r + v * 8;
-          float t = 0.f;
+      for (int b = 0; b < B; ++b) acc[q][b] = cmp[q][b] = 0.f;
+    for (int v0 = lane; v0 < nv; v0 += 32 * U) {
+      uint4 w[RPW][U];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) t = fmaf(ub[e], w[e], t);
-          kahan_add(acc[b], cmp[b], t);
+      for (int q = 0; q < RPW; ++q)
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          const int v = v0 + 32 * j;
+          const int row = row0 + q;
+          w[q][j] = (v < nv && row < N) ? ld_nc_v4(W + (size_t)row * len + v * 8)
+                                        : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const int v = v0 + 32 * j;
+        if (v >= nv) break;
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+          if (b >= nB) break;
+          float xin[8];
+          load_in8<TIn>(in + (size_t)b * len + v * 8, xin);
+#pragma unroll
+          for (int q = 0; q < RPW; ++q) {
+            float wf[8];
+            h8_to_f8(w[q][j], wf);
+            float t = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) t = fmaf(xin[e], wf[e], t);
+            kahan_add(acc[q][b], cmp[q][b], t);
+          }
         }
       }
     }
 #pragma unroll
-    for (int b = 0; b < B; ++b) {
-      if (b < nB) {
-        const float t = warp_sum(acc[b] - cmp[b]);
-        if (lane == 0) scores[(size_t)b * ld + row] = t;
+    for (int q = 0; q < RPW; ++q)
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        float t = warp_sum(acc[q][b] - cmp[q][b]);
+        if (relu && t < 0.f) t = 0.f;
+        if (lane == 0 && b < nB && row0 + q < N) out[(size_t)b * ld + row0 + q] = t;
       }
-    }
   }
 }
 
@@ -658,14 +757,16 @@ __global__ void __launch_bounds__(256) k_pred2(const float* __restrict__ u, int 
 // ---------------------------------------------------------------------------
 static int pick_V(int nvec, int tmax) { return (nvec + tmax - 1) / tmax; }
 
+int g_stage_target = 48 * 1024;  // bytes per ring stage (rows are grouped up to this)
+
 static bool make_geom(StreamGeom& g, int d, int B, int ring_budget, int CH) {
   const int nvec = d / 8;
-  const int tmax = (B == 1) ? 256 : 384;
+  const int tmax = (B == 1) ? 512 : 384;
   const int V = pick_V(nvec, tmax);
   g.T = ((nvec + V - 1) / V + 31) / 32 * 32;
   g.B = B;
   g.row_bytes = (uint32_t)d * 2;
-  g.R = std::max(1, (int)(16384 / g.row_bytes));
+  g.R = std::min(rows_max(V == 7 ? 8 : V), std::max(1, (int)(g_stage_target / g.row_bytes)));
   g.stage_bytes = g.R * g.row_bytes;
   g.NS = std::min(16, ring_budget / (int)g.stage_bytes);
   if (g.NS < 2) g.NS = 2;
@@ -701,17 +802,17 @@ int stream_ctas_max(int CH_rows, long long rows, int target) {
 }
 
 static int launch_stream(int kind, StreamParams& p, long long rows, int target_ctas,
-                         int ring_budget, cudaStream_t stream, int* grid_out) {
+                         int ring_budget, cudaStream_t stream, int* grid_out, bool pdl) {
   const int Bt = p.B == 1 ? 1 : 4;
-  const int CH = (Bt == 1) ? 512 : 256;
+  const int CH = 256;
   if (!make_geom(p.g, p.d, Bt, ring_budget, CH)) return DV_ERR_UNSUPPORTED;
-  const int V = pick_V(p.d / 8, Bt == 1 ? 256 : 384);
+  const int V = pick_V(p.d / 8, Bt == 1 ? 512 : 384);
   void* fn = nullptr;
   switch (kind) {
     case KIND_MLP: fn = stream_kernel<KIND_MLP>(Bt, V); break;
     case KIND_QKV: fn = stream_kernel<KIND_QKV>(Bt, V); break;
-    case KIND_P1: fn = stream_kernel<KIND_P1>(Bt, V); break;
     case KIND_WO: fn = stream_kernel<KIND_WO>(Bt, V); break;
+    case KIND_P1: fn = stream_kernel<KIND_P1>(Bt, V); break;
   }
   if (!fn) return DV_ERR_UNSUPPORTED;
   int grid = stream_ctas_max(CH, rows, target_ctas);
@@ -723,19 +824,19 @@ static int launch_stream(int kind, StreamParams& p, long long rows, int target_c
   void* args[] = {&p};
   static const int tags[4] = {DV_TAG_MLP, DV_TAG_QKV, DV_TAG_PRED1, DV_TAG_WO};
   note_launch(tags[kind], 0, stream);
-  const cudaError_t e = cudaLaunchKernel(fn, dim3(grid), dim3(p.g.T + 32), args, p.g.total, stream);
+  const cudaError_t e = launch_k(fn, dim3(grid), dim3(p.g.T + 32), p.g.total, stream, args, pdl);
   note_launch(tags[kind], 1, stream);
   return e == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
 }
 
 int reduce_launch(const float* part, int G, int B, int d, const uint16_t* x, const uint16_t* bias,
                   uint16_t* out, cudaStream_t stream) {
-  const int groups = d / 4;
-  dim3 grid((groups + 255) / 256, B);
+  dim3 grid((d + 63) / 64, B);
+  void* args[] = {&part, &G, &B, &d, &x, &bias, &out};
   note_launch(DV_TAG_REDUCE, 0, stream);
-  k_reduce<<<grid, 256, 0, stream>>>(part, G, B, d, x, bias, out);
+  const cudaError_t e = launch_k((const void*)k_reduce, grid, dim3(256), 0, stream, args, true);
   note_launch(DV_TAG_REDUCE, 1, stream);
-  return cudaGetLastError() == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
+  return e == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
 }
 
 // ---- public launchers (declared in dv_internal.h) -------------------------
@@ -744,14 +845,14 @@ int launch_mlp(const uint16_t* x, int B, int d, int F, const uint16_t* ln_g, con
                float eps, const uint16_t* fc1, const uint16_t* b1, const uint16_t* fc2T,
                const uint16_t* b2, const int32_t* idx, int k, const int32_t* dev_count, int flags,
                uint16_t* out, int* st, float* part, int target_ctas, int ring_budget,
-               cudaStream_t stream) {
+               cudaStream_t stream, bool pdl) {
   const uint16_t* resid = (flags & DV_NO_RESIDUAL) ? nullptr : x;
   StreamParams p{};
   p.d = d; p.B = B; p.x = x; p.ln_g = ln_g; p.ln_b = ln_b; p.eps = eps;
   p.W0 = fc1; p.W1 = fc2T; p.bias0 = b1; p.idx = idx; p.k = k; p.dev_count = dev_count;
   p.n_rows_total = F; p.flags = flags; p.part = part; p.st = st;
   int grid = 0;
-  int rc = launch_stream(KIND_MLP, p, k, target_ctas, ring_budget, stream, &grid);
+  int rc = launch_stream(KIND_MLP, p, k, target_ctas, ring_budget, stream, &grid, pdl);
   if (rc != DV_OK) return rc;
   return reduce_launch(part, grid, B, d, resid, b2, out, stream);
 }
@@ -762,59 +863,70 @@ int launch_qkv(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const u
                const int32_t* idx, int k, const int32_t* dev_count, float scale, float* qbuf,
                uint16_t* K, uint16_t* V, int n, int n_max, uint16_t* Kr, uint16_t* Vr,
                const int32_t* kept_count, int b_max, uint16_t* y_side, uint32_t* kv_missing,
-               int* st, int target_ctas, int ring_budget, cudaStream_t stream) {
+               int* zero_cnt, int n_zero, const uint16_t* P1, int n_pred, int relu, float* u_out,
+               int* st, int target_ctas, int ring_budget, cudaStream_t stream, bool pdl) {
   StreamParams p{};
+  p.zero_cnt = zero_cnt; p.n_zero = n_zero;
+  p.P1 = P1; p.n_pred = P1 ? n_pred : 0; p.relu = relu; p.u_out = u_out;
   p.d = d; p.B = B; p.x = x; p.ln_g = ln_g; p.ln_b = ln_b; p.eps = eps;
   p.W0 = Wq; p.W1 = Wk; p.W2 = Wv; p.bias0 = bq; p.bias1 = bk; p.bias2 = bv;
   p.idx = idx; p.k = k; p.dev_count = dev_count; p.G = G; p.dh = dh; p.h_kv = h_kv;
   p.scale = scale; p.qbuf = qbuf; p.K = K; p.V = V; p.n = n; p.n_max = n_max;
   p.Kr = Kr; p.Vr = Vr; p.kept_count = kept_count; p.b_max = b_max;
   p.y_side = y_side; p.kv_missing = kv_missing; p.st = st;
-  return launch_stream(KIND_QKV, p, (long long)k * (G + 2) * dh, target_ctas, ring_budget, stream,
-                       nullptr);
+  return launch_stream(KIND_QKV, p, (long long)k * (G + 2) * dh + p.n_pred, target_ctas,
+                       ring_budget, stream, nullptr, pdl);
 }
 
 int launch_wo(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const uint16_t* WoT,
               const uint16_t* bo, const int32_t* idx, int k, const int32_t* dev_count,
-              const float* sk_part, int S, uint16_t* out, int* st, float* part, int target_ctas,
+              const float* H, uint16_t* out, int* st, float* part, int target_ctas,
               int ring_budget, cudaStream_t stream) {
   // x: residual added by the reduce (NULL: none)
   StreamParams p{};
   p.d = d; p.B = B; p.x = x; p.W0 = WoT; p.idx = idx; p.k = k; p.dev_count = dev_count;
-  p.G = G; p.dh = dh; p.h_kv = h_kv; p.sk_part = sk_part; p.S = S; p.part = part; p.st = st;
+  p.G = G; p.dh = dh; p.h_kv = h_kv; p.Hc = H; p.part = part; p.st = st;
   int grid = 0;
   int rc = launch_stream(KIND_WO, p, (long long)k * G * dh, target_ctas, ring_budget, stream,
-                         &grid);
+                         &grid, true);
   if (rc != DV_OK) return rc;
   return reduce_launch(part, grid, B, d, x, bo, out, stream);
+}
+
+// Second predictor layer: scores[b][row] = sum_j u[b][j] P2[row][j].
+int launch_pred2(const float* u, int B, int r, const uint16_t* P2, int N, float* scores, int ld,
+                 int target_ctas, cudaStream_t stream) {
+  const int threads = 256, nw = threads / 32;
+  const int g2 = std::max(1, std::min(target_ctas, (N + 2 * nw - 1) / (2 * nw)));
+  note_launch(DV_TAG_PRED2, 0, stream);
+  if (B == 1)
+    k_gemv<float, 1, 2><<<g2, threads, 0, stream>>>(u, B, r, P2, N, scores, ld, 0);
+  else
+    k_gemv<float, 4, 2><<<g2, threads, 0, stream>>>(u, B, r, P2, N, scores, ld, 0);
+  note_launch(DV_TAG_PRED2, 1, stream);
+  return cudaGetLastError() == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
+}
+
+// Both predictor layers: P1 streamed by the weight-streaming engine (dense
+// rows, raw input, no LayerNorm), then the second layer.
+int launch_pred1(const uint16_t* y, int B, int d, const uint16_t* P1, int r, int relu, float* u,
+                 int target_ctas, int ring_budget, cudaStream_t stream) {
+  StreamParams p{};
+  p.d = d; p.B = B; p.x = y; p.W0 = P1; p.idx = nullptr; p.k = r; p.n_rows_total = r;
+  p.u_out = u; p.relu = relu; p.n_pred = r;
+  return launch_stream(KIND_P1, p, r, target_ctas, ring_budget, stream, nullptr, false);
 }
 
 int launch_predict(const uint16_t* y, int B, int d, const uint16_t* P1, int r,
                    const uint16_t* P2, int N, int relu, float* scores, int ld, float* u,
                    int target_ctas, int ring_budget, cudaStream_t stream) {
-  StreamParams p{};
-  p.d = d; p.B = B; p.x = y; p.W0 = P1; p.idx = nullptr; p.k = r; p.n_rows_total = r;
-  p.u_out = u; p.relu = relu;
-  int rc = launch_stream(KIND_P1, p, r, target_ctas, ring_budget, stream, nullptr);
+  int rc = launch_pred1(y, B, d, P1, r, relu, u, target_ctas, ring_budget, stream);
   if (rc != DV_OK) return rc;
-  const int threads = 256, nw = threads / 32;
-  int grid = std::min((N + nw - 1) / nw, std::max(1, target_ctas));
-  const size_t smem = (size_t)B * r * sizeof(float);
-  if (smem > 48 * 1024) {
-    cudaFuncSetAttribute(k_pred2<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    cudaFuncSetAttribute(k_pred2<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  }
-  note_launch(DV_TAG_PRED2, 0, stream);
-  if (B == 1)
-    k_pred2<1><<<grid, threads, smem, stream>>>(u, r, P2, N, scores, ld, B);
-  else
-    k_pred2<4><<<grid, threads, smem, stream>>>(u, r, P2, N, scores, ld, B);
-  note_launch(DV_TAG_PRED2, 1, stream);
-  return cudaGetLastError() == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
+  return launch_pred2(u, B, r, P2, N, scores, ld, target_ctas, stream);
 }
 
 size_t stream_part_bytes(int d, int B, long long max_rows, int target_ctas) {
-  const int CH = (B == 1) ? 512 : 256;
+  const int CH = 256;
   const int grid = stream_ctas_max(CH, max_rows, target_ctas);
   return (size_t)grid * B * d * sizeof(float);
 }

@@ -84,7 +84,7 @@ def lib():
         L.dv_status_string.argtypes = [_i]
         L.dv_workspace_size.restype = _sz
         L.dv_workspace_size.argtypes = [ctypes.POINTER(Dims), _i, _i]
-        L.dv_set_tuning.argtypes = [_i, _i, _i, _i, _i]
+        L.dv_set_tuning.argtypes = [_i, _i, _i, _i, _i, _i, _i]
         L.dv_predict.argtypes = [_p, _i, _i, _p, _i, _p, _i, _i, _p, _p, _sz, _p]
         L.dv_select_topk.argtypes = [_p, _i, _i, _i, _i, _p, _p, _p, _p, _p, _sz, _p]
         L.dv_sparse_mlp.argtypes = [_p, _i, ctypes.POINTER(Dims), ctypes.POINTER(LayerWeights),
@@ -172,9 +172,10 @@ def workspace(D: Dims, B=1, flags=0, device="cuda"):
     return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def set_tuning(main_ctas=0, side_ctas=16, main_ring_kb=160, side_ring_kb=32, attn_ctas=0):
-    _check(lib().dv_set_tuning(main_ctas, side_ctas, main_ring_kb, side_ring_kb, attn_ctas),
-           "dv_set_tuning")
+def set_tuning(main_ctas=0, side_ctas=0, main_ring_kb=160, side_ring_kb=32, attn_ctas=0, pdl=1,
+               stage_kb=48):
+    _check(lib().dv_set_tuning(main_ctas, side_ctas, main_ring_kb, side_ring_kb, attn_ctas, pdl,
+                               stage_kb), "dv_set_tuning")
 
 
 # ---------------------------------------------------------------------------

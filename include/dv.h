@@ -151,10 +151,14 @@ size_t dv_workspace_size(const dv_dims* dims, int B, int flags);
 
 /* Launch-shape tuning (aux, process-wide; the defaults need no call): CTAs of
  * the weight-streaming kernels (0: one per SM), CTAs of the side-stream
- * predictor (>= 1), shared-memory ring budgets in KB (main 16..200, side
- * 8..200), split-K CTA target (0: four per SM). DV_OK or DV_ERR_DIMS. */
+ * predictor (0: two per SM), shared-memory ring budgets in KB (main 16..200, side
+ * 8..200), split-K CTA target (0: two per SM), and whether consecutive kernels
+ * of one call use programmatic dependent launch (pdl != 0, the default: the
+ * next kernel's weight stream starts while the previous kernel drains), and the
+ * target size in KB of one weight-stream ring stage (4..100; rows are grouped
+ * up to it). DV_OK or DV_ERR_DIMS. */
 int dv_set_tuning(int main_ctas, int side_ctas, int main_ring_kb, int side_ring_kb,
-                  int attn_ctas);
+                  int attn_ctas, int pdl, int stage_kb);
 
 /* Kernel-launch accounting (aux). dv_profile(events, tags, cap): from now on
  * every kernel launch of the library is bracketed by two cudaEventRecord calls
