@@ -110,7 +110,7 @@ def lib():
 EXPORTED = ["dv_version", "dv_status_string", "dv_workspace_size", "dv_set_tuning", "dv_profile",
             "dv_launch_count", "dv_predict",
             "dv_select_topk", "dv_sparse_mlp", "dv_sparse_attn", "dv_kv_select_attn",
-            "dv_decode_layer", "dv_decode_step"]
+            "dv_decode_layer", "dv_decode_step", "dv_sparse_mlp_noalloc"]
 
 
 def status_string(code: int) -> str:
