@@ -138,7 +138,7 @@ static WsLayout ws_layout(const dv_dims* D, int B, int flags) {
   off += al((size_t)B * D->h_kv * G * L.S_max * (D->d_h + 2) * 4);
   L.hcomb = off;
   off += al((size_t)B * D->h * D->d_h * 4);
-  L.cnt = off;
+  L.cnt = off;  // split-K counters [B][h_kv]
   off += al((size_t)B * D->h_kv * 4);
   L.hmid = off;
   off += al((size_t)B * D->d * 2);
@@ -534,12 +534,12 @@ int dv_decode_layer(const dv_dims* dims, const dv_keep* keep, int B, const dv_la
     if (rc != DV_OK) return rc;
     if (cudaEventRecord(ev_join, side) != cudaSuccess) return DV_ERR_LAUNCH;
   }
-  rc = attn_rest(y_in, B, dims, w, selH, kHe, cntH, kv, n, flags, hmid, dev_status, ws, L, main);
-  if (rc != DV_OK) return rc;
-  // MLP block: y' = h + MLP_{S_M}(h).
   const int32_t* selN = nd ? nullptr : (B == 1 ? cur->idx_N : cur->uN);
   const int32_t* cntN = (nd || B == 1) ? nullptr : cur->ucnt;
   const int kNe = (nd || B == 1) ? kN : std::min(dims->F, B * kN);
+  rc = attn_rest(y_in, B, dims, w, selH, kHe, cntH, kv, n, flags, hmid, dev_status, ws, L, main);
+  if (rc != DV_OK) return rc;
+  // MLP block: y' = h + MLP_{S_M}(h).
   rc = run_mlp(hmid, B, dims, w, selN, kNe, cntN, flags, y_out, dev_status, ws, L, main, true);
   if (rc != DV_OK) return rc;
   return launch_status();

@@ -110,11 +110,8 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
       bulk_g2s(sK, Kb + (size_t)t0 * DH, bytes, &kv_bar, pol);
       bulk_g2s(sV, Vb + (size_t)t0 * DH, bytes, &kv_bar, pol);
     }
-    staged = mbar_wait(&kv_bar, 0);
-    if (!staged && (threadIdx.x & 31) == 0) flag(p.st, DV_DEV_TIMEOUT);
   }
-  staged = __syncthreads_and(staged);
-
+  // The queries load while the bulk copies are in flight.
   float q[G][8];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -122,6 +119,12 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) q[g][i] = qs[i] * kLog2e;
   }
+  if (bytes) {
+    staged = mbar_wait(&kv_bar, 0);
+    if (!staged && (threadIdx.x & 31) == 0) flag(p.st, DV_DEV_TIMEOUT);
+  }
+  staged = __syncthreads_and(staged);
+
   float m[G], l[G], o[G][8];
 #pragma unroll
   for (int g = 0; g < G; ++g) {

@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(const float* __restrict__
 constexpr int kClusterTopk = 8;
 
 template <int KPT>
-__global__ void __cluster_dims__(kClusterTopk, 1, 1) __launch_bounds__(256)
+__global__ void __cluster_dims__(kClusterTopk, 1, 1) __launch_bounds__(256, 4)
     k_topk_cluster(const float* __restrict__ scores, int ld, int N, int k,
                    int32_t* __restrict__ idx, int ld_idx, int* st) {
   cg::cluster_group cluster = cg::this_cluster();

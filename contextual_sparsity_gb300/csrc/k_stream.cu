@@ -696,10 +696,11 @@ DV_DEV void load_in8<float>(const float* p, float* f) {
 }
 
 template <typename TIn, int B, int RPW>
-__global__ void __launch_bounds__(256) k_gemv(const TIn* __restrict__ in, int nB, int len,
+__global__ void __launch_bounds__(256, 4) k_gemv(const TIn* __restrict__ in, int nB, int len,
                                               const uint16_t* __restrict__ W, int N,
                                               float* __restrict__ out, int ld, int relu) {
-  constexpr int U = 8;  // loads in flight per lane and row
+  constexpr int U = 4;  // loads in flight per lane and row (64 registers: fits next to a
+                        // weight-streaming CTA on the same SM)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nw = blockDim.x >> 5;
   const int nv = len >> 3;

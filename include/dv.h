@@ -152,7 +152,7 @@ size_t dv_workspace_size(const dv_dims* dims, int B, int flags);
 /* Launch-shape tuning (aux, process-wide; the defaults need no call): CTAs of
  * the weight-streaming kernels (0: one per SM), CTAs of the side-stream
  * predictor (0: two per SM), shared-memory ring budgets in KB (main 16..200, side
- * 8..200), split-K CTA target (0: two per SM), and whether consecutive kernels
+ * 8..200), split-K CTA target (0: two per SM), whether consecutive kernels
  * of one call use programmatic dependent launch (pdl != 0, the default: the
  * next kernel's weight stream starts while the previous kernel drains), and the
  * target size in KB of one weight-stream ring stage (4..100; rows are grouped
