@@ -391,8 +391,7 @@ def run_ours(a):
     # (r rows of d) when predicting ahead
     p1_rows = w.r if (lookahead and (w.keep_N < 1 or w.keep_H < 1) and w.layers > 1) else 0
     algo = {
-        "qkv": traffic.qkv_bytes(w.d, G, w.dh, m.kH) + traffic.pred_bytes(w.d, p1_rows, 0)
-        if p1_rows else traffic.qkv_bytes(w.d, G, w.dh, m.kH),
+        "qkv": traffic.qkv_bytes(w.d, G, w.dh, m.kH) + traffic.p1_bytes(w.d, p1_rows),
         "wo": traffic.wo_bytes(w.d, G, w.dh, m.kH),
         "mlp": traffic.mlp_bytes(w.d, m.kN),
         "splitk": traffic.kv_bytes(w.dh, m.kH, w.n + 1),

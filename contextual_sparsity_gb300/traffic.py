@@ -36,6 +36,11 @@ def kv_bytes(dh, units, keys):
     return units * 2 * dh * keys * E
 
 
+def p1_bytes(d, r):
+    """The predictor's first layer P1 [r][d]."""
+    return r * d * E
+
+
 def pred_bytes(d, r, rows):
     return 0 if rows == 0 else r * (d + rows) * E
 
