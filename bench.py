@@ -49,7 +49,10 @@ def parse():
     ap.add_argument("--keep-h", type=float, default=None)
     ap.add_argument("--layers", type=int, default=None)
     ap.add_argument("--n", type=int, default=None, help="cached tokens")
+    ap.add_argument("--batch", type=int, default=None, help="sequences per step (1..4)")
     ap.add_argument("--sync", action="store_true", help="no look-ahead (predict each layer first)")
+    ap.add_argument("--kv-dense", action="store_true",
+                    help="composition workload: read the full cache (dense split-K baseline)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -71,13 +74,16 @@ def workload(a):
         over["layers"] = a.layers
     if a.n is not None:
         over["n"] = a.n
+    if a.batch is not None:
+        over["B"] = a.batch
     return synth.workload(a.workload, **over)
 
 
 def workload_name(w, lookahead=True):
+    kv = f", KV keep {w.keep_KV:g}" if w.keep_KV < 1 else ""
     return (f"{w.name} (d {w.d}, {w.h}/{w.h_kv} heads x {w.dh}, FFN {w.F}, rank {w.r}, "
-            f"{w.layers} layers, n {w.n}), neuron keep {w.keep_N:g}, head keep {w.keep_H:g}, "
-            f"batch {w.B}, {'look-ahead' if lookahead else 'sync'} prediction")
+            f"{w.layers} layers, n {w.n}), neuron keep {w.keep_N:g}, head keep {w.keep_H:g}"
+            f"{kv}, batch {w.B}, {'look-ahead' if lookahead else 'sync'} prediction")
 
 
 # ---------------------------------------------------------------------------
@@ -179,13 +185,13 @@ class ClockSampler:
 # the workload on the GPU
 # ---------------------------------------------------------------------------
 class Model:
-    def __init__(self, w, device, lookahead=True, seed=0):
+    def __init__(self, w, device, lookahead=True, seed=0, kv_dense=False):
         self.w = w
         self.L = w.layers
         self.n = w.n
         self.n_max = w.n + 8
         self.D = dv.dims(w.d, w.h, w.h_kv, w.dh, w.F, w.r, self.n_max)
-        self.keep = dv.Keep(w.keep_N, w.keep_H, 1.0)
+        self.keep = dv.Keep(w.keep_N, w.keep_H, w.keep_KV)
         self.kN = traffic.k_of(w.keep_N, w.F)
         self.kH = traffic.k_of(w.keep_H, w.h_kv)
         self.W = [synth.layer_weights(w, l, seed=seed, device=device) for l in range(self.L)]
@@ -194,9 +200,43 @@ class Model:
             k, v = synth.kv_cache(w, l, self.n_max, seed=seed, device=device)
             self.K.append(k)
             self.V.append(v)
-        self.kvs = [dv.kv_cache(self.K[l], self.V[l]) for l in range(self.L)]
+        # Composition with attention-scored KV selection: the scoring pass runs
+        # once per layer (prefill time); every decode step then reads the
+        # retained buffer through the same split-K kernel.
+        self.retained = w.keep_KV < 1.0 and not kv_dense
+        self.kv_flags = dv.DV_KV_RETAINED if self.retained else 0
+        self.select_ms = None
+        self.keys = w.n + 1
+        flags_ws = dv.DV_KV_RESELECT if self.retained else 0
+        self.ws = dv.workspace(self.D, w.B, flags_ws)
+        if self.retained:
+            self.b = int(w.n * w.keep_KV + 1e-9)
+            self.b_max = self.b + 8
+            self.keys = self.b + 1
+            self.Kr, self.Vr, self.kp, self.kc, self.kvs = [], [], [], [], []
+            qd = torch.zeros(w.h, w.dh, device=device)
+            Hd = torch.zeros(w.h, w.dh, device=device)
+            e0, e1 = dv.event(True), dv.event(True)
+            e0.record()
+            for l in range(self.L):
+                Kr = torch.empty(w.h_kv, self.b_max, w.dh, dtype=torch.float16, device=device)
+                Vr = torch.empty_like(Kr)
+                kp = torch.zeros(w.h_kv, self.b_max, dtype=torch.int32, device=device)
+                kc = torch.zeros(w.h_kv, dtype=torch.int32, device=device)
+                kv = dv.kv_cache(self.K[l], self.V[l], Kr=Kr, Vr=Vr, kept_pos=kp, kept_count=kc,
+                                 b_max=self.b_max)
+                q_obs = synth.obs_queries(w, l, seed=seed, device=device)
+                dv.kv_select_attn(qd, self.D, kv, w.n, Hd, self.ws, q_obs=q_obs,
+                                  obs_window=w.obs_window, n_sinks=w.n_sinks, smooth=w.smooth,
+                                  kv_keep=w.keep_KV, flags=dv.DV_KV_RESELECT)
+                self.Kr.append(Kr); self.Vr.append(Vr); self.kp.append(kp); self.kc.append(kc)
+                self.kvs.append(kv)
+            e1.record()
+            torch.cuda.synchronize()
+            self.select_ms = e0.elapsed_time(e1)
+        else:
+            self.kvs = [dv.kv_cache(self.K[l], self.V[l]) for l in range(self.L)]
         self.sets = [dv.sets(w.B, w.F, w.h_kv, self.kN, self.kH, device=device) for _ in range(2)]
-        self.ws = dv.workspace(self.D, w.B)
         self.x = synth.hidden(w, seed=seed, device=device)
         self.y_tmp = torch.empty(2, w.B, w.d, dtype=torch.float16, device=device)
         self.y_out = torch.empty(w.B, w.d, dtype=torch.float16, device=device)
@@ -204,7 +244,7 @@ class Model:
         self.evf = dv.event()
         self.evj = dv.event()
         self.st = torch.zeros(1, dtype=torch.int32, device=device)
-        flags = dv.DV_LOOKAHEAD if lookahead else 0
+        flags = (dv.DV_LOOKAHEAD if lookahead else 0) | self.kv_flags
         self.step = dv.Step(self.D, self.keep, self.W, self.kvs, [s for s, _ in self.sets],
                             self.ws, flags, self.side, self.evf, self.evj, dev_status=self.st)
 
@@ -334,7 +374,7 @@ def run_ours(a):
         dv.set_tuning(*[int(x) for x in a.tuning.split(",")])
     w = workload(a)
     lookahead = not a.sync
-    m = Model(w, dev, lookahead=lookahead)
+    m = Model(w, dev, lookahead=lookahead, kv_dense=a.kv_dense)
     stream = torch.cuda.Stream(device=dev)
     g, per_step = m.capture(stream)
     torch.cuda.synchronize()
@@ -358,7 +398,7 @@ def run_ours(a):
     us_layer = ms_step * 1e3 / w.layers
     assert m.st.item() == 0, f"device status {m.st.item()}"
 
-    sel, pred = traffic.layer_bytes(w)
+    sel, pred = traffic.layer_bytes(w, keys=m.keys)
     gbs_sel = sel / (us_layer * 1e-6) / 1e9
     gbs_all = (sel + pred) / (us_layer * 1e-6) / 1e9
     print(f"[bench] {us_layer:.2f} us/layer, {gbs_sel:.0f} GB/s selected, {gbs_all:.0f} GB/s all, "
@@ -394,7 +434,7 @@ def run_ours(a):
         "qkv": traffic.qkv_bytes(w.d, G, w.dh, m.kH) + traffic.p1_bytes(w.d, p1_rows),
         "wo": traffic.wo_bytes(w.d, G, w.dh, m.kH),
         "mlp": traffic.mlp_bytes(w.d, m.kN),
-        "splitk": traffic.kv_bytes(w.dh, m.kH, w.n + 1),
+        "splitk": traffic.kv_bytes(w.dh, m.kH, m.keys),
     }
     totals = {k: sum(v) for k, v in per_kind.items()}
     dom = max(algo, key=lambda k: totals.get(k, 0.0))
@@ -456,6 +496,9 @@ def run_ours(a):
                    "l2": "inputs larger than L2 (every step streams ~"
                          f"{(sel + pred) * w.layers / 1e9:.1f} GB)"},
         "selected_bytes_per_layer": sel, "predictor_bytes_per_layer": pred,
+        "kv": ({"mode": "retained", "keep": w.keep_KV, "budget": m.b, "keys_read": m.keys,
+                "selection_ms_all_layers": round(m.select_ms, 3)} if m.retained else
+               {"mode": "full cache", "keys_read": m.keys}),
         "gbs_selected": round(gbs_sel, 1), "frac_of_8tbs_selected": round(gbs_sel / NOMINAL_HBM, 4),
         "gbs_all_traffic": round(gbs_all, 1),
         "frac_of_measured_hbm_selected": round(gbs_sel / peak, 4),

@@ -1,0 +1,113 @@
+"""Parity at the workloads' full sizes, in the launch configuration the
+benchmark times: the whole L-layer stack on the GPU (seeded weights drawn on
+the device), one decode step replayed from its captured CUDA graph with the
+look-ahead predictor on the side stream. The last layer is then checked
+against the oracle, teacher-forced: its input y_{L-1} and its index sets come
+from the GPU; the sets are checked against the oracle's predictor scores on
+y_{L-2} (the look-ahead input), and the layer output against the oracle layer.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bench
+import oracle
+from contextual_sparsity_gb300 import dv, synth
+from gpu_helpers import TOL, check_sets, np16, npf, rel_err, setup_lib
+
+pytestmark = pytest.mark.gpu
+
+
+def _step(w, kv_dense=False):
+    setup_lib()
+    dv.set_tuning()
+    m = bench.Model(w, torch.device("cuda", 0), lookahead=True, kv_dense=kv_dense)
+    s = torch.cuda.Stream()
+    g, _ = m.capture(s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert m.st.item() == 0, m.st.item()
+    return m
+
+
+def _check_last_layer(m, kv_sel=None):
+    w, L = m.w, m.L
+    y_prev = m.y_tmp[(L - 3) & 1] if L >= 3 else m.x          # y_{L-2}
+    y_in = m.y_tmp[(L - 2) & 1] if L >= 2 else m.x            # y_{L-1}
+    sets_t = m.sets[(L - 1) & 1][1]
+    Wh = {k: np16(v) for k, v in m.W[L - 1].items()}
+    for b in range(w.B):
+        ref = oracle.predict(np16(y_prev[b]), Wh["P1"], Wh["P2"])
+        if w.keep_N < 1:
+            check_sets(sets_t["idx_N"][b].cpu().numpy(), ref[: w.F], m.kN)
+        if w.keep_H < 1:
+            check_sets(sets_t["idx_H"][b].cpu().numpy(), ref[w.F:], m.kH)
+    if w.B == 1:
+        selN = sets_t["idx_N"][0].cpu().numpy() if w.keep_N < 1 else np.arange(w.F)
+        selH = sets_t["idx_H"][0].cpu().numpy() if w.keep_H < 1 else np.arange(w.h_kv)
+    else:
+        c = sets_t["ucnt"].cpu().numpy()
+        selN = sets_t["uN"][: c[0]].cpu().numpy() if w.keep_N < 1 else np.arange(w.F)
+        selH = sets_t["uH"][: c[1]].cpu().numpy() if w.keep_H < 1 else np.arange(w.h_kv)
+        assert np.array_equal(selN, oracle.union(sets_t["idx_N"].cpu().numpy(), w.F))
+    K, V = np16(m.K[L - 1]), np16(m.V[L - 1])
+    for b in range(w.B):
+        if kv_sel is None:
+            y_ref, *_ = oracle.layer(np16(y_in[b]), Wh, K[b], V[b], w.n, selH, selN)
+        else:
+            kept, counts = kv_sel
+            a = oracle.attn_kvsel(np16(y_in[b]), Wh, K[b], V[b], w.n, kept, counts)
+            hmid = oracle.round_fp16(npf(y_in[b]) + a.delta)
+            mm = oracle.mlp_gather(hmid, Wh["fc1"], Wh["b1"], Wh["fc2T"], Wh.get("b2"), selN)
+            y_ref = oracle.round_fp16(hmid.astype(float) + mm)
+        assert rel_err(npf(m.y_out[b]), y_ref) < TOL, b
+
+
+def test_opt175b_stack_as_benchmarked():
+    # 24 layers, d 12288, 96 heads, FFN 49152, neuron keep 10 %, head keep 50 %
+    m = _step(synth.workload("opt-175b"))
+    _check_last_layer(m)
+
+
+def test_opt67b_stack():
+    m = _step(synth.workload("opt-6.7b"))
+    _check_last_layer(m)
+
+
+@pytest.mark.parametrize("kn,kh", [(0.25, 1.0), (1.0, 0.5)])
+def test_opt67b_keep_variants(kn, kh):
+    m = _step(synth.workload("opt-6.7b", keep_N=kn, keep_H=kh, layers=4))
+    _check_last_layer(m)
+
+
+def test_opt66b_batch4_union():
+    m = _step(synth.workload("opt-66b", B=4))
+    _check_last_layer(m)
+
+
+@pytest.mark.parametrize("n", [2048, 8192])
+def test_composition_retained_kv(n):
+    # d 4096, 32 query / 8 KV heads x 128, neuron keep 1/2, KV keep 1/8;
+    # the full 32 layers, decode through the retained KV buffers
+    w = synth.workload("compose", n=n)
+    m = _step(w)
+    L = m.L
+    counts = m.kc[L - 1].cpu().numpy()
+    b = int(n * w.keep_KV)
+    W = w.obs_window
+    kept = np.zeros((w.h_kv, int(counts.max())), np.int32)
+    for u in range(w.h_kv):
+        k = m.kp[L - 1][u, : counts[u]].cpu().numpy()
+        assert counts[u] == b and np.all(np.diff(k) > 0)
+        assert set(range(4)) <= set(k) and set(range(n - W, n)) <= set(k)
+        # the retained rows are the cache rows at the kept positions
+        assert np.array_equal(np16(m.Kr[L - 1][u, : counts[u]]).view(np.uint16),
+                              np16(m.K[L - 1][0, u, k]).view(np.uint16))
+        kept[u, : counts[u]] = k
+    _check_last_layer(m, kv_sel=(kept, counts))
+
+
+def test_composition_dense_split_k_baseline():
+    w = synth.workload("compose", n=8192, layers=4)
+    m = _step(w, kv_dense=True)
+    _check_last_layer(m)
