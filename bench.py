@@ -247,9 +247,12 @@ class Model:
         flags = (dv.DV_LOOKAHEAD if lookahead else 0) | self.kv_flags
         self.step = dv.Step(self.D, self.keep, self.W, self.kvs, [s for s, _ in self.sets],
                             self.ws, flags, self.side, self.evf, self.evj, dev_status=self.st)
+        # the seeded draws above ran on the current stream; the step runs on others
+        torch.cuda.synchronize()
 
     def capture(self, stream, profiler=None):
         g = torch.cuda.CUDAGraph()
+        stream.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(stream):
             self.step(self.x, self.y_tmp, self.y_out, self.n, stream=stream)  # warm, outside capture
             torch.cuda.synchronize()

@@ -128,7 +128,7 @@ static WsLayout ws_layout(const dv_dims* D, int B, int flags) {
   const int target = main_ctas();
   const size_t part = std::max(stream_part_bytes(D->d, B, D->F, target),
                                stream_part_bytes(D->d, B, (long long)D->h * D->d_h, target));
-  L.S_max = split_plan(D->n_max + 1, 1, B, attn_ctas()).S;
+  L.S_max = kSplitsMax;
   size_t off = 0;
   L.part = off;
   off += al(part);

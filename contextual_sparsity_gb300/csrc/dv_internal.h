@@ -47,6 +47,7 @@ struct SplitPlan {
   int C;  // keys per split
   int S;  // splits
 };
+constexpr int kSplitsMax = 64;  // splits per unit, any plan
 SplitPlan split_plan(int max_keys, int units, int B, int target_ctas);
 
 int launch_splitk(const float* q, int B, int dh, int G, int h_kv, const int32_t* idx, int k,

@@ -49,19 +49,23 @@ DV_DEV void merge(float& m, float& l, float* o, float m2, float l2, const float*
   m = M;
 }
 
-// The CTA's contiguous K and V rows (at most kSplitMax keys) are brought into
-// shared memory by two 1-D bulk copies (one round trip to memory), then the
-// online softmax runs from shared memory.
-constexpr int kSplitMax = 128;
+// Each CTA owns a contiguous range of keys of one unit and walks it in chunks
+// of kChunk keys: a chunk's K and V rows (contiguous in the cache or in the
+// retained buffer) arrive by two 1-D bulk copies into one of two shared-memory
+// stages, so the next chunk is in flight while this one is consumed.
+constexpr int kChunk = 64;
 
 template <int DH, int G>
 __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
-  constexpr int LPK = DH / 8;        // lanes per key (8 dims each)
-  constexpr int KPW = 32 / LPK;      // keys per warp step
-  constexpr int U = 8;               // unrolled steps
+  constexpr int LPK = DH / 8;            // lanes per key (8 dims each)
+  constexpr int KPW = 32 / LPK;          // keys per warp step
+  constexpr int U = kChunk / (4 * KPW);  // warp steps per chunk
   __shared__ float red[4][G][DH + 2];
-  __shared__ __align__(8) uint64_t kv_bar;
-  extern __shared__ __align__(128) uint16_t kv_smem[];  // [C][DH] K, then [C][DH] V
+  __shared__ __align__(8) uint64_t kv_bar[2];
+  __shared__ float cw[G][kSplitsMax];    // combine: weight of each split
+  __shared__ float cinv[G];              // combine: 1 / sum of weighted l
+  __shared__ int last;
+  extern __shared__ __align__(128) uint16_t kv_smem[];  // [2 stages][K, V][kChunk][DH]
 
   const int s = blockIdx.x, e = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -89,29 +93,34 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
     Vb = p.V + (((size_t)b * p.h_kv + u) * p.n_max) * DH;
     count = p.n + 1;
   }
-  const int t0 = s * p.C;
+  const int t0 = min(count, s * p.C);
   const int t1 = min(count, t0 + p.C);
-  uint16_t* sK = kv_smem;
-  uint16_t* sV = kv_smem + (size_t)p.C * DH;
-  const uint32_t bytes = t1 > t0 ? (uint32_t)(t1 - t0) * DH * 2 : 0u;
+  const int nch = (t1 - t0 + kChunk - 1) / kChunk;
+
   if (threadIdx.x == 0) {
-    mbar_init(&kv_bar, 1);
+    mbar_init(&kv_bar[0], 1);
+    mbar_init(&kv_bar[1], 1);
     fence_mbar_init();
   }
   __syncthreads();
-  bool staged = true;
-  if (bytes) {
-    if (threadIdx.x == 0) {
-      // K/V rows were written by generic stores (the new token, by the QKV
-      // kernel); order them before the async-proxy reads.
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      const uint64_t pol = policy_evict_first();
-      mbar_arrive_expect_tx(&kv_bar, 2 * bytes);
-      bulk_g2s(sK, Kb + (size_t)t0 * DH, bytes, &kv_bar, pol);
-      bulk_g2s(sV, Vb + (size_t)t0 * DH, bytes, &kv_bar, pol);
-    }
+  // Thread 0 only: chunk c into stage c & 1.
+  auto issue = [&](int c) {
+    const int a0 = t0 + c * kChunk, a1 = min(t1, a0 + kChunk);
+    const uint32_t bytes = (uint32_t)(a1 - a0) * DH * 2;
+    uint16_t* stg = kv_smem + (size_t)(c & 1) * 2 * kChunk * DH;
+    const uint64_t pol = policy_evict_first();
+    mbar_arrive_expect_tx(&kv_bar[c & 1], 2 * bytes);
+    bulk_g2s(stg, Kb + (size_t)a0 * DH, bytes, &kv_bar[c & 1], pol);
+    bulk_g2s(stg + kChunk * DH, Vb + (size_t)a0 * DH, bytes, &kv_bar[c & 1], pol);
+  };
+  if (threadIdx.x == 0 && nch > 0) {
+    // K/V rows were written by generic stores (the new token, by the QKV
+    // kernel); order them before the async-proxy reads.
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    issue(0);
+    if (nch > 1) issue(1);
   }
-  // The queries load while the bulk copies are in flight.
+  // The queries load while the first copies are in flight.
   float q[G][8];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -119,12 +128,6 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) q[g][i] = qs[i] * kLog2e;
   }
-  if (bytes) {
-    staged = mbar_wait(&kv_bar, 0);
-    if (!staged && (threadIdx.x & 31) == 0) flag(p.st, DV_DEV_TIMEOUT);
-  }
-  staged = __syncthreads_and(staged);
-
   float m[G], l[G], o[G][8];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -134,24 +137,35 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
     for (int i = 0; i < 8; ++i) o[g][i] = 0.f;
   }
 
-  const int step = 4 * KPW;  // keys per CTA step
-  // The loop bound is warp-uniform (the shuffles below need every lane);
-  // lanes whose key lies past the split's end carry a zero weight.
-  for (int wbase = t0 + warp * KPW; wbase < t1; wbase += step * U) {
+  int failed = -1;  // first chunk whose copies did not arrive in time
+  for (int c = 0; c < nch; ++c) {
+    bool staged = mbar_wait(&kv_bar[c & 1], (c >> 1) & 1);
+    if (!staged && lane == 0) flag(p.st, DV_DEV_TIMEOUT);
+    if (!__syncthreads_and(staged)) {
+      failed = c;
+      break;
+    }
+    const uint16_t* sK = kv_smem + (size_t)(c & 1) * 2 * kChunk * DH;
+    const uint16_t* sV = sK + kChunk * DH;
+    const int na = min(kChunk, t1 - (t0 + c * kChunk));
+    // Every lane runs every step (the shuffles below need all of them); a
+    // lane whose key lies past the chunk carries a zero weight.
     uint4 kv[U], vv[U];
     bool valid[U];
 #pragma unroll
     for (int j = 0; j < U; ++j) {
-      const int t = wbase + grp + j * step;
-      valid[j] = staged && t < t1;
+      const int t = warp * KPW + grp + j * 4 * KPW;  // key within the chunk
+      valid[j] = t < na;
       if (valid[j]) {
-        kv[j] = *reinterpret_cast<const uint4*>(sK + (size_t)(t - t0) * DH + sub * 8);
-        vv[j] = *reinterpret_cast<const uint4*>(sV + (size_t)(t - t0) * DH + sub * 8);
+        kv[j] = *reinterpret_cast<const uint4*>(sK + (size_t)t * DH + sub * 8);
+        vv[j] = *reinterpret_cast<const uint4*>(sV + (size_t)t * DH + sub * 8);
       } else {
         kv[j] = make_uint4(0, 0, 0, 0);
         vv[j] = kv[j];
       }
     }
+    __syncthreads();  // the stage is in registers everywhere: refill it
+    if (threadIdx.x == 0 && c + 2 < nch) issue(c + 2);
     float sc[U][G];
 #pragma unroll
     for (int j = 0; j < U; ++j) {
@@ -189,6 +203,11 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
       m[g] = mx;
     }
   }
+  if (failed >= 0 && threadIdx.x == 0) {
+    // Give the copies still in flight (chunks failed .. failed + 1) one more
+    // bounded wait before the CTA's shared memory goes away.
+    for (int c = failed; c < min(nch, failed + 2); ++c) mbar_wait(&kv_bar[c & 1], (c >> 1) & 1);
+  }
   // Merge the KPW key groups of the warp (lanes with equal sub).
 #pragma unroll
   for (int off = 16; off >= LPK; off >>= 1) {
@@ -214,7 +233,7 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
     }
   }
   __syncthreads();
-  // Merge the 4 warps and write the split's partial.
+  // Merge the 4 warps and write the split's partial (m, l, o).
   for (int i = threadIdx.x; i < G * (DH + 2); i += blockDim.x) {
     const int g = i / (DH + 2), c = i % (DH + 2);
     float M = -INFINITY;
@@ -238,39 +257,62 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
   // The last split of this unit to finish combines all splits (no waiting:
   // the others have already published their partials):
   // H = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
-  __shared__ int last;
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) last = (atomicAdd(&p.cnt[(size_t)b * p.k + e], 1) == p.S - 1);
   __syncthreads();
   if (!last) return;
   __threadfence();
+  const float* ubase = p.part + (((size_t)b * p.k + e) * G) * p.S * (DH + 2);
+  for (int g = warp; g < G; g += 4) {  // one warp per query head: split weights
+    const float* base = ubase + (size_t)g * p.S * (DH + 2);
+    float ms[kSplitsMax / 32], ls[kSplitsMax / 32];
+    float M = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kSplitsMax / 32; ++j) {
+      const int t = lane + 32 * j;
+      ms[j] = t < p.S ? __ldcg(base + (size_t)t * (DH + 2)) : -INFINITY;
+      ls[j] = t < p.S ? __ldcg(base + (size_t)t * (DH + 2) + 1) : 0.f;
+      M = fmaxf(M, ms[j]);
+    }
+    M = warp_max(M);
+    float L = 0.f;
+#pragma unroll
+    for (int j = 0; j < kSplitsMax / 32; ++j) {
+      const float w = (ls[j] > 0.f) ? exp2f(ms[j] - M) : 0.f;
+      if (lane + 32 * j < kSplitsMax) cw[g][lane + 32 * j] = w;
+      L += w * ls[j];
+    }
+    L = warp_sum(L);
+    if (lane == 0) cinv[g] = L > 0.f ? 1.f / L : 0.f;
+  }
+  __syncthreads();
   for (int i = threadIdx.x; i < G * DH; i += blockDim.x) {
     const int g = i / DH, c = i % DH;
-    const float* base = p.part + ((((size_t)b * p.k + e) * G + g) * p.S) * (DH + 2);
-    float M = -INFINITY;
-    for (int t = 0; t < p.S; ++t) M = fmaxf(M, __ldcg(base + (size_t)t * (DH + 2)));
-    float L = 0.f, O = 0.f;
-    for (int t = 0; t < p.S; ++t) {
-      const float* ps = base + (size_t)t * (DH + 2);
-      const float mt = __ldcg(ps), lt = __ldcg(ps + 1);
-      const float w = (lt > 0.f) ? exp2f(mt - M) : 0.f;
-      L += w * lt;
-      O += w * __ldcg(ps + 2 + c);
+    const float* base = ubase + (size_t)g * p.S * (DH + 2) + 2 + c;
+    float O0 = 0.f, O1 = 0.f;
+    int t = 0;
+    for (; t + 1 < p.S; t += 2) {
+      O0 += cw[g][t] * __ldcg(base + (size_t)t * (DH + 2));
+      O1 += cw[g][t + 1] * __ldcg(base + (size_t)(t + 1) * (DH + 2));
     }
-    p.H[(((size_t)b * p.k + e) * G + g) * DH + c] = L > 0.f ? O / L : 0.f;
+    if (t < p.S) O0 += cw[g][t] * __ldcg(base + (size_t)t * (DH + 2));
+    p.H[(((size_t)b * p.k + e) * G + g) * DH + c] = (O0 + O1) * cinv[g];
   }
   if (threadIdx.x == 0) p.cnt[(size_t)b * p.k + e] = 0;
 }
 
 SplitPlan split_plan(int max_keys, int units, int B, int target_ctas) {
+  // About target_ctas CTAs in all; each split a whole number of chunks; at
+  // most kSplitsMax splits per unit.
   SplitPlan pl;
-  const long long want = std::max(1, target_ctas);
-  long long per = ((long long)max_keys * units * B + want - 1) / want;
-  per = std::max<long long>(32, std::min<long long>(per, kSplitMax));
-  per = (per + 31) / 32 * 32;
+  const long long ub = std::max(1LL, (long long)units * B);
+  long long S = (std::max(1, target_ctas) + ub - 1) / ub;
+  S = std::max(1LL, std::min<long long>(S, std::min<long long>(kSplitsMax, (max_keys + kChunk - 1) / kChunk)));
+  long long per = (max_keys + S - 1) / S;
+  per = std::max<long long>(kChunk, (per + kChunk - 1) / kChunk * kChunk);
   pl.C = (int)per;
-  pl.S = (int)((max_keys + per - 1) / per);
+  pl.S = (int)std::max(1LL, (max_keys + per - 1) / per);
   return pl;
 }
 
@@ -295,7 +337,7 @@ int launch_splitk(const float* q, int B, int dh, int G, int h_kv, const int32_t*
   SplitParams p{q, K, V, Kr, Vr, kept_count, idx, dev_count, k, h_kv, n, n_max, b_max,
                 retained, plan.C, plan.S, part, H, cnt, st};
   void* args[] = {&p};
-  const size_t smem = (size_t)2 * plan.C * dh * 2;
+  const size_t smem = (size_t)2 * 2 * kChunk * dh * 2;  // two stages of K and V
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return DV_ERR_LAUNCH;
