@@ -232,17 +232,14 @@ static int sets_from_u(const dv_dims* D, int B, const float* u, const uint16_t* 
   int rc = launch_pred2(u, B, D->r, P2 + (size_t)row0 * D->r, row1 - row0, sets->scores + row0, ld,
                         ctas, s);
   if (rc != DV_OK) return rc;
-  if (!neuron_dense) {
-    rc = launch_topk(sets->scores, B, ld, D->F, nullptr, kN, sets->idx_N, kN, st, s);
-    if (rc == DV_OK && B > 1) rc = launch_union(sets->idx_N, B, kN, D->F, sets->uN, sets->ucnt, s);
-    if (rc != DV_OK) return rc;
-  }
-  if (!head_dense) {
+  if (!neuron_dense) rc = launch_topk(sets->scores, B, ld, D->F, nullptr, kN, sets->idx_N, kN, st, s);
+  if (rc == DV_OK && !head_dense)
     rc = launch_topk(sets->scores + D->F, B, ld, D->h_kv, nullptr, kH, sets->idx_H, kH, st, s);
-    if (rc == DV_OK && B > 1)
-      rc = launch_union(sets->idx_H, B, kH, D->h_kv, sets->uH, sets->ucnt + 1, s);
-    if (rc != DV_OK) return rc;
-  }
+  if (rc != DV_OK) return rc;
+  if (B > 1 && !neuron_dense) rc = launch_union(sets->idx_N, B, kN, D->F, sets->uN, sets->ucnt, s);
+  if (rc == DV_OK && B > 1 && !head_dense)
+    rc = launch_union(sets->idx_H, B, kH, D->h_kv, sets->uH, sets->ucnt + 1, s);
+  if (rc != DV_OK) return rc;
   return DV_OK;
 }
 

@@ -287,17 +287,41 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
     if (lane == 0) cinv[g] = L > 0.f ? 1.f / L : 0.f;
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < G * DH; i += blockDim.x) {
-    const int g = i / DH, c = i % DH;
-    const float* base = ubase + (size_t)g * p.S * (DH + 2) + 2 + c;
-    float O0 = 0.f, O1 = 0.f;
-    int t = 0;
-    for (; t + 1 < p.S; t += 2) {
-      O0 += cw[g][t] * __ldcg(base + (size_t)t * (DH + 2));
-      O1 += cw[g][t + 1] * __ldcg(base + (size_t)(t + 1) * (DH + 2));
+  // O[g][c] = sum_s w[g][s] o_s[g][c]: 128 / DH threads per column, each
+  // over every (128 / DH)-th group of 8 splits, with all G x 8 loads issued
+  // before they are summed.
+  constexpr int TPC = 128 / DH;
+  const int c = threadIdx.x % DH, tp = threadIdx.x / DH;
+  float O[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) O[g] = 0.f;
+  for (int t0 = tp * 8; t0 < p.S; t0 += 8 * TPC) {
+    float v[G][8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        v[g][j] = (t0 + j < p.S) ? __ldcg(ubase + ((size_t)g * p.S + t0 + j) * (DH + 2) + 2 + c)
+                                 : 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        if (t0 + j < p.S) O[g] = fmaf(cw[g][t0 + j], v[g][j], O[g]);
+  }
+  if (TPC > 1) {
+    __syncthreads();  // red is free: the split partial was written above
+    if (tp == 1)
+#pragma unroll
+      for (int g = 0; g < G; ++g) red[0][g][c] = O[g];
+    __syncthreads();
+  }
+  if (tp == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float o = TPC > 1 ? O[g] + red[0][g][c] : O[g];
+      p.H[(((size_t)b * p.k + e) * G + g) * DH + c] = o * cinv[g];
     }
-    if (t < p.S) O0 += cw[g][t] * __ldcg(base + (size_t)t * (DH + 2));
-    p.H[(((size_t)b * p.k + e) * G + g) * DH + c] = (O0 + O1) * cinv[g];
   }
   if (threadIdx.x == 0) p.cnt[(size_t)b * p.k + e] = 0;
 }

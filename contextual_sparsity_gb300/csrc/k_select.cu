@@ -304,6 +304,113 @@ __global__ void __cluster_dims__(kClusterTopk, 1, 1) __launch_bounds__(256, 4)
   cluster.sync();  // keep this CTA's shared memory alive until all peers read it
 }
 
+// ---------------------------------------------------------------------------
+// Short rows (N <= kSmallN, e.g. the head scores): one CTA of 256 threads per
+// row (small enough to share an SM with a weight-streaming CTA) loads the
+// row's keys into shared memory once, runs the 4-pass radix select there and
+// compacts in index order with warp ballots over per-warp segments.
+// ---------------------------------------------------------------------------
+constexpr int kSmallN = 4096;
+
+DV_DEV uint32_t key_of(float f) { return isnan(f) ? 0u : fkey(f); }
+
+// Scanning hist[0, nb) from the top bin down, find the bin where the running
+// count reaches krem: sh[0] = that bin, sh[1] = krem minus the keys above it.
+DV_DEV void select_bin(const uint32_t* hist, int nb, uint32_t krem, uint32_t* sh, int* tmp) {
+  const int per = nb / (int)blockDim.x;
+  const int top = nb - 1 - per * (int)threadIdx.x;
+  uint32_t loc = 0;
+  for (int j = 0; j < per; ++j) loc += hist[top - j];
+  int total;
+  const uint32_t excl = (uint32_t)block_exscan((int)loc, tmp, &total);
+  if (excl < krem && krem <= excl + loc) {
+    uint32_t above = excl;
+    for (int j = 0; j < per; ++j) {
+      const uint32_t c = hist[top - j];
+      if (above + c >= krem) {
+        sh[0] = (uint32_t)(top - j);
+        sh[1] = krem - above;
+        break;
+      }
+      above += c;
+    }
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 4) k_topk_small(const float* __restrict__ scores,
+                                                                 int ld, int N, int k,
+                                                                 int32_t* __restrict__ idx,
+                                                                 int ld_idx, int* st) {
+  constexpr int NW = kTopkThreads / 32;
+  __shared__ uint32_t keys[kSmallN];
+  __shared__ uint32_t hist[256];
+  __shared__ int tmp[32];
+  __shared__ uint32_t sh[2];
+  __shared__ int wgt[NW], weq[NW];
+  const float* s = scores + (size_t)blockIdx.x * ld;
+  int32_t* out = idx + (size_t)blockIdx.x * ld_idx;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  k = max(1, min(k, N));
+
+  bool nan_seen = false;
+  for (int i = tid; i < N; i += kTopkThreads) {
+    const float f = s[i];
+    nan_seen |= isnan(f);
+    keys[i] = key_of(f);
+  }
+  if (__syncthreads_or(nan_seen) && tid == 0) flag(st, DV_DEV_NONFINITE);
+
+  uint32_t prefix = 0, mask = 0, krem = (uint32_t)k;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < N; i += kTopkThreads)
+      if ((keys[i] & mask) == prefix) atomicAdd(&hist[(keys[i] >> shift) & 255u], 1u);
+    __syncthreads();
+    select_bin(hist, 256, krem, sh, tmp);
+    prefix |= sh[0] << shift;
+    krem = sh[1];
+    mask |= 255u << shift;
+  }
+  const uint32_t T = prefix;  // the k-th largest key; krem of the keys equal to T are taken
+
+  // Ordered compaction over warp segments (multiples of 32 positions).
+  const int seg = (N + kTopkThreads - 1) / kTopkThreads * 32;
+  const int w0 = min(N, warp * seg), w1 = min(N, w0 + seg);
+  int gt = 0, eq = 0;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const bool v = i < w1;
+    const uint32_t key = v ? keys[i] : 0u;
+    gt += __popc(__ballot_sync(0xffffffffu, v && key > T));
+    eq += __popc(__ballot_sync(0xffffffffu, v && key == T));
+  }
+  if (lane == 0) {
+    wgt[warp] = gt;
+    weq[warp] = eq;
+  }
+  __syncthreads();
+  int pos = 0, eqb = 0;
+  for (int w = 0; w < warp; ++w) {
+    pos += wgt[w] + min(weq[w], max(0, (int)krem - eqb));
+    eqb += weq[w];
+  }
+  const unsigned lt = (1u << lane) - 1u;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const bool v = i < w1;
+    const uint32_t key = v ? keys[i] : 0u;
+    const unsigned me = __ballot_sync(0xffffffffu, v && key == T);
+    const bool take = v && (key > T || (key == T && eqb + __popc(me & lt) < (int)krem));
+    const unsigned mt = __ballot_sync(0xffffffffu, take);
+    if (take) out[pos + __popc(mt & lt)] = i;
+    pos += __popc(mt);
+    eqb += __popc(me);
+  }
+}
+
 template <int KPT>
 static int launch_topk_cluster(const float* scores, int B, int ld, int N, int k, int32_t* idx,
                                int ld_idx, int* st, cudaStream_t stream) {
@@ -316,7 +423,10 @@ int launch_topk(const float* scores, int B, int ld, int N, const int* k_per_row,
   const int per = (N + kClusterTopk * 256 - 1) / (kClusterTopk * 256);  // keys per thread
   int rc = DV_ERR_UNSUPPORTED;
   note_launch(DV_TAG_TOPK, 0, stream);
-  if (!k_per_row && per <= 64) {
+  if (!k_per_row && N <= kSmallN) {
+    k_topk_small<<<B, kTopkThreads, 0, stream>>>(scores, ld, N, k, idx, ld_idx, st);
+    rc = cudaGetLastError() == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
+  } else if (!k_per_row && per <= 64) {
     if (per <= 1) rc = launch_topk_cluster<1>(scores, B, ld, N, k, idx, ld_idx, st, stream);
     else if (per <= 4) rc = launch_topk_cluster<4>(scores, B, ld, N, k, idx, ld_idx, st, stream);
     else if (per <= 8) rc = launch_topk_cluster<8>(scores, B, ld, N, k, idx, ld_idx, st, stream);

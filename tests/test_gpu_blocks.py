@@ -77,6 +77,20 @@ def test_topk_bit_exact_with_ties(N, B):
         assert np.array_equal(uni.cpu().numpy()[: len(u)], u)
 
 
+@pytest.mark.parametrize("N,B", [(96, 2), (2047, 1), (49152, 2), (65536, 1), (65537, 1)])
+def test_topk_bit_exact_continuous(N, B):
+    # distinct scores: the threshold bin's keys fit in shared memory
+    g = torch.Generator().manual_seed(N + B)
+    s = torch.randn(B, N, generator=g) * 3.0
+    sd = s.cuda()
+    for k in sorted({1, 2, max(1, N // 10), N - 1, N} - {0}):
+        idx = torch.zeros(B, k, dtype=torch.int32, device="cuda")
+        dv.select_topk(sd, N, k, idx)
+        torch.cuda.synchronize()
+        ref = np.stack([oracle.topk(s[b].double().numpy(), k) for b in range(B)])
+        assert np.array_equal(idx.cpu().numpy(), ref), k
+
+
 def test_topk_flags_nan_without_faulting():
     s = torch.randn(1, 100)
     s[0, 17] = float("nan")
