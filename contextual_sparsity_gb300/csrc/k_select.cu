@@ -158,160 +158,6 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(const float* __restrict__
   }
 }
 
-// ---------------------------------------------------------------------------
-// Cluster top-k: one cluster of 8 CTAs per row. CTA r of the cluster owns
-// positions [r C, (r+1) C) (C = ceil(N / 8)); its thread t keeps the KPT
-// consecutive keys starting at r C + t KPT in registers. Each radix pass builds
-// per-warp histograms, sums them into a CTA histogram, and every CTA reads the
-// 8 CTA histograms through distributed shared memory in rank order (so every
-// CTA takes the same, deterministic decision). The compaction offsets come
-// from the CTAs' totals exchanged the same way. No global atomics, no spin.
-// ---------------------------------------------------------------------------
-constexpr int kClusterTopk = 8;
-
-template <int KPT>
-__global__ void __cluster_dims__(kClusterTopk, 1, 1) __launch_bounds__(256, 4)
-    k_topk_cluster(const float* __restrict__ scores, int ld, int N, int k,
-                   int32_t* __restrict__ idx, int ld_idx, int* st) {
-  cg::cluster_group cluster = cg::this_cluster();
-  __shared__ uint32_t whist[8][256];
-  __shared__ uint32_t ctah[256];
-  __shared__ int tmp[32];
-  __shared__ uint32_t sh_prefix, sh_krem;
-  __shared__ int tot[2];  // this CTA's count of keys > T, == T
-  const int rank = (int)cluster.block_rank();
-  const int row = blockIdx.x / kClusterTopk;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const float* s = scores + (size_t)row * ld;
-  int32_t* out = idx + (size_t)row * ld_idx;
-  const int C = (N + kClusterTopk - 1) / kClusterTopk;
-  const int c0 = min(N, rank * C), c1 = min(N, c0 + C);
-  const int p0 = c0 + tid * KPT;
-  k = max(1, min(k, N));
-
-  uint32_t key[KPT];
-  bool nan_seen = false;
-#pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    const int i = p0 + j;
-    key[j] = 0u;
-    if (i < c1) {
-      const float f = s[i];
-      nan_seen |= isnan(f);
-      key[j] = isnan(f) ? 0u : fkey(f);
-    }
-  }
-  if (__syncthreads_or(nan_seen) && tid == 0) flag(st, DV_DEV_NONFINITE);
-
-  uint32_t prefix = 0, mask = 0, krem = (uint32_t)k;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 8 * 256; i += blockDim.x) (&whist[0][0])[i] = 0;
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < KPT; ++j)
-      if (p0 + j < c1 && (key[j] & mask) == prefix)
-        atomicAdd(&whist[warp][(key[j] >> shift) & 255u], 1u);
-    __syncthreads();
-    {
-      uint32_t t = 0;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) t += whist[w][tid];
-      ctah[tid] = t;
-    }
-    cluster.sync();
-    {
-      // Cluster histogram: thread t gathers bin t from the 8 CTAs (rank order).
-      uint32_t t = 0;
-#pragma unroll
-      for (int r = 0; r < kClusterTopk; ++r) t += cluster.map_shared_rank(ctah, r)[tid];
-      whist[0][tid] = t;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane L owns digits [255 - 8L - 7, 255 - 8L], scanned from the top.
-      uint32_t c[8], loc = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = whist[0][255 - 8 * lane - j];
-        loc += c[j];
-      }
-      uint32_t incl = loc;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const uint32_t excl = incl - loc;
-      if (excl < krem && krem <= incl) {
-        uint32_t above = excl;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (above + c[j] >= krem) {
-            sh_prefix = prefix | ((uint32_t)(255 - 8 * lane - j) << shift);
-            sh_krem = krem - above;
-            break;
-          }
-          above += c[j];
-        }
-      }
-    }
-    cluster.sync();  // every CTA is done reading the others' histograms
-    prefix = sh_prefix;
-    krem = sh_krem;
-    mask |= 255u << shift;
-  }
-  const uint32_t T = prefix;
-
-  // Ordered compaction.
-  int gt = 0, eq = 0;
-#pragma unroll
-  for (int j = 0; j < KPT; ++j)
-    if (p0 + j < c1) {
-      gt += key[j] > T;
-      eq += key[j] == T;
-    }
-  int cta_eq, cta_gt;
-  const int eq_before_local = block_exscan(eq, tmp, &cta_eq);
-  const int gt_dummy = block_exscan(gt, tmp, &cta_gt);
-  (void)gt_dummy;
-  if (tid == 0) {
-    tot[0] = cta_gt;
-    tot[1] = cta_eq;
-  }
-  cluster.sync();
-  int eq_before_cta = 0, out_before_cta = 0;
-  for (int r = 0; r < rank; ++r) {
-    const int* o = cluster.map_shared_rank(tot, r);
-    const int g_r = o[0], e_r = o[1];
-    const int take_r = min(e_r, max(0, (int)krem - eq_before_cta));
-    out_before_cta += g_r + take_r;
-    eq_before_cta += e_r;
-  }
-  int take_eq = min(eq, max(0, (int)krem - (eq_before_cta + eq_before_local)));
-  int total_unused;
-  int pos = out_before_cta + block_exscan(gt + take_eq, tmp, &total_unused);
-#pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    if (p0 + j >= c1) break;
-    if (key[j] > T) {
-      out[pos++] = p0 + j;
-    } else if (key[j] == T && take_eq > 0) {
-      out[pos++] = p0 + j;
-      --take_eq;
-    }
-  }
-  cluster.sync();  // keep this CTA's shared memory alive until all peers read it
-}
-
-// ---------------------------------------------------------------------------
-// Short rows (N <= kSmallN, e.g. the head scores): one CTA of 256 threads per
-// row (small enough to share an SM with a weight-streaming CTA) loads the
-// row's keys into shared memory once, runs the 4-pass radix select there and
-// compacts in index order with warp ballots over per-warp segments.
-// ---------------------------------------------------------------------------
-constexpr int kSmallN = 4096;
-
 DV_DEV uint32_t key_of(float f) { return isnan(f) ? 0u : fkey(f); }
 
 // Scanning hist[0, nb) from the top bin down, find the bin where the running
@@ -337,6 +183,309 @@ DV_DEV void select_bin(const uint32_t* hist, int nb, uint32_t krem, uint32_t* sh
   }
   __syncthreads();
 }
+
+// ---------------------------------------------------------------------------
+// Cluster top-k: one cluster of 8 CTAs per row. CTA r of the cluster owns
+// positions [r C, (r+1) C) (C = ceil(N / 8)) and keeps their keys in shared
+// memory (one coalesced read of the row; every later pass is a short rolled
+// loop, so the code stays small -- the kernel runs once per prediction, with
+// a cold instruction cache). Cluster exchanges go through distributed shared
+// memory, each CTA reading its peers in rank order, so all CTAs take the same
+// decisions:
+//   1. the row's smallest and largest score (and key);
+//   2. a histogram over kRangeBins equal value ranges of [min, max] (any
+//      monotone map of the scores is exact here: bins only narrow the search;
+//      equal ranges spread the keys out, so few atomics collide and few keys
+//      share the bin holding the k-th largest score, b1);
+//   3. b1's keys of all CTAs gathered; their exact ranks (greater keys, then
+//      equal keys at lower positions) give the k-th largest key T and how
+//      many keys equal to T are taken -- or, when more than kCandMax keys
+//      share b1, an MSB-first radix select (8 bits a pass) over b1's keys;
+//   4. ordered compaction: per-warp segments counted with ballots, the CTAs'
+//      counts exchanged, then the indices written in ascending order, keys
+//      equal to T to the lowest positions first.
+// No global atomics, no spin.
+// ---------------------------------------------------------------------------
+constexpr int kClusterTopk = 8;
+constexpr int kRangeBins = 2048;
+constexpr int kCandCta = 256;   // b1 keys one CTA can hold for the exchange
+constexpr int kCandMax = 512;   // b1 keys of the whole row ranked in shared memory
+
+// Inverse of fkey (NaN's key 0 comes back as a NaN).
+DV_DEV float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+struct RangeBins {
+  bool byval;
+  float fmn, vscale;
+  uint32_t kmn;
+  float kscale;
+  DV_DEV int operator()(uint32_t key) const {
+    float t;
+    if (byval) {
+      const float f = key_float(key);
+      t = isnan(f) ? 0.f : (f - fmn) * vscale;
+    } else {
+      t = __uint2float_rn(key - kmn) * kscale;
+    }
+    return min(kRangeBins - 1, max(0, (int)t));
+  }
+};
+
+__global__ void __cluster_dims__(kClusterTopk, 1, 1) __launch_bounds__(kTopkThreads, 4)
+    k_topk_cluster(const float* __restrict__ scores, int ld, int N, int k,
+                   int32_t* __restrict__ idx, int ld_idx, int* st) {
+  constexpr int NT = kTopkThreads, NW = NT / 32;
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ uint32_t keys[];                    // [C] this CTA's keys
+  __shared__ __align__(16) uint32_t hist[kRangeBins];   // this CTA's (peers read it)
+  __shared__ __align__(16) uint32_t ghist[kRangeBins];  // the cluster's; per-warp in the radix path
+  __shared__ uint32_t lkey[kCandCta];                   // this CTA's b1 keys (peers read them)
+  __shared__ int lpos[kCandCta];
+  __shared__ uint32_t ckey[kCandMax];                   // the row's b1 keys
+  __shared__ int cpos[kCandMax];
+  __shared__ float mmf[2];                              // this CTA's min, max score (peers read)
+  __shared__ uint32_t mmk[2];                           // this CTA's min, max key (peers read)
+  __shared__ int lcount;                                // (peers read)
+  __shared__ int tot[2];                                // keys > T, == T here (peers read)
+  __shared__ int wgt[NW], weq[NW];
+  __shared__ int tmp[32];
+  __shared__ float tmpf[2][NW];
+  __shared__ uint32_t tmpk[2][NW];
+  __shared__ uint32_t sh[2];
+  const int rank = (int)cluster.block_rank();
+  const int row = blockIdx.x / kClusterTopk;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const float* s = scores + (size_t)row * ld;
+  int32_t* out = idx + (size_t)row * ld_idx;
+  const int C = (N + kClusterTopk - 1) / kClusterTopk;
+  const int c0 = min(N, rank * C), c1 = min(N, c0 + C), cn = c1 - c0;
+  k = max(1, min(k, N));
+
+  bool nan_seen = false;
+  float fmn = INFINITY, fmx = -INFINITY;
+  uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;
+  for (int i = tid; i < cn; i += NT) {
+    const float f = s[c0 + i];
+    nan_seen |= isnan(f);
+    if (!isnan(f)) {
+      fmn = fminf(fmn, f);
+      fmx = fmaxf(fmx, f);
+    }
+    const uint32_t key = key_of(f);
+    kmn = min(kmn, key);
+    kmx = max(kmx, key);
+    keys[i] = key;
+  }
+  for (int i = tid; i < kRangeBins; i += NT) hist[i] = 0;
+  if (tid == 0) lcount = 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    fmn = fminf(fmn, __shfl_xor_sync(0xffffffffu, fmn, o));
+    fmx = fmaxf(fmx, __shfl_xor_sync(0xffffffffu, fmx, o));
+    kmn = min(kmn, __shfl_xor_sync(0xffffffffu, kmn, o));
+    kmx = max(kmx, __shfl_xor_sync(0xffffffffu, kmx, o));
+  }
+  if (lane == 0) {
+    tmpf[0][warp] = fmn;
+    tmpf[1][warp] = fmx;
+    tmpk[0][warp] = kmn;
+    tmpk[1][warp] = kmx;
+  }
+  if (__syncthreads_or(nan_seen) && tid == 0) flag(st, DV_DEV_NONFINITE);
+  if (tid == 0) {
+    for (int w = 1; w < NW; ++w) {
+      tmpf[0][0] = fminf(tmpf[0][0], tmpf[0][w]);
+      tmpf[1][0] = fmaxf(tmpf[1][0], tmpf[1][w]);
+      tmpk[0][0] = min(tmpk[0][0], tmpk[0][w]);
+      tmpk[1][0] = max(tmpk[1][0], tmpk[1][w]);
+    }
+    mmf[0] = tmpf[0][0];
+    mmf[1] = tmpf[1][0];
+    mmk[0] = tmpk[0][0];
+    mmk[1] = tmpk[1][0];
+  }
+  cluster.sync();  // (1)
+  fmn = INFINITY;
+  fmx = -INFINITY;
+  kmn = 0xFFFFFFFFu;
+  kmx = 0u;
+  for (int r = 0; r < kClusterTopk; ++r) {
+    const float* pf = cluster.map_shared_rank(mmf, r);
+    const uint32_t* pk = cluster.map_shared_rank(mmk, r);
+    fmn = fminf(fmn, pf[0]);
+    fmx = fmaxf(fmx, pf[1]);
+    kmn = min(kmn, pk[0]);
+    kmx = max(kmx, pk[1]);
+  }
+  // Bins by value when the scores' range is finite, else by key.
+  RangeBins bin_of;
+  bin_of.byval = isfinite(fmn) && isfinite(fmx);
+  bin_of.fmn = fmn;
+  bin_of.vscale = bin_of.byval ? (float)kRangeBins / fmaxf(fmx - fmn, 1e-30f) : 0.f;
+  bin_of.kmn = kmn;
+  bin_of.kscale = (float)kRangeBins / ((float)(kmx - kmn) + 1.f);
+
+  for (int i = tid; i < cn; i += NT) atomicAdd(&hist[bin_of(keys[i])], 1u);
+  cluster.sync();  // (2)
+  for (int b0 = tid * 4; b0 < kRangeBins; b0 += 4 * NT) {
+    uint4 t = make_uint4(0, 0, 0, 0);
+    for (int r = 0; r < kClusterTopk; ++r) {
+      const uint4 h = *reinterpret_cast<const uint4*>(cluster.map_shared_rank(hist, r) + b0);
+      t.x += h.x; t.y += h.y; t.z += h.z; t.w += h.w;
+    }
+    *reinterpret_cast<uint4*>(ghist + b0) = t;
+  }
+  __syncthreads();
+  select_bin(ghist, kRangeBins, (uint32_t)k, sh, tmp);
+  const int b1 = (int)sh[0];
+  uint32_t krem = sh[1];
+
+  for (int i = tid; i < cn; i += NT)
+    if (bin_of(keys[i]) == b1) {
+      const int c = atomicAdd(&lcount, 1);
+      if (c < kCandCta) {
+        lkey[c] = keys[i];
+        lpos[c] = c0 + i;
+      }
+    }
+  cluster.sync();  // (3)
+  int nc = 0;
+  bool fits = true;
+  for (int r = 0; r < kClusterTopk; ++r) {
+    const int cr = *cluster.map_shared_rank(&lcount, r);
+    fits &= cr <= kCandCta;
+    nc += cr;
+  }
+  fits &= nc <= kCandMax;
+
+  uint32_t T;  // the k-th largest key; krem of the keys equal to T are taken
+  if (fits) {
+    int off = 0;
+    for (int r = 0; r < kClusterTopk; ++r) {
+      const int cr = *cluster.map_shared_rank(&lcount, r);
+      const uint32_t* pk = cluster.map_shared_rank(lkey, r);
+      const int* pp = cluster.map_shared_rank(lpos, r);
+      for (int c = tid; c < cr; c += NT) {
+        ckey[off + c] = pk[c];
+        cpos[off + c] = pp[c];
+      }
+      off += cr;
+    }
+    __syncthreads();
+    for (int c = tid; c < nc; c += NT) {
+      const uint32_t kc = ckey[c];
+      const int pc = cpos[c];
+      int r = 0;
+      for (int c2 = 0; c2 < nc; ++c2) {
+        const uint32_t k2 = ckey[c2];
+        r += (k2 > kc) || (k2 == kc && cpos[c2] < pc);
+      }
+      if (r == (int)krem - 1) sh[0] = kc;
+    }
+    __syncthreads();
+    T = sh[0];
+    int g = 0;
+    for (int c = tid; c < nc; c += NT) g += ckey[c] > T;
+    int gtot;
+    block_exscan(g, tmp, &gtot);
+    krem -= (uint32_t)gtot;
+  } else {
+    // Radix select over b1's keys; per-warp histograms in ghist, the CTA's in
+    // hist (read by the peers between the two cluster barriers of a pass).
+    uint32_t prefix = 0, mask = 0;
+    uint32_t* whist = ghist;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int i = tid; i < NW * 256; i += NT) whist[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < cn; i += NT) {
+        const uint32_t key = keys[i];
+        if (bin_of(key) == b1 && (key & mask) == prefix)
+          atomicAdd(&whist[warp * 256 + ((key >> shift) & 255u)], 1u);
+      }
+      __syncthreads();
+      {
+        uint32_t t = 0;
+        for (int w = 0; w < NW; ++w) t += whist[w * 256 + tid];
+        hist[tid] = t;
+      }
+      cluster.sync();
+      {
+        uint32_t t = 0;
+        for (int r = 0; r < kClusterTopk; ++r) t += cluster.map_shared_rank(hist, r)[tid];
+        whist[tid] = t;
+      }
+      __syncthreads();
+      select_bin(whist, 256, krem, sh, tmp);
+      prefix |= sh[0] << shift;
+      krem = sh[1];
+      mask |= 255u << shift;
+      cluster.sync();  // the peers are done reading hist
+    }
+    T = prefix;
+  }
+
+  // Ordered compaction over warp segments (multiples of 32 positions).
+  const int seg = (cn + NT - 1) / NT * 32;
+  const int w0 = min(cn, warp * seg), w1 = min(cn, w0 + seg);
+  int gt = 0, eq = 0;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const bool v = i < w1;
+    const uint32_t key = v ? keys[i] : 0u;
+    gt += __popc(__ballot_sync(0xffffffffu, v && key > T));
+    eq += __popc(__ballot_sync(0xffffffffu, v && key == T));
+  }
+  if (lane == 0) {
+    wgt[warp] = gt;
+    weq[warp] = eq;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int a = 0, b = 0;
+    for (int w = 0; w < NW; ++w) {
+      a += wgt[w];
+      b += weq[w];
+    }
+    tot[0] = a;
+    tot[1] = b;
+  }
+  cluster.sync();  // (4)
+  int pos = 0, eqb = 0;
+  for (int r = 0; r < rank; ++r) {
+    const int* o = cluster.map_shared_rank(tot, r);
+    pos += o[0] + min(o[1], max(0, (int)krem - eqb));
+    eqb += o[1];
+  }
+  for (int w = 0; w < warp; ++w) {
+    pos += wgt[w] + min(weq[w], max(0, (int)krem - eqb));
+    eqb += weq[w];
+  }
+  const unsigned lt = (1u << lane) - 1u;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const bool v = i < w1;
+    const uint32_t key = v ? keys[i] : 0u;
+    const unsigned me = __ballot_sync(0xffffffffu, v && key == T);
+    const bool take = v && (key > T || (key == T && eqb + __popc(me & lt) < (int)krem));
+    const unsigned mt = __ballot_sync(0xffffffffu, take);
+    if (take) out[pos + __popc(mt & lt)] = c0 + i;
+    pos += __popc(mt);
+    eqb += __popc(me);
+  }
+  cluster.sync();  // (5) keep this CTA's shared memory alive until all peers read it
+}
+
+// ---------------------------------------------------------------------------
+// Short rows (N <= kSmallN, e.g. the head scores): one CTA of 256 threads per
+// row (small enough to share an SM with a weight-streaming CTA) loads the
+// row's keys into shared memory once, runs the 4-pass radix select there and
+// compacts in index order with warp ballots over per-warp segments.
+// ---------------------------------------------------------------------------
+constexpr int kSmallN = 4096;
+
 
 __global__ void __launch_bounds__(kTopkThreads, 4) k_topk_small(const float* __restrict__ scores,
                                                                  int ld, int N, int k,
@@ -411,29 +560,29 @@ __global__ void __launch_bounds__(kTopkThreads, 4) k_topk_small(const float* __r
   }
 }
 
-template <int KPT>
+constexpr int kClusterMaxN = 131072;  // 64 KB of keys per CTA (opt-in shared memory)
+
 static int launch_topk_cluster(const float* scores, int B, int ld, int N, int k, int32_t* idx,
                                int ld_idx, int* st, cudaStream_t stream) {
-  k_topk_cluster<KPT><<<B * kClusterTopk, 256, 0, stream>>>(scores, ld, N, k, idx, ld_idx, st);
+  // The keys go in dynamic shared memory; together with the static arrays
+  // they can pass the 48 KB that needs no opt-in, so the limit is always set.
+  const size_t smem = (size_t)((N + kClusterTopk - 1) / kClusterTopk) * 4;
+  if (cudaFuncSetAttribute((const void*)k_topk_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return DV_ERR_LAUNCH;
+  k_topk_cluster<<<B * kClusterTopk, kTopkThreads, smem, stream>>>(scores, ld, N, k, idx, ld_idx, st);
   return cudaGetLastError() == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
 }
 
 int launch_topk(const float* scores, int B, int ld, int N, const int* k_per_row, int k,
                 int32_t* idx, int ld_idx, int* st, cudaStream_t stream) {
-  const int per = (N + kClusterTopk * 256 - 1) / (kClusterTopk * 256);  // keys per thread
   int rc = DV_ERR_UNSUPPORTED;
   note_launch(DV_TAG_TOPK, 0, stream);
   if (!k_per_row && N <= kSmallN) {
     k_topk_small<<<B, kTopkThreads, 0, stream>>>(scores, ld, N, k, idx, ld_idx, st);
     rc = cudaGetLastError() == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
-  } else if (!k_per_row && per <= 64) {
-    if (per <= 1) rc = launch_topk_cluster<1>(scores, B, ld, N, k, idx, ld_idx, st, stream);
-    else if (per <= 4) rc = launch_topk_cluster<4>(scores, B, ld, N, k, idx, ld_idx, st, stream);
-    else if (per <= 8) rc = launch_topk_cluster<8>(scores, B, ld, N, k, idx, ld_idx, st, stream);
-    else if (per <= 16) rc = launch_topk_cluster<16>(scores, B, ld, N, k, idx, ld_idx, st, stream);
-    else if (per <= 24) rc = launch_topk_cluster<24>(scores, B, ld, N, k, idx, ld_idx, st, stream);
-    else if (per <= 32) rc = launch_topk_cluster<32>(scores, B, ld, N, k, idx, ld_idx, st, stream);
-    else rc = launch_topk_cluster<64>(scores, B, ld, N, k, idx, ld_idx, st, stream);
+  } else if (!k_per_row && N <= kClusterMaxN) {
+    rc = launch_topk_cluster(scores, B, ld, N, k, idx, ld_idx, st, stream);
   } else {
     k_topk<<<B, kTopkThreads, 0, stream>>>(scores, ld, N, k_per_row, k, idx, ld_idx, st);
     rc = cudaGetLastError() == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
@@ -478,8 +627,10 @@ int launch_union(const int32_t* idx, int B, int k, int N, int32_t* out, int32_t*
                  cudaStream_t stream) {
   const size_t smem = (size_t)((N + 31) / 32) * 4;
   if (smem > 200 * 1024) return DV_ERR_UNSUPPORTED;
-  if (smem > 48 * 1024)
-    cudaFuncSetAttribute(k_union, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (smem + 1024 > 48 * 1024 &&  // with the static scan buffer
+      cudaFuncSetAttribute(k_union, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess)
+    return DV_ERR_LAUNCH;
   note_launch(DV_TAG_UNION, 0, stream);
   k_union<<<1, 256, smem, stream>>>(idx, B, k, N, out, count);
   note_launch(DV_TAG_UNION, 1, stream);
