@@ -343,9 +343,19 @@ def peaks():
         return 6800.0, "fallback"
 
 
+# Source files each timed kernel is built from: a traffic record taken by ncu
+# stays valid while these are unchanged.
+KERNEL_SOURCES = {
+    "k_stream<KIND_QKV>": ["k_stream.cu", "dv_common.cuh", "dv_internal.h"],
+    "k_stream<KIND_WO>": ["k_stream.cu", "dv_common.cuh", "dv_internal.h"],
+    "k_stream<KIND_MLP>": ["k_stream.cu", "dv_common.cuh", "dv_internal.h"],
+    "k_splitk": ["k_attn.cu", "dv_common.cuh", "dv_internal.h"],
+}
+
+
 def traffic_record(kernel):
     """ncu DRAM bytes per launch of `kernel`, if the capture in profiles/ was
-    taken on the current kernel source (else None)."""
+    taken on the kernel's current source (else None)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(p) as f:
@@ -355,15 +365,14 @@ def traffic_record(kernel):
     rec = j.get(kernel)
     if not rec:
         return None
-    return rec["bytes_per_launch"] if rec.get("source_sha") == source_sha() else None
+    return rec["bytes_per_launch"] if rec.get("source_sha") == source_sha(kernel) else None
 
 
-def source_sha():
+def source_sha(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "contextual_sparsity_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
