@@ -63,17 +63,28 @@ static int main_ctas() { return g_tune.main_ctas > 0 ? g_tune.main_ctas : sm_cou
 static bool g_pdl = true;
 
 cudaError_t launch_k(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                     void** args, bool pdl) {
+                     void** args, bool pdl, int cluster_x) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl && g_pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (cluster_x > 0) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cluster_x;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = (pdl && g_pdl) ? 1 : 0;
+  cfg.numAttrs = na;
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 static int attn_ctas() { return g_tune.attn_ctas > 0 ? g_tune.attn_ctas : 2 * sm_count(); }
@@ -232,9 +243,12 @@ static int sets_from_u(const dv_dims* D, int B, const float* u, const uint16_t* 
   int rc = launch_pred2(u, B, D->r, P2 + (size_t)row0 * D->r, row1 - row0, sets->scores + row0, ld,
                         ctas, s);
   if (rc != DV_OK) return rc;
-  if (!neuron_dense) rc = launch_topk(sets->scores, B, ld, D->F, nullptr, kN, sets->idx_N, kN, st, s);
-  if (rc == DV_OK && !head_dense)
+  // The head set first: the next layer's first kernel needs it, the neuron
+  // set only its last.
+  if (!head_dense)
     rc = launch_topk(sets->scores + D->F, B, ld, D->h_kv, nullptr, kH, sets->idx_H, kH, st, s);
+  if (rc == DV_OK && !neuron_dense)
+    rc = launch_topk(sets->scores, B, ld, D->F, nullptr, kN, sets->idx_N, kN, st, s);
   if (rc != DV_OK) return rc;
   if (B > 1 && !neuron_dense) rc = launch_union(sets->idx_N, B, kN, D->F, sets->uN, sets->ucnt, s);
   if (rc == DV_OK && B > 1 && !head_dense)

@@ -85,7 +85,7 @@ int sm_count();
 // Launch with (pdl) or without a programmatic dependency on the previous
 // kernel of the stream.
 cudaError_t launch_k(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                     void** args, bool pdl);
+                     void** args, bool pdl, int cluster_x = 0);
 
 // Launch accounting: call with phase 0 just before a kernel launch and phase 1
 // just after it (see dv_profile / dv_launch_count).

@@ -13,9 +13,13 @@
 // the observation-window queries over the cache, pooled over the window and
 // the query heads of each KV head, smoothed by a centred mean, sinks and the
 // window forced, top positions per KV head, gathered into a contiguous buffer.
+#include <cooperative_groups.h>
+
 #include "dv_internal.h"
 
 namespace dv {
+
+namespace cg = cooperative_groups;
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -51,21 +55,33 @@ DV_DEV void merge(float& m, float& l, float* o, float m2, float l2, const float*
 
 // Each CTA owns a contiguous range of keys of one unit and walks it in chunks
 // of kChunk keys: a chunk's K and V rows (contiguous in the cache or in the
-// retained buffer) arrive by two 1-D bulk copies into one of two shared-memory
-// stages, so the next chunk is in flight while this one is consumed.
+// retained buffer) arrive by two 1-D bulk copies into one of NST shared-memory
+// stages, so up to NST chunks are in flight at once. Two stages (64 KB at
+// d_h 128) leave room on the SM for the side-stream kernels; three serve long
+// ranges, where the bytes in flight set the pace.
+//
+// The splits of a unit are combined either through global memory (their
+// partials written, an atomic count, the last split to finish combines:
+// any number of splits) or, when they are at most kClusterSplits, as one
+// thread-block cluster: each split leaves its partial in shared memory and
+// rank 0 reads the others through distributed shared memory (no global
+// partials, no fence, no atomic).
 constexpr int kChunk = 64;
+constexpr int kClusterSplits = 8;
+constexpr int kLongRangeChunks = 4;  // more chunks per CTA than this: three stages
 
-template <int DH, int G>
+template <int DH, int G, bool CL, int NST>
 __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
   constexpr int LPK = DH / 8;            // lanes per key (8 dims each)
   constexpr int KPW = 32 / LPK;          // keys per warp step
   constexpr int U = kChunk / (4 * KPW);  // warp steps per chunk
   __shared__ float red[4][G][DH + 2];
-  __shared__ __align__(8) uint64_t kv_bar[2];
-  __shared__ float cw[G][kSplitsMax];    // combine: weight of each split
-  __shared__ float cinv[G];              // combine: 1 / sum of weighted l
+  __shared__ float cpart[G][DH + 2];     // cluster combine: this split's (m, l, o)
+  __shared__ __align__(8) uint64_t kv_bar[NST];
+  __shared__ float cw[G][kSplitsMax];    // global combine: weight of each split
+  __shared__ float cinv[G];              // global combine: 1 / sum of weighted l
   __shared__ int last;
-  extern __shared__ __align__(128) uint16_t kv_smem[];  // [2 stages][K, V][kChunk][DH]
+  extern __shared__ __align__(128) uint16_t kv_smem[];  // [NST][K, V][kChunk][DH]
 
   const int s = blockIdx.x, e = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -75,7 +91,7 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
 
   int kk = p.k;
   if (p.dev_count) kk = min(kk, *p.dev_count);
-  if (e >= kk) return;
+  if (e >= kk) return;  // uniform over a unit's splits (one cluster)
   int u = p.idx ? p.idx[e] : e;
   if (u < 0 || u >= p.h_kv) {
     if (threadIdx.x == 0) flag(p.st, DV_DEV_BAD_INDEX);
@@ -98,27 +114,26 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
   const int nch = (t1 - t0 + kChunk - 1) / kChunk;
 
   if (threadIdx.x == 0) {
-    mbar_init(&kv_bar[0], 1);
-    mbar_init(&kv_bar[1], 1);
+#pragma unroll
+    for (int i = 0; i < NST; ++i) mbar_init(&kv_bar[i], 1);
     fence_mbar_init();
   }
   __syncthreads();
-  // Thread 0 only: chunk c into stage c & 1.
+  // Thread 0 only: chunk c into stage c % NST.
   auto issue = [&](int c) {
     const int a0 = t0 + c * kChunk, a1 = min(t1, a0 + kChunk);
     const uint32_t bytes = (uint32_t)(a1 - a0) * DH * 2;
-    uint16_t* stg = kv_smem + (size_t)(c & 1) * 2 * kChunk * DH;
+    uint16_t* stg = kv_smem + (size_t)(c % NST) * 2 * kChunk * DH;
     const uint64_t pol = policy_evict_first();
-    mbar_arrive_expect_tx(&kv_bar[c & 1], 2 * bytes);
-    bulk_g2s(stg, Kb + (size_t)a0 * DH, bytes, &kv_bar[c & 1], pol);
-    bulk_g2s(stg + kChunk * DH, Vb + (size_t)a0 * DH, bytes, &kv_bar[c & 1], pol);
+    mbar_arrive_expect_tx(&kv_bar[c % NST], 2 * bytes);
+    bulk_g2s(stg, Kb + (size_t)a0 * DH, bytes, &kv_bar[c % NST], pol);
+    bulk_g2s(stg + kChunk * DH, Vb + (size_t)a0 * DH, bytes, &kv_bar[c % NST], pol);
   };
   if (threadIdx.x == 0 && nch > 0) {
     // K/V rows were written by generic stores (the new token, by the QKV
     // kernel); order them before the async-proxy reads.
     asm volatile("fence.proxy.async.global;" ::: "memory");
-    issue(0);
-    if (nch > 1) issue(1);
+    for (int c = 0; c < min(nch, NST); ++c) issue(c);
   }
   // The queries load while the first copies are in flight.
   float q[G][8];
@@ -139,13 +154,13 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
 
   int failed = -1;  // first chunk whose copies did not arrive in time
   for (int c = 0; c < nch; ++c) {
-    bool staged = mbar_wait(&kv_bar[c & 1], (c >> 1) & 1);
+    bool staged = mbar_wait(&kv_bar[c % NST], (c / NST) & 1);
     if (!staged && lane == 0) flag(p.st, DV_DEV_TIMEOUT);
     if (!__syncthreads_and(staged)) {
       failed = c;
       break;
     }
-    const uint16_t* sK = kv_smem + (size_t)(c & 1) * 2 * kChunk * DH;
+    const uint16_t* sK = kv_smem + (size_t)(c % NST) * 2 * kChunk * DH;
     const uint16_t* sV = sK + kChunk * DH;
     const int na = min(kChunk, t1 - (t0 + c * kChunk));
     // Every lane runs every step (the shuffles below need all of them); a
@@ -165,7 +180,7 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
       }
     }
     __syncthreads();  // the stage is in registers everywhere: refill it
-    if (threadIdx.x == 0 && c + 2 < nch) issue(c + 2);
+    if (threadIdx.x == 0 && c + NST < nch) issue(c + NST);
     float sc[U][G];
 #pragma unroll
     for (int j = 0; j < U; ++j) {
@@ -204,9 +219,10 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
     }
   }
   if (failed >= 0 && threadIdx.x == 0) {
-    // Give the copies still in flight (chunks failed .. failed + 1) one more
-    // bounded wait before the CTA's shared memory goes away.
-    for (int c = failed; c < min(nch, failed + 2); ++c) mbar_wait(&kv_bar[c & 1], (c >> 1) & 1);
+    // Give the copies still in flight one more bounded wait before the CTA's
+    // shared memory goes away.
+    for (int c = failed; c < min(nch, failed + NST); ++c)
+      mbar_wait(&kv_bar[c % NST], (c / NST) & 1);
   }
   // Merge the KPW key groups of the warp (lanes with equal sub).
 #pragma unroll
@@ -233,7 +249,7 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
     }
   }
   __syncthreads();
-  // Merge the 4 warps and write the split's partial (m, l, o).
+  // Merge the 4 warps: this split's partial (m, l, o).
   for (int i = threadIdx.x; i < G * (DH + 2); i += blockDim.x) {
     const int g = i / (DH + 2), c = i % (DH + 2);
     float M = -INFINITY;
@@ -252,8 +268,36 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
         }
       }
     }
-    p.part[((((size_t)b * p.k + e) * G + g) * p.S + s) * (DH + 2) + c] = val;
+    if (CL) cpart[g][c] = val;
+    else p.part[((((size_t)b * p.k + e) * G + g) * p.S + s) * (DH + 2) + c] = val;
   }
+
+  if (CL) {
+    // H = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the cluster's
+    // splits, read by rank 0 in rank order.
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (cluster.block_rank() == 0) {
+      const int ns = (int)cluster.num_blocks();
+      for (int i = threadIdx.x; i < G * DH; i += blockDim.x) {
+        const int g = i / DH, c = i % DH;
+        float M = -INFINITY;
+        for (int r = 0; r < ns; ++r) M = fmaxf(M, cluster.map_shared_rank(&cpart[g][0], r)[0]);
+        float L = 0.f, O = 0.f;
+        for (int r = 0; r < ns; ++r) {
+          const float* pr = cluster.map_shared_rank(&cpart[g][0], r);
+          const float lr = pr[1];
+          const float w = (lr > 0.f) ? exp2f(pr[0] - M) : 0.f;
+          L += w * lr;
+          O += w * pr[2 + c];
+        }
+        p.H[(((size_t)b * p.k + e) * G + g) * DH + c] = L > 0.f ? O / L : 0.f;
+      }
+    }
+    cluster.sync();  // the peers' shared memory stays until rank 0 has read it
+    return;
+  }
+
   // The last split of this unit to finish combines all splits (no waiting:
   // the others have already published their partials):
   // H = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
@@ -295,19 +339,19 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
   float O[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) O[g] = 0.f;
-  for (int t0 = tp * 8; t0 < p.S; t0 += 8 * TPC) {
+  for (int t0s = tp * 8; t0s < p.S; t0s += 8 * TPC) {
     float v[G][8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
 #pragma unroll
       for (int g = 0; g < G; ++g)
-        v[g][j] = (t0 + j < p.S) ? __ldcg(ubase + ((size_t)g * p.S + t0 + j) * (DH + 2) + 2 + c)
-                                 : 0.f;
+        v[g][j] = (t0s + j < p.S) ? __ldcg(ubase + ((size_t)g * p.S + t0s + j) * (DH + 2) + 2 + c)
+                                  : 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j)
 #pragma unroll
       for (int g = 0; g < G; ++g)
-        if (t0 + j < p.S) O[g] = fmaf(cw[g][t0 + j], v[g][j], O[g]);
+        if (t0s + j < p.S) O[g] = fmaf(cw[g][t0s + j], v[g][j], O[g]);
   }
   if (TPC > 1) {
     __syncthreads();  // red is free: the split partial was written above
@@ -340,15 +384,21 @@ SplitPlan split_plan(int max_keys, int units, int B, int target_ctas) {
   return pl;
 }
 
-template <int DH>
+template <int DH, bool CL, int NST>
 static void* splitk_fn(int G) {
   switch (G) {
-    case 1: return (void*)k_splitk<DH, 1>;
-    case 2: return (void*)k_splitk<DH, 2>;
-    case 4: return (void*)k_splitk<DH, 4>;
-    case 8: return (void*)k_splitk<DH, 8>;
+    case 1: return (void*)k_splitk<DH, 1, CL, NST>;
+    case 2: return (void*)k_splitk<DH, 2, CL, NST>;
+    case 4: return (void*)k_splitk<DH, 4, CL, NST>;
+    case 8: return (void*)k_splitk<DH, 8, CL, NST>;
     default: return nullptr;
   }
+}
+
+template <int DH>
+static void* splitk_pick(int G, bool cl, int nst) {
+  if (cl) return splitk_fn<DH, true, 2>(G);
+  return nst == 3 ? splitk_fn<DH, false, 3>(G) : splitk_fn<DH, false, 2>(G);
 }
 
 int launch_splitk(const float* q, int B, int dh, int G, int h_kv, const int32_t* idx, int k,
@@ -356,17 +406,21 @@ int launch_splitk(const float* q, int B, int dh, int G, int h_kv, const int32_t*
                   const uint16_t* Kr, const uint16_t* Vr, const int32_t* kept_count, int b_max,
                   int retained, SplitPlan plan, float* part, float* H, int* cnt, int* st,
                   cudaStream_t stream, bool pdl) {
-  void* fn = dh == 128 ? splitk_fn<128>(G) : (dh == 64 ? splitk_fn<64>(G) : nullptr);
+  const bool cl = plan.S <= kClusterSplits;
+  const int nst = (!cl && (plan.C + kChunk - 1) / kChunk > kLongRangeChunks) ? 3 : 2;
+  void* fn = nullptr;
+  if (dh == 128) fn = splitk_pick<128>(G, cl, nst);
+  if (dh == 64) fn = splitk_pick<64>(G, cl, nst);
   if (!fn) return DV_ERR_UNSUPPORTED;
   SplitParams p{q, K, V, Kr, Vr, kept_count, idx, dev_count, k, h_kv, n, n_max, b_max,
                 retained, plan.C, plan.S, part, H, cnt, st};
   void* args[] = {&p};
-  const size_t smem = (size_t)2 * 2 * kChunk * dh * 2;  // two stages of K and V
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  const size_t smem = (size_t)nst * 2 * kChunk * dh * 2;  // nst stages of K and V
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return DV_ERR_LAUNCH;
   note_launch(DV_TAG_SPLITK, 0, stream);
-  const cudaError_t e = launch_k(fn, dim3(plan.S, k, B), dim3(128), smem, stream, args, pdl);
+  const cudaError_t e = launch_k(fn, dim3(plan.S, k, B), dim3(128), smem, stream, args, pdl,
+                                 cl ? plan.S : 0);
   note_launch(DV_TAG_SPLITK, 1, stream);
   return e == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
 }
