@@ -423,7 +423,15 @@ def run_ours(a):
     ms_step = ms_total / a.steps
     assert m.st.item() == 0, f"device status {m.st.item()}"
 
-    sel, pred = traffic.layer_bytes(w, keys=m.keys)
+    union = None
+    if w.B > 1:
+        # the union sizes the step produced (the two set buffers hold the
+        # last two layers' sets)
+        c = [t["ucnt"].cpu().tolist() for _, t in m.sets]
+        uN = sum(x[0] for x in c) / 2 if w.keep_N < 1 else w.F
+        uH = sum(x[1] for x in c) / 2 if w.keep_H < 1 else w.h_kv
+        union = (uN, uH)
+    sel, pred = traffic.layer_bytes(w, keys=m.keys, union=union)
     job = job_figures(ms_total, a.steps, w.layers, wsz, sel, pred)
     us_layer = job["us_layer_replica"]
     gbs_sel, gbs_all = job["gbs_selected"], job["gbs_all"]
@@ -455,12 +463,14 @@ def run_ours(a):
     G = w.h // w.h_kv
     # the QKV launch also streams the next layer's first predictor layer
     # (r rows of d) when predicting ahead
-    p1_rows = w.r if (lookahead and (w.keep_N < 1 or w.keep_H < 1) and w.layers > 1) else 0
+    p1_rows = (w.r if (lookahead and (w.keep_N < 1 or w.keep_H < 1) and w.layers > 1 and w.B == 1)
+               else 0)
+    kH_e, kN_e = (union[1], union[0]) if union else (m.kH, m.kN)
     algo = {
-        "qkv": traffic.qkv_bytes(w.d, G, w.dh, m.kH) + traffic.p1_bytes(w.d, p1_rows),
-        "wo": traffic.wo_bytes(w.d, G, w.dh, m.kH),
-        "mlp": traffic.mlp_bytes(w.d, m.kN),
-        "splitk": traffic.kv_bytes(w.dh, m.kH, m.keys),
+        "qkv": traffic.qkv_bytes(w.d, G, w.dh, kH_e) + traffic.p1_bytes(w.d, p1_rows),
+        "wo": traffic.wo_bytes(w.d, G, w.dh, kH_e),
+        "mlp": traffic.mlp_bytes(w.d, kN_e),
+        "splitk": w.B * traffic.kv_bytes(w.dh, kH_e, m.keys),
     }
     totals = {k: sum(v) for k, v in per_kind.items()}
     dom = max(algo, key=lambda k: totals.get(k, 0.0))
@@ -473,32 +483,53 @@ def run_ours(a):
             "algorithmic_bytes_per_launch": algo[dom], "avg_launch_us": kernel_us[dom],
             "traffic": traffic_record(names[dom])}
 
-    # End to end through the public API: pinned host input -> device, one
-    # dv_decode_step call (eager, all layers), device -> pinned host output.
+    # End to end through the public API: every step copies its input from
+    # pinned host memory, runs dv_decode_step (all layers) and copies the
+    # result back, and the host waits for that result. Reported as a serving
+    # caller would run it (the three calls captured once in a CUDA graph,
+    # replayed per step) and, beside it, with dv_decode_step called eagerly.
     e2e = None
     if not a.no_e2e:
         hin = torch.empty(w.B, w.d, dtype=torch.float16).pin_memory()
         hin.copy_(m.x.cpu())
         hout = torch.empty(w.B, w.d, dtype=torch.float16).pin_memory()
         xin = torch.empty_like(m.x)
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                xin.copy_(hin, non_blocking=True)
-                m.step(xin, m.y_tmp, m.y_out, m.n, stream=stream)
-                hout.copy_(m.y_out, non_blocking=True)
-            stream.synchronize()
-            barrier(wsz)
-            t0 = time.perf_counter()
-            for _ in range(a.e2e_steps):
-                xin.copy_(hin, non_blocking=True)
-                m.step(xin, m.y_tmp, m.y_out, m.n, stream=stream)
-                hout.copy_(m.y_out, non_blocking=True)
+
+        def one_step():
+            xin.copy_(hin, non_blocking=True)
+            m.step(xin, m.y_tmp, m.y_out, m.n, stream=stream)
+            hout.copy_(m.y_out, non_blocking=True)
+
+        def timed(run):
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    run()
                 stream.synchronize()
-            el = time.perf_counter() - t0
-        el = max_over_ranks(el, wsz)
-        e2e = {"value": round(el / a.e2e_steps * 1e6 / w.layers / wsz, 2), "unit": UNIT,
+                barrier(wsz)
+                t0 = time.perf_counter()
+                for _ in range(a.e2e_steps):
+                    run()
+                    stream.synchronize()
+                el = time.perf_counter() - t0
+            return max_over_ranks(el, wsz) / a.e2e_steps * 1e6 / w.layers / wsz
+
+        ge = torch.cuda.CUDAGraph()
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            one_step()
+            stream.synchronize()
+            with torch.cuda.graph(ge, stream=stream):
+                one_step()
+        us_graph = timed(ge.replay)
+        us_eager = timed(one_step)
+        assert m.st.item() == 0, f"device status {m.st.item()}"
+        e2e = {"value": round(us_graph, 2), "unit": UNIT,
                "h2d_bytes_per_step": hin.numel() * 2, "d2h_bytes_per_step": hout.numel() * 2,
-               "steps": a.e2e_steps, "api": "dv_decode_step (eager C-ABI call per step)"}
+               "steps": a.e2e_steps,
+               "api": "dv_decode_step with the pinned H2D input copy and the D2H result copy, "
+                      "captured once in a CUDA graph, replayed per step, host waits per step",
+               "eager_value": round(us_eager, 2),
+               "eager_api": "dv_decode_step called per step (one C-ABI call, all layers)"}
 
     cpu = None
     if rank == 0 and wsz == 1 and not a.no_cpu_baseline:
@@ -521,7 +552,8 @@ def run_ours(a):
                    "parallelism": "replicas" if wsz > 1 else "single GPU",
                    "l2": "inputs larger than L2 (every step streams ~"
                          f"{(sel + pred) * w.layers / 1e9:.1f} GB)"},
-        "selected_bytes_per_layer": sel, "predictor_bytes_per_layer": pred,
+        "selected_bytes_per_layer": round(sel), "predictor_bytes_per_layer": pred,
+        "union_sizes": ({"neurons": union[0], "units": union[1]} if union else None),
         "kv": ({"mode": "retained", "keep": w.keep_KV, "budget": m.b, "keys_read": m.keys,
                 "selection_ms_all_layers": round(m.select_ms, 3)} if m.retained else
                {"mode": "full cache", "keys_read": m.keys}),

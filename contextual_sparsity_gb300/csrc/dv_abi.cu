@@ -515,7 +515,8 @@ int dv_decode_layer(const dv_dims* dims, const dv_keep* keep, int B, const dv_la
     REQ_PTR(P2_next);
   }
 
-  if ((flags & DV_JOIN) && ev_join)
+  // (the previous layer recorded the join only if it predicted ahead)
+  if ((flags & DV_JOIN) && ev_join && need_pred)
     if (cudaStreamWaitEvent(main, ev_join, 0) != cudaSuccess) return DV_ERR_LAUNCH;
   if ((flags & DV_SYNC_PREDICT) && need_pred) {
     REQ_PTR(w->P1); REQ_PTR(w->P2);
@@ -533,13 +534,21 @@ int dv_decode_layer(const dv_dims* dims, const dv_keep* keep, int B, const dv_la
   // PDL for the QKV kernel only when its index list was not produced by the
   // kernel right before it (a synchronous prediction on this stream).
   const bool pdl_qkv = !((flags & DV_SYNC_PREDICT) && need_pred) && (flags & DV_JOIN);
+  // At batch 1 the next layer's P1 rows ride in this QKV launch; at B > 1
+  // they run on the side stream (the fused form would spill registers).
+  const bool fuse_p1 = look && B == 1;
   rc = attn_qkv(y_in, B, dims, w, selH, kHe, cntH, kv, n, softmax_scale, flags,
-                look ? P1_next : nullptr, at<float>(ws, L.u_side), dev_status, ws, L, main,
+                fuse_p1 ? P1_next : nullptr, at<float>(ws, L.u_side), dev_status, ws, L, main,
                 pdl_qkv);
   if (rc != DV_OK) return rc;
   if (look) {
     if (cudaEventRecord(ev_fork, main) != cudaSuccess) return DV_ERR_LAUNCH;
     if (cudaStreamWaitEvent(side, ev_fork, 0) != cudaSuccess) return DV_ERR_LAUNCH;
+    if (!fuse_p1) {
+      rc = launch_pred1_gemv(y_in, B, dims->d, P1_next, dims->r, (flags & DV_PRED_RELU) ? 1 : 0,
+                             at<float>(ws, L.u_side), side_ctas(), side);
+      if (rc != DV_OK) return rc;
+    }
     rc = sets_from_u(dims, B, at<float>(ws, L.u_side), P2_next, kN, nd, kH, hd, next, dev_status,
                      side_ctas(), side);
     if (rc != DV_OK) return rc;

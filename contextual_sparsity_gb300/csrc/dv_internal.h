@@ -37,6 +37,8 @@ int launch_predict(const uint16_t* y, int B, int d, const uint16_t* P1, int r,
 int launch_pred1(const uint16_t* y, int B, int d, const uint16_t* P1, int r, int relu, float* u,
                  int target_ctas, int ring_budget, cudaStream_t stream);
 
+int launch_pred1_gemv(const uint16_t* y, int B, int d, const uint16_t* P1, int r, int relu,
+                      float* u, int target_ctas, cudaStream_t stream);
 int launch_pred2(const float* u, int B, int r, const uint16_t* P2, int N, float* scores, int ld,
                  int target_ctas, cudaStream_t stream);
 

@@ -601,9 +601,19 @@ __global__ void __launch_bounds__(256) k_union(const int32_t* __restrict__ idx, 
   const int words = (N + 31) / 32;
   for (int w = threadIdx.x; w < words; w += blockDim.x) bits[w] = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < B * k; i += blockDim.x) {
-    const int j = idx[i];
-    if (j >= 0 && j < N) atomicOr(&bits[j >> 5], 1u << (j & 31));
+  // Eight indices in flight per thread (one dependent load per iteration
+  // would make this loop latency-bound).
+  const int nidx = B * k;
+  for (int i0 = threadIdx.x; i0 < nidx; i0 += 8 * blockDim.x) {
+    int j[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x;
+      j[u] = i < nidx ? __ldg(idx + i) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (j[u] >= 0 && j[u] < N) atomicOr(&bits[j[u] >> 5], 1u << (j[u] & 31));
   }
   __syncthreads();
   const int per = (words + blockDim.x - 1) / blockDim.x;

@@ -278,7 +278,11 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
   if (tid == 0) pdl_launch_dependents();
   // Activation columns of this thread: vectors v_m = tid + m T (8 columns each).
   float z[B][V][8];
-  uint4 xraw[B][V];  // the raw fp16 input (predictor rows read y, not LN(y))
+  // The raw fp16 input, for predictor rows fused into a QKV launch (they read
+  // y, not LN(y)); batch-1 launches only (at B = 4 the extra registers would
+  // spill: the predictor's first layer then runs as its own launch).
+  constexpr bool kRaw = (KIND == KIND_QKV && B == 1);
+  uint4 xraw[kRaw ? B : 1][kRaw ? V : 1];
   int it = 0;
   if (has_dot) {
     // --- load x, optional LayerNorm ("Deja Vu" App. C.3: blocks read LN(y)).
@@ -291,10 +295,10 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         const int v = tid + m * T;
 #pragma unroll
         for (int e = 0; e < 8; ++e) z[b][m][e] = 0.f;
-        xraw[b][m] = make_uint4(0, 0, 0, 0);
+        if (kRaw) xraw[kRaw ? b : 0][kRaw ? m : 0] = make_uint4(0, 0, 0, 0);
         if (v < nvec && b < p.B) {
           uint4 xv = *reinterpret_cast<const uint4*>(p.x + (size_t)b * p.d + v * 8);
-          xraw[b][m] = xv;
+          if (kRaw) xraw[kRaw ? b : 0][kRaw ? m : 0] = xv;
           h8_to_f8(xv, z[b][m]);
 #pragma unroll
           for (int e = 0; e < 8; ++e) s1[b] += z[b][m][e];
@@ -408,11 +412,11 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
           for (int m = 0; m < V; ++m) {
             float w[8];
             h8_to_f8(wv[c][m], w);
-            if (raw) {
+            if (kRaw && raw) {
 #pragma unroll
               for (int b = 0; b < B; ++b) {
                 float xf[8];
-                h8_to_f8(xraw[b][m], xf);
+                h8_to_f8(xraw[kRaw ? b : 0][kRaw ? m : 0], xf);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) acc[b] = fmaf(xf[e], w[e], acc[b]);
               }
@@ -892,6 +896,22 @@ int launch_wo(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const ui
                          &grid, true);
   if (rc != DV_OK) return rc;
   return reduce_launch(part, grid, B, d, x, bo, out, stream);
+}
+
+// First predictor layer on the side stream (batch > 1, where it is not fused
+// into the QKV launch): u[b][j] = act(sum_c y[b][c] P1[j][c]), small CTAs that
+// share SMs with the main-stream kernels.
+int launch_pred1_gemv(const uint16_t* y, int B, int d, const uint16_t* P1, int r, int relu,
+                      float* u, int target_ctas, cudaStream_t stream) {
+  const int threads = 256, nw = threads / 32;
+  const int g1 = std::max(1, std::min(target_ctas, (r + 2 * nw - 1) / (2 * nw)));
+  note_launch(DV_TAG_PRED1, 0, stream);
+  if (B == 1)
+    k_gemv<uint16_t, 1, 2><<<g1, threads, 0, stream>>>(y, B, d, P1, r, u, r, relu);
+  else
+    k_gemv<uint16_t, 4, 2><<<g1, threads, 0, stream>>>(y, B, d, P1, r, u, r, relu);
+  note_launch(DV_TAG_PRED1, 1, stream);
+  return cudaGetLastError() == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
 }
 
 // Second predictor layer: scores[b][row] = sum_j u[b][j] P2[row][j].

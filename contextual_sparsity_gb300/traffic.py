@@ -45,15 +45,22 @@ def pred_bytes(d, r, rows):
     return 0 if rows == 0 else r * (d + rows) * E
 
 
-def layer_bytes(w, keep_N=None, keep_H=None, keys=None):
-    """(selected bytes, predictor bytes) of one decode layer of workload w."""
+def layer_bytes(w, keep_N=None, keep_H=None, keys=None, union=None):
+    """(selected bytes, predictor bytes) of one decode layer of workload w.
+
+    At batch B > 1 every row is computed over the union of the B sets
+    ("Deja Vu" App. C.1): `union` = (|U_N|, |U_H|) replaces k_N, k_H for the
+    weight rows, and each sequence reads its own cache rows of the union's
+    units."""
     keep_N = w.keep_N if keep_N is None else keep_N
     keep_H = w.keep_H if keep_H is None else keep_H
     G = w.h // w.h_kv
     kN = k_of(keep_N, w.F)
     kH = k_of(keep_H, w.h_kv)
+    if union is not None:
+        kN, kH = union
     keys = (w.n + 1) if keys is None else keys
     sel = (qkv_bytes(w.d, G, w.dh, kH) + wo_bytes(w.d, G, w.dh, kH) + mlp_bytes(w.d, kN)
-           + kv_bytes(w.dh, kH, keys))
+           + w.B * kv_bytes(w.dh, kH, keys))
     rows = (w.F if keep_N < 1 else 0) + (w.h_kv if keep_H < 1 else 0)
     return sel, pred_bytes(w.d, w.r, rows)
