@@ -74,7 +74,7 @@ def test_opt67b_stack():
     _check_last_layer(m)
 
 
-@pytest.mark.parametrize("kn,kh", [(0.25, 1.0), (1.0, 0.5)])
+@pytest.mark.parametrize("kn,kh", [(0.25, 1.0), (1.0, 0.5), (1.0, 1.0)])
 def test_opt67b_keep_variants(kn, kh):
     m = _step(synth.workload("opt-6.7b", keep_N=kn, keep_H=kh, layers=4))
     _check_last_layer(m)
