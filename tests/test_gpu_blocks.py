@@ -115,7 +115,8 @@ def _mlp_case(wl, d=None, F=None, seed=0, full_bias=True):
 
 @pytest.mark.parametrize("wl,d,F,keep", [("tiny", None, None, 0.25), ("tiny", 264, 520, 0.1),
                                          ("opt-6.7b", None, None, 0.1),
-                                         ("opt-6.7b", None, None, 1.0)])
+                                         ("opt-6.7b", None, None, 1.0),
+                                         ("opt-6.7b", 16384, 512, 0.25)])     # largest d
 @pytest.mark.parametrize("flags", [0, dv.DV_SKIP_INACTIVE])
 def test_mlp_parity(wl, d, F, keep, flags):
     w, W = _mlp_case(wl, d, F)
@@ -160,9 +161,9 @@ def test_mlp_k1_and_masked_form():
         assert rel_err(npf(out[0]), ref) < TOL
 
 
-@pytest.mark.parametrize("B", [2, 4])
-def test_mlp_batch_union(B):
-    w, W = _mlp_case("tiny", d=512, F=2048)
+@pytest.mark.parametrize("B,d", [(2, 512), (4, 512), (4, 12288)])   # 12288: largest d at B = 4
+def test_mlp_batch_union(B, d):
+    w, W = _mlp_case("tiny", d=d, F=2048)
     x = synth.hidden(w, B=B, seed=7)
     rng = np.random.default_rng(B)
     k = 200
@@ -235,6 +236,10 @@ def _run_attn(w, W, K, V, x, n, n_max, sel, flags=dv.DV_NO_RESIDUAL, dev_count=N
     ("tiny", {}, 64, None),                                # all heads
     ("compose", dict(d=512, h=8, h_kv=2, F=64), 300, [1]),  # GQA, 4 query heads per KV head
     ("opt-6.7b", dict(F=64), 200, [0, 5, 31]),
+    ("opt-6.7b", dict(d=16384, h=8, h_kv=8, F=64), 100, [2, 5]),       # largest d
+    ("compose", dict(d=512, h=8, h_kv=4, F=64), 300, [1, 3]),         # 2 query heads per KV head
+    ("compose", dict(d=512, h=16, h_kv=2, F=64), 300, [0, 1]),        # 8 query heads per KV head
+    ("opt-6.7b", dict(d=512, h=4, h_kv=4, F=64), 20000, [2]),         # long range: 3-stage splits
 ])
 def test_attn_parity(wl, over, n, sel):
     w = synth.workload(wl, **over)
@@ -311,6 +316,7 @@ def _kvsel_case(over, n, keep, seed=0, plant=None):
     (dict(h=8, h_kv=2, obs_window=16), 300, 0.125, 150),
     (dict(obs_window=64), 2048, 0.125, None),              # composition shape (32q/8kv x 128)
     (dict(h=8, h_kv=2, obs_window=16), 100, 1.0, None),    # budget covers everything
+    (dict(h=8, h_kv=2, obs_window=16), 300, 0.05, None),   # budget below sinks + window
 ])
 def test_kv_select_parity(over, n, keep, plant):
     w, n_max, K, V, q_obs, q = _kvsel_case(over, n, keep, plant=plant)
