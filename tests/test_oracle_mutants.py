@@ -53,3 +53,39 @@ def test_pins_catch_mutant(name, tmp_path):
                         "tests/test_oracle_pins.py"], cwd=tmp_path, env=env,
                        capture_output=True, text=True, timeout=300)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
+
+
+GATE_MUTANTS = {
+    "gate_no_new_token": ("kv = B * uH * 2 * dh * (tokens + 1) * ELT", "kv = B * uH * 2 * dh * tokens * ELT"),
+    "gate_kv_shared_by_batch": ("kv = B * uH * 2 * dh", "kv = uH * 2 * dh"),
+    "gate_no_predictor": ("return weights + kv + pred", "return weights + kv"),
+    "gate_union_additive": ("return N * (1.0 - (1.0 - k / N) ** B)", "return min(N, k * B)"),
+    "gate_keep_unfloored": ("kN, kH = keep_count(keep_N, F), keep_count(keep_H, h_kv)",
+                            "kN, kH = keep_N * F, keep_H * h_kv"),
+    "gate_budget_ignored": ("tokens = min(float(n), kv_budget) if kv_budget > 0 else keep_KV * n",
+                            "tokens = keep_KV * n"),
+    "gate_dense_linear": ("return math.exp(lys[i] + t * (lys[i + 1] - lys[i]))",
+                          "return ys[i] + t * (ys[i + 1] - ys[i])"),
+    "gate_select_every_step": ("t += linear(n, ctx, select_us) / steps", "t += linear(n, ctx, select_us)"),
+    "gate_cost_unscaled": ("measured_us[DENSE][i] * bytes_at(m, c) / bytes_at(DENSE, c)",
+                           "measured_us[DENSE][i]"),
+    "gate_ties_to_higher": ("key=lambda m: (ts[m], m)", "key=lambda m: (ts[m], -m)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(GATE_MUTANTS))
+def test_gate_pins_catch_mutant(name, tmp_path):
+    old, new = GATE_MUTANTS[name]
+    src = open(os.path.join(ROOT, "oracle", "gate.py")).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    shutil.copytree(os.path.join(ROOT, "oracle"), tmp_path / "oracle",
+                    ignore=shutil.ignore_patterns("*.so", "__pycache__"))
+    (tmp_path / "oracle" / "gate.py").write_text(src.replace(old, new))
+    os.makedirs(tmp_path / "tests")
+    for f in ("conftest.py", "test_gate_pins.py"):
+        shutil.copy(os.path.join(ROOT, "tests", f), tmp_path / "tests" / f)
+    env = dict(os.environ, PYTHONPATH=str(tmp_path))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        "tests/test_gate_pins.py"], cwd=tmp_path, env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
