@@ -16,6 +16,7 @@ its own copy of the workload on its own GPU; no data-path collective.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -61,6 +62,12 @@ def parse():
                     help="main,side,main_ring_kb,side_ring_kb,attn,pdl,stage_kb (see dv_set_tuning)")
     ap.add_argument("--timeline", type=int, default=0,
                     help="print start/end of the first N launches of a profiled step to stderr")
+    ap.add_argument("--gate", action="store_true",
+                    help="calibrate the latency gate on a context sweep and validate it")
+    ap.add_argument("--gate-ctx", default="2048,8192,32768,131072",
+                    help="sweep contexts the gate is calibrated on")
+    ap.add_argument("--gate-val", default="4096,16384,65536",
+                    help="held-out contexts the gate's predictions are checked on")
     return ap.parse_args()
 
 
@@ -570,10 +577,135 @@ def run_ours(a):
     print(json.dumps(out))
 
 
+# ---------------------------------------------------------------------------
+# latency gate: calibrate on a context sweep, validate, dispatch a request mix
+# ---------------------------------------------------------------------------
+GATE_KEEP = {  # (keep_N, keep_H, keep_KV) of each mode over the workload's own keeps
+    dv.MODE_DENSE: lambda w: (1.0, 1.0, 1.0),
+    dv.MODE_ACT: lambda w: (w.keep_N, w.keep_H, 1.0),
+    dv.MODE_KV: lambda w: (1.0, 1.0, w.keep_KV),
+    dv.MODE_COMPOSED: lambda w: (w.keep_N, w.keep_H, w.keep_KV),
+}
+
+# Requests of a mixed workload ("Where Activation Sparsity and KV-Cache
+# Sparsity Cross in LLM Decoding" §5.4, App. I: chat turns, questions over long
+# documents, agent loops): (context, decode steps, count).
+GATE_MIX = [(2048, 256, 6), (4096, 128, 6), (8192, 64, 4), (16384, 64, 4), (32768, 256, 3),
+            (65536, 128, 2), (131072, 256, 2)]
+
+
+def _time_mode(w, dev, steps, warmup):
+    """Per-layer µs of one graph-replayed decode step, and the scoring pass per
+    layer (modes that select KV)."""
+    m = Model(w, dev, lookahead=True, kv_dense=w.keep_KV >= 1.0)
+    stream = torch.cuda.Stream(device=dev)
+    g, _ = m.capture(stream)
+    for _ in range(max(3, warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    assert m.st.item() == 0, f"device status {m.st.item()}"
+    us = e0.elapsed_time(e1) * 1e3 / (steps * w.layers)
+    sel = (m.select_ms * 1e3 / w.layers) if m.select_ms is not None else 0.0
+    del m, g
+    torch.cuda.empty_cache()
+    return us, sel
+
+
+def _measured_crossing(ctx, ta, tb):
+    """Between the last context where a leads and the first where b leads,
+    the linear zero of t_a - t_b (None if neither overtakes the other)."""
+    for i in range(len(ctx) - 1):
+        d0, d1 = ta[i] - tb[i], ta[i + 1] - tb[i + 1]
+        if (d0 < 0 <= d1) or (d0 > 0 >= d1):
+            return ctx[i] + d0 / (d0 - d1) * (ctx[i + 1] - ctx[i])
+    return None
+
+
+def run_gate(a):
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dvbuild.build()
+    dv.lib()
+    base = workload(a)
+    cal = [int(x) for x in a.gate_ctx.split(",")]
+    val = [int(x) for x in a.gate_val.split(",")]
+    every = sorted(set(cal) | set(val) | {c for c, _, _ in GATE_MIX})
+    steps = max(5, min(a.steps, 50))
+    T = {m: {} for m in range(4)}
+    S = {}
+    for n in every:
+        for m in range(4):
+            kn, kh, kkv = GATE_KEEP[m](base)
+            w = dataclasses.replace(base, n=n, keep_N=kn, keep_H=kh, keep_KV=kkv)
+            T[m][n], sel = _time_mode(w, dev, steps, a.warmup)
+            if sel:
+                S.setdefault(n, []).append(sel)
+        print(f"[gate] n {n}: " + ", ".join(f"{dv.MODES[m]} {T[m][n]:.1f}" for m in range(4))
+              + f" us/layer, scoring {statistics.mean(S[n]):.0f} us/layer", file=sys.stderr, flush=True)
+    sel_us = {n: float(statistics.mean(v)) for n, v in S.items()}
+    D = dv.dims(base.d, base.h, base.h_kv, base.dh, base.F, base.r, 1)
+    keep = dv.Keep(base.keep_N, base.keep_H, base.keep_KV)
+    cm = dv.cost_calibrate(D, keep, dv.request(), [float(c) for c in cal],
+                           [[T[m][c] for c in cal] for m in range(4)], [sel_us[c] for c in cal])
+    per_step = dv.request(steps=10**9)   # per-step times, the scoring pass left out
+    checks = []
+    for n in val:
+        p = dv.plan_decode(D, keep, per_step, cm, float(n))
+        checks.append({"n": n, "measured_us": [round(T[m][n], 2) for m in range(4)],
+                       "predicted_us": [round(x, 2) for x in p["us"]],
+                       "err_pct": [round(100 * (p["us"][m] / T[m][n] - 1), 2) for m in range(4)]})
+    pairs = [(dv.MODE_DENSE, dv.MODE_ACT), (dv.MODE_DENSE, dv.MODE_KV),
+             (dv.MODE_ACT, dv.MODE_KV), (dv.MODE_ACT, dv.MODE_COMPOSED),
+             (dv.MODE_KV, dv.MODE_COMPOSED), (dv.MODE_DENSE, dv.MODE_COMPOSED)]
+    crossings = []
+    for x, y in pairs:
+        pred = dv.plan_crossing(D, keep, per_step, cm, x, y, float(every[0]), float(every[-1]))
+        meas = _measured_crossing(every, [T[x][n] for n in every], [T[y][n] for n in every])
+        crossings.append({"modes": f"{dv.MODES[x]}/{dv.MODES[y]}",
+                          "predicted": None if pred is None else round(pred),
+                          "measured": None if meas is None else round(meas)})
+    # dispatch: each request runs its decode steps in one mode, paying the
+    # scoring pass once if that mode selects KV
+    def cost(mode, n, st):
+        return st * T[mode][n] + (sel_us[n] if mode in (dv.MODE_KV, dv.MODE_COMPOSED) else 0.0)
+    totals = {name: 0.0 for name in list(dv.MODES) + ["gate"]}
+    picks = []
+    for n, st, count in GATE_MIX:
+        choice = dv.plan_decode(D, keep, dv.request(steps=st), cm, float(n))["choice"]
+        picks.append({"n": n, "steps": st, "mode": dv.MODES[choice]})
+        for mode in range(4):
+            totals[dv.MODES[mode]] += count * cost(mode, n, st)
+        totals["gate"] += count * cost(choice, n, st)
+    best = sum(count * min(cost(mode, n, st) for mode in range(4))
+                      for n, st, count in GATE_MIX)
+    speedup = {k: round(totals["dense"] / v, 3) for k, v in totals.items()}
+    out = {
+        "metric": "latency_gate", "workload": workload_name(base), "data": "synthetic",
+        "calibration_ctx": cal, "validation_ctx": val, "steps_timed": steps,
+        "us_per_layer": {dv.MODES[m]: {str(n): round(T[m][n], 2) for n in every} for m in range(4)},
+        "scoring_us_per_layer": {str(n): round(v, 1) for n, v in sel_us.items()},
+        "cost_us": {dv.MODES[m]: [round(cm.cost_us[m][i], 2) for i in range(len(cal))]
+                    for m in range(4)},
+        "validation": checks, "crossings": crossings, "dispatch": picks,
+        "mix_speedup_over_dense": speedup,
+        "mix_gate_vs_best_per_request": round(best / totals["gate"], 4),
+    }
+    print(json.dumps(out))
+
+
 def main():
     a = parse()
     if a.impl == "reference":
         run_reference(a)
+    elif a.gate:
+        run_gate(a)
     else:
         run_ours(a)
 

@@ -70,6 +70,26 @@ class Sets(ctypes.Structure):
                 ("scores", _p)]
 
 
+MODE_DENSE, MODE_ACT, MODE_KV, MODE_COMPOSED = 0, 1, 2, 3
+MODES = ("dense", "act", "kv", "composed")
+PLAN_MAX_CTX = 16
+_d = ctypes.c_double
+
+
+class Request(ctypes.Structure):
+    _fields_ = [("B", _i), ("steps", _i), ("union_N", _i), ("union_H", _i), ("kv_budget", _i),
+                ("modes", ctypes.c_uint)]
+
+
+class CostModel(ctypes.Structure):
+    _fields_ = [("n_ctx", _i), ("ctx", _d * PLAN_MAX_CTX), ("dense_us", _d * PLAN_MAX_CTX),
+                ("cost_us", (_d * PLAN_MAX_CTX) * 4), ("select_us", _d * PLAN_MAX_CTX)]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("bytes", _d * 4), ("us", _d * 4), ("choice", _i)]
+
+
 _lib = None
 
 
@@ -103,6 +123,13 @@ def lib():
                                      ctypes.POINTER(LayerWeights), ctypes.POINTER(KvCache), _i, _f,
                                      ctypes.POINTER(Sets), _p, _p, _p, _i, _p, _p, _sz, _p, _p, _p,
                                      _p]
+        _R, _C = ctypes.POINTER(Request), ctypes.POINTER(CostModel)
+        _D, _K = ctypes.POINTER(Dims), ctypes.POINTER(Keep)
+        L.dv_plan_bytes.argtypes = [_D, _K, _R, _d, ctypes.POINTER(_d)]
+        L.dv_cost_calibrate.argtypes = [_D, _K, _R, _i, ctypes.POINTER(_d), ctypes.POINTER(_d),
+                                        ctypes.POINTER(_d), _C]
+        L.dv_plan_decode.argtypes = [_D, _K, _R, _C, _d, ctypes.POINTER(Plan)]
+        L.dv_plan_crossing.argtypes = [_D, _K, _R, _C, _i, _i, _d, _d, ctypes.POINTER(_d)]
         _lib = L
     return _lib
 
@@ -110,7 +137,8 @@ def lib():
 EXPORTED = ["dv_version", "dv_status_string", "dv_workspace_size", "dv_set_tuning", "dv_profile",
             "dv_launch_count", "dv_predict",
             "dv_select_topk", "dv_sparse_mlp", "dv_sparse_attn", "dv_kv_select_attn",
-            "dv_decode_layer", "dv_decode_step", "dv_sparse_mlp_noalloc"]
+            "dv_decode_layer", "dv_decode_step", "dv_sparse_mlp_noalloc", "dv_plan_bytes",
+            "dv_cost_calibrate", "dv_plan_decode", "dv_plan_crossing"]
 
 
 def status_string(code: int) -> str:
@@ -345,3 +373,59 @@ class Step:
                                     _stream(stream), self.side.cuda_stream,
                                     _ev(self.ev_fork), _ev(self.ev_join)),
                "dv_decode_step")
+
+
+# ---------------------------------------------------------------------------
+# latency gate (host-only calls: no device needed)
+# ---------------------------------------------------------------------------
+def request(B=1, steps=1, union_N=0, union_H=0, kv_budget=0, modes=0) -> Request:
+    return Request(B, steps, union_N, union_H, kv_budget, modes)
+
+
+def plan_bytes(D: Dims, keep: Keep, req: Request, n: float) -> list:
+    out = (_d * 4)()
+    _check(lib().dv_plan_bytes(ctypes.byref(D), ctypes.byref(keep), ctypes.byref(req), n, out),
+           "dv_plan_bytes")
+    return list(out)
+
+
+def cost_calibrate(D: Dims, keep: Keep, req: Request, ctx, measured_us, select_us=None) -> CostModel:
+    """measured_us[m][i]: mode m's layer time (µs) at ctx[i]; row 0 = dense."""
+    nc = len(ctx)
+    c = (_d * nc)(*ctx)
+    m = (_d * (4 * nc))(*[float(v) for row in measured_us for v in row])
+    s = (_d * nc)(*select_us) if select_us is not None else None
+    cm = CostModel()
+    _check(lib().dv_cost_calibrate(ctypes.byref(D), ctypes.byref(keep), ctypes.byref(req), nc, c,
+                                   m, s, ctypes.byref(cm)), "dv_cost_calibrate")
+    return cm
+
+
+def cost_model(ctx, dense_us, cost_us, select_us=None) -> CostModel:
+    cm = CostModel()
+    cm.n_ctx = len(ctx)
+    for i, c in enumerate(ctx):
+        cm.ctx[i], cm.dense_us[i] = c, dense_us[i]
+        cm.select_us[i] = 0.0 if select_us is None else select_us[i]
+        for m in range(4):
+            cm.cost_us[m][i] = cost_us[m][i]
+    return cm
+
+
+def plan_decode(D: Dims, keep: Keep, req: Request, cm: CostModel, n: float) -> dict:
+    """Predicted per-layer µs of the four modes at context n and the chosen
+    mode (the fastest admitted one)."""
+    p = Plan()
+    _check(lib().dv_plan_decode(ctypes.byref(D), ctypes.byref(keep), ctypes.byref(req),
+                                ctypes.byref(cm), n, ctypes.byref(p)), "dv_plan_decode")
+    return {"choice": p.choice, "us": list(p.us), "bytes": list(p.bytes)}
+
+
+def plan_crossing(D: Dims, keep: Keep, req: Request, cm: CostModel, a: int, b: int, lo: float,
+                  hi: float):
+    """First context in [lo, hi] where modes a and b are predicted equal, or None."""
+    x = _d()
+    _check(lib().dv_plan_crossing(ctypes.byref(D), ctypes.byref(keep), ctypes.byref(req),
+                                  ctypes.byref(cm), a, b, lo, hi, ctypes.byref(x)),
+           "dv_plan_crossing")
+    return None if x.value < 0 else x.value

@@ -12,7 +12,8 @@
  *        App. C.3 (residual form of a layer).
  *   [BX] "Where Activation Sparsity and KV-Cache Sparsity Cross in LLM
  *        Decoding" (arXiv 2609.33889): §3.2 (branches keep all state),
- *        §4.1 and App. A (attention-scored KV selection, split-K attention).
+ *        §4.1 and App. A (attention-scored KV selection, split-K attention);
+ *        §3.1-3.3, §5.4, App. D (byte account, latency gate, dispatch).
  *
  * Conventions (every entry point):
  *  - fp16 data are IEEE binary16 bit patterns (uint16_t). Accumulation is fp32.
@@ -302,6 +303,97 @@ int dv_decode_step(const dv_dims* dims, const dv_keep* keep, int B, int L,
                    uint16_t* y_out, int flags, int* dev_status, void* ws, size_t ws_bytes,
                    cudaStream_t main, cudaStream_t side, cudaEvent_t ev_fork,
                    cudaEvent_t ev_join);
+
+/* ---- latency gate: choose the decode mode per request --------------------
+ * ([BX] §3.1-3.3, §5.4, App. D, App. I; [DV] §2.3 Eq. 1-2, §4.1, App. C.1.)
+ * Host-only: these take host pointers, make no CUDA call and can run on a
+ * machine without a GPU. A step of one layer over B sequences with n cached
+ * tokens each reads, in fp16 bytes:
+ *   weights  U_H (2 G d_h + 2 d_h) d 2 + U_N 2 d 2      (G = h / h_kv)
+ *   KV       B U_H 2 d_h (t + 1) 2                       (the new token's row included)
+ *   predictor r (d + rows) 2, rows = F [keep->neuron < 1] + h_kv [keep->head < 1]
+ * where the modes take
+ *   DENSE     U_N = F, U_H = h_kv, t = n, no predictor;
+ *   ACT       U_N, U_H = the selected counts k = max(1, floor(keep N)) (B = 1)
+ *             or the union of the B sets (B > 1), t = n, the predictor;
+ *   KV        U_N = F, U_H = h_kv, t = keep->kv n (or min(n, kv_budget));
+ *   COMPOSED  ACT's rows and predictor with KV's t.
+ * n and t are real numbers here (t is not floored), so times and crossings are
+ * continuous in n. Per-layer time of one step in mode m at context n ([BX]
+ * App. D): T_m(n) = D(n) bytes_m(n) / bytes_DENSE(n) + c_m(n)
+ *                   [+ s(n) / steps for KV and COMPOSED: the scoring pass, run
+ *                    once per request, spread over its decode steps]
+ * with D the dense time interpolated piecewise-linearly in (log n, log D)
+ * through the sweep contexts (the end segments extended beyond them), and the
+ * kernel costs c_m and scoring times s interpolated piecewise-linearly in n
+ * (held at the end values beyond them). */
+#define DV_MODE_DENSE 0    /* every weight row, the full cache */
+#define DV_MODE_ACT 1      /* projection branch: selected neurons / units, full cache */
+#define DV_MODE_KV 2       /* every weight row, the retained KV */
+#define DV_MODE_COMPOSED 3 /* selected rows and the retained KV */
+#define DV_PLAN_MAX_CTX 16
+
+typedef struct {
+  int B;          /* sequences decoded together, >= 1 */
+  int steps;      /* decode steps the request runs, >= 1 */
+  int union_N;    /* B > 1: |union of the B neuron sets|, 0..F; 0 = independent
+                     uniform draws: F (1 - (1 - k_N / F)^B) */
+  int union_H;    /* B > 1: the same for attention units, 0..h_kv */
+  int kv_budget;  /* > 0: a fixed budget, t = min(n, kv_budget) ([BX] §3.3:
+                     r_KV = b / n); 0: t = keep->kv n */
+  unsigned modes; /* admitted modes (quality admissibility, [BX] §6): bit m
+                     admits mode m; 0 admits all four */
+} dv_request;
+
+typedef struct {
+  int n_ctx;                          /* sweep contexts, 2..DV_PLAN_MAX_CTX */
+  double ctx[DV_PLAN_MAX_CTX];        /* strictly ascending, > 0 */
+  double dense_us[DV_PLAN_MAX_CTX];   /* DENSE layer time at ctx[i], > 0 */
+  double cost_us[4][DV_PLAN_MAX_CTX]; /* c_m at ctx[i], µs (c_DENSE = 0) */
+  double select_us[DV_PLAN_MAX_CTX];  /* one layer's scoring pass at ctx[i], >= 0 */
+} dv_cost_model;
+
+typedef struct {
+  double bytes[4]; /* bytes_m(n) of one layer's step */
+  double us[4];    /* T_m(n), µs per layer per step */
+  int choice;      /* the admitted mode with the lowest T_m (ties: the lower
+                      mode number); KV and COMPOSED are admitted only for
+                      B == 1, the batch the retained buffers serve */
+} dv_plan;
+
+/* bytes[m] = bytes_m(n) of one layer's step for the four modes (n >= 0).
+ * DV_OK, DV_ERR_NULL, DV_ERR_DIMS (d, h, h_kv, d_h, F >= 1, h % h_kv == 0,
+ * r >= 0; B, steps >= 1; unions in range; kv_budget >= 0; n finite),
+ * DV_ERR_KEEP (a keep ratio outside (0, 1]). */
+int dv_plan_bytes(const dv_dims* dims, const dv_keep* keep, const dv_request* req, double n,
+                  double bytes[4]);
+
+/* Fit the kernel costs of a sweep ([BX] App. D): measured_us [4][n_ctx] holds
+ * each mode's measured layer time at ctx[i] (row DV_MODE_DENSE = the dense
+ * times); out->cost_us[m][i] = measured_us[m][i] - measured_us[0][i]
+ * bytes_m(ctx[i]) / bytes_DENSE(ctx[i]); select_us [n_ctx] (nullable: 0) is
+ * copied. All host arrays. Errors as dv_plan_bytes, plus DV_ERR_DIMS for
+ * n_ctx outside 2..DV_PLAN_MAX_CTX, contexts not ascending or <= 0, a dense
+ * time <= 0, a negative scoring time or a non-finite value. */
+int dv_cost_calibrate(const dv_dims* dims, const dv_keep* keep, const dv_request* req, int n_ctx,
+                      const double* ctx, const double* measured_us, const double* select_us,
+                      dv_cost_model* out);
+
+/* Predict T_m(n) for the four modes at context n > 0 and choose the fastest
+ * admitted one. DV_ERR_UNSUPPORTED if no admitted mode can run (KV-only
+ * admission at B > 1); other errors as dv_cost_calibrate. */
+int dv_plan_decode(const dv_dims* dims, const dv_keep* keep, const dv_request* req,
+                   const dv_cost_model* cm, double n, dv_plan* out);
+
+/* The first context in [n_lo, n_hi] (0 < n_lo < n_hi) where modes a and b take
+ * equal predicted time, T_a(n) = T_b(n) ([BX] App. D: solve for equal branch
+ * latency), to a relative 1e-12; *n_star = -1 if T_a - T_b keeps its sign over
+ * the range. A root is bracketed on 8192 log-spaced points, then bisected, so
+ * two crossings closer than that spacing can be missed. Errors as
+ * dv_plan_decode, DV_ERR_DIMS for a mode outside 0..3 or a == b. */
+int dv_plan_crossing(const dv_dims* dims, const dv_keep* keep, const dv_request* req,
+                     const dv_cost_model* cm, int mode_a, int mode_b, double n_lo, double n_hi,
+                     double* n_star);
 
 #ifdef __cplusplus
 }
