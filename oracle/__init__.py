@@ -326,3 +326,32 @@ def layer(x, W, Kc, Vc, n, head_sel, neuron_idx, scale=None, eps=1e-5):
                    ln_g=W.get("ln2_g"), ln_b=W.get("ln2_b"), eps=eps)
     y = round_fp16(h2d(_h(hmid)) + m)
     return y, hmid, a, m
+
+
+def token_kv(x, W, hkv, dh, eps=1e-5):
+    """k, v of every unit for one token (fp16 [hkv][dh] each): z = LN1(x)
+    projected by W^K, W^V plus biases, rounded as the cache stores them. These
+    are the rows "Deja Vu" §4.2 recomputes from a stored token embedding."""
+    K0 = np.zeros((hkv, 1, dh), np.float16)
+    a = attn_masked(x, W, K0, K0.copy(), 0, None, eps=eps)
+    return a.knew, a.vnew
+
+
+def attn_steps(ys, W, Kc, Vc, n0, sels, scale=None, eps=1e-5):
+    """T decode steps of the head-sparse attention block ("Deja Vu" §2.3 Eq. 2,
+    §4.2). Step t reads input ys[t] with n0 + t cached tokens and attends, for
+    the units in sels[t], over positions 0..n0+t. A step computes k, v only for
+    the units it selects; the units it skips keep a copy of the token's input,
+    and their k, v are computed from that copy before a later step reads them.
+    So every step sees, at every past position, the k, v of that position's own
+    token: this function computes them directly. Returns the per-step outputs
+    (AttnOut) and the completed caches K, V [hkv][n_max][dh] (fp16)."""
+    K = np.array(Kc, dtype=np.float16, copy=True)
+    V = np.array(Vc, dtype=np.float16, copy=True)
+    hkv, dh = K.shape[0], K.shape[2]
+    outs = []
+    for t, (y, sel) in enumerate(zip(ys, sels)):
+        n = n0 + t
+        outs.append(attn_gather(y, W, K, V, n, sel, scale=scale, eps=eps))
+        K[:, n], V[:, n] = token_kv(y, W, hkv, dh, eps=eps)
+    return outs, K, V

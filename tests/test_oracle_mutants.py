@@ -89,3 +89,32 @@ def test_gate_pins_catch_mutant(name, tmp_path):
                         "tests/test_gate_pins.py"], cwd=tmp_path, env=env,
                        capture_output=True, text=True, timeout=300)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
+
+
+PY_MUTANTS = {
+    "steps_position_off_by_one": ("K[:, n], V[:, n] = token_kv(y, W, hkv, dh, eps=eps)",
+                                  "K[:, n - 1], V[:, n - 1] = token_kv(y, W, hkv, dh, eps=eps)"),
+    "steps_skipped_units_left_stale": ("K[:, n], V[:, n] = token_kv(y, W, hkv, dh, eps=eps)",
+                                       "K[sel, n], V[sel, n] = outs[-1].knew[sel], outs[-1].vnew[sel]"),
+    "token_kv_no_layernorm": ("a = attn_masked(x, W, K0, K0.copy(), 0, None, eps=eps)",
+                              "a = attn_masked(x, W, K0, K0.copy(), 0, None, eps=1e30)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_multistep_pins_catch_mutant(name, tmp_path):
+    old, new = PY_MUTANTS[name]
+    src = open(os.path.join(ROOT, "oracle", "__init__.py")).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    shutil.copytree(os.path.join(ROOT, "oracle"), tmp_path / "oracle",
+                    ignore=shutil.ignore_patterns("*.so", "__pycache__"))
+    (tmp_path / "oracle" / "__init__.py").write_text(src.replace(old, new))
+    os.makedirs(tmp_path / "tests")
+    for f in ("conftest.py", "test_oracle_pins.py"):
+        shutil.copy(os.path.join(ROOT, "tests", f), tmp_path / "tests" / f)
+    shutil.copytree(os.path.join(ROOT, "tests", "golden"), tmp_path / "tests" / "golden")
+    env = dict(os.environ, PYTHONPATH=str(tmp_path))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        "tests/test_oracle_pins.py", "-k", "token_kv or attn_steps"],
+                       cwd=tmp_path, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"

@@ -487,3 +487,52 @@ def test_kv_budget():
     assert oracle.kv_budget(2048, 0.125) == 256
     assert oracle.kv_budget(131072, 0.125) == 16384
     assert oracle.kv_budget(100, 0.3) == 30
+
+
+# --------------------------------------------------------------------------
+# multi-step decode with missing K/V ("Deja Vu" §4.2)
+# --------------------------------------------------------------------------
+def _np_layernorm(x, eps=1e-5):
+    x = np.asarray(x, float)
+    mu = x.mean()
+    return (x - mu) / np.sqrt(((x - mu) ** 2).mean() + eps)
+
+
+def test_token_kv_is_the_projection_of_the_normalised_token():
+    # k = fp16(LN(y) W^K^T + b_k), v likewise, computed here with numpy's matmul
+    rng = np.random.default_rng(5)
+    d, hkv, dh = 48, 3, 8
+    W = _attn_weights(d, hkv, hkv, dh, rng, 0.3)
+    W["bk"] = f16(rng.standard_normal(hkv * dh) * 0.1)
+    W["bv"] = f16(rng.standard_normal(hkv * dh) * 0.1)
+    y = f16(rng.standard_normal(d) * 2 + 0.5)
+    z = _np_layernorm(y.astype(float))
+    k_ref = (W["Wk"].astype(float) @ z + W["bk"].astype(float)).astype(F16).reshape(hkv, dh)
+    v_ref = (W["Wv"].astype(float) @ z + W["bv"].astype(float)).astype(F16).reshape(hkv, dh)
+    k, v = oracle.token_kv(y, W, hkv, dh)
+    assert np.array_equal(k, k_ref) and np.array_equal(v, v_ref)
+
+
+def test_attn_steps_cache_rows_come_from_their_own_token():
+    # however the units were selected, position n0 + t ends up holding the k, v
+    # of token t (an off-by-one in the position, a row left at zero or a row
+    # taken from another token fails), and the prefilled rows are untouched
+    rng = np.random.default_rng(6)
+    d, hkv, dh, n0, T = 32, 4, 4, 5, 6
+    W = _attn_weights(d, hkv, hkv, dh, rng, 0.4)
+    K = f16(rng.standard_normal((hkv, n0 + T + 1, dh)))
+    V = f16(rng.standard_normal((hkv, n0 + T + 1, dh)))
+    ys = [f16(rng.standard_normal(d)) for _ in range(T)]
+    sels = [[0], [1, 2], [0], [3], [0, 1, 2, 3], [2]]
+    outs, Kf, Vf = oracle.attn_steps(ys, W, K, V, n0, sels)
+    assert np.array_equal(Kf[:, :n0], K[:, :n0]) and np.array_equal(Vf[:, :n0], V[:, :n0])
+    for t, y in enumerate(ys):
+        z = _np_layernorm(y.astype(float))
+        k_ref = (W["Wk"].astype(float) @ z).astype(F16).reshape(hkv, dh)
+        assert np.array_equal(Kf[:, n0 + t], k_ref)
+    # unit 3 is selected only at step 3: it attends over five filled rows of
+    # its own tokens' keys; the same step with every unit selected at every
+    # earlier step gives it the same output
+    dense = oracle.attn_steps(ys, W, K, V, n0, [[0, 1, 2, 3]] * T)[0]
+    assert _close(outs[3].H[3], dense[3].H[3], atol=TIGHT)
+    assert not np.allclose(outs[3].H[3], 0.0)
