@@ -181,10 +181,21 @@ static int attn_qkv(const uint16_t* x, int B, const dv_dims* D, const dv_layer_w
                     const WsLayout& L, cudaStream_t s, bool pdl) {
   const int G = D->h / D->h_kv;
   const bool ret = (flags & DV_KV_RETAINED) != 0;
+  const bool fill = (flags & DV_KV_FILL) != 0;
+  if (fill) {
+    // [DV] 4.2: the selected units' missing k, v first, from the kept inputs
+    // (the QKV launch below then clears their marks).
+    int rc = launch_kv_fill(kv->y_side, kv->kv_missing, B, D->d, D->h_kv, D->d_h, w->ln1_g,
+                            w->ln1_b, D->ln_eps, w->Wk, w->bk, w->Wv, w->bv, sel, k, dev_count,
+                            kv->K, kv->V, n, D->n_max, st, s, pdl);
+    if (rc != DV_OK) return rc;
+    pdl = true;  // the fill waited for the index list before letting QKV start
+  }
   return launch_qkv(x, B, D->d, G, D->d_h, D->h_kv, w->ln1_g, w->ln1_b, D->ln_eps, w->Wq, w->bq,
                     w->Wk, w->bk, w->Wv, w->bv, sel, k, dev_count, scale, at<float>(ws, L.qbuf),
                     kv->K, kv->V, n, D->n_max, ret ? kv->Kr : nullptr, ret ? kv->Vr : nullptr,
-                    kv->kept_count, kv->b_max, kv->y_side, kv->kv_missing, at<int>(ws, L.cnt),
+                    kv->kept_count, kv->b_max, kv->y_side, kv->kv_missing, fill ? 1 : 0,
+                    at<int>(ws, L.cnt),
                     B * D->h_kv, P1n, D->r, (flags & DV_PRED_RELU) ? 1 : 0, u_out, st,
                     main_ctas(), g_tune.main_ring, s, pdl);
 }
@@ -287,6 +298,11 @@ static int check_kv(const dv_dims* D, const dv_kv_cache* kv, int B, int n, int f
   REQ_PTR(kv->K); REQ_PTR(kv->V);
   OPT_PTR(kv->y_side);
   REQ(n >= 0 && n < D->n_max, DV_ERR_DIMS);
+  if (flags & DV_KV_FILL) {
+    REQ_PTR(kv->y_side);
+    REQ(kv->kv_missing, DV_ERR_NULL);
+    REQ(!(flags & (DV_KV_RETAINED | DV_KV_RESELECT)), DV_ERR_UNSUPPORTED);
+  }
   if (flags & (DV_KV_RETAINED | DV_KV_RESELECT)) {
     REQ(B == 1, DV_ERR_UNSUPPORTED);
     REQ_PTR(kv->Kr); REQ_PTR(kv->Vr);

@@ -22,8 +22,18 @@ int launch_qkv(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const u
                const int32_t* idx, int k, const int32_t* dev_count, float scale, float* qbuf,
                uint16_t* K, uint16_t* V, int n, int n_max, uint16_t* Kr, uint16_t* Vr,
                const int32_t* kept_count, int b_max, uint16_t* y_side, uint32_t* kv_missing,
-               int* zero_cnt, int n_zero, const uint16_t* P1, int n_pred, int relu, float* u_out,
-               int* st, int target_ctas, int ring_budget, cudaStream_t stream, bool pdl);
+               int fill_clear, int* zero_cnt, int n_zero, const uint16_t* P1, int n_pred,
+               int relu, float* u_out, int* st, int target_ctas, int ring_budget,
+               cudaStream_t stream, bool pdl);
+
+// k_fill.cu -------------------------------------------------------------------
+// Missing K/V of the selected units recomputed from the kept inputs.
+int launch_kv_fill(const uint16_t* y_side, const uint32_t* missing, int B, int d, int h_kv,
+                   int dh, const uint16_t* ln_g, const uint16_t* ln_b, float eps,
+                   const uint16_t* Wk, const uint16_t* bk, const uint16_t* Wv,
+                   const uint16_t* bv, const int32_t* idx, int k, const int32_t* dev_count,
+                   uint16_t* K, uint16_t* V, int n, int n_max, int* st, cudaStream_t stream,
+                   bool pdl);
 
 int launch_wo(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const uint16_t* WoT,
               const uint16_t* bo, const int32_t* idx, int k, const int32_t* dev_count,

@@ -1,0 +1,218 @@
+// k_fill.cu -- recompute of missing K/V rows before a decode step (sm_103a).
+//
+// "Deja Vu: Contextual Sparsity for Efficient LLMs at Inference Time", §4.2:
+// a step computes k, v only for the attention units it selects; for the other
+// units the token's input y is kept aside and its k, v are marked missing.
+// When a later step selects such a unit, the missing rows are computed from
+// the kept inputs before that step's attention reads them:
+//   k_t = LN1(y_t) W^K_u^T + b^K_u,  v_t = LN1(y_t) W^V_u^T + b^V_u  (fp16),
+// for every position t of the unit still marked missing.
+//
+// A unit's missing positions are always a suffix [n - depth, n) of the cache:
+// positions are marked when the unit is skipped, and a step that selects the
+// unit fills all of its marks (the marks themselves are cleared by that step's
+// QKV launch, which runs after this kernel). So each CTA finds `depth` by
+// scanning the marks backwards from n - 1, 32 positions per warp step.
+#include "dv_internal.h"
+
+namespace dv {
+
+constexpr int kFillRows = 32;   // K/V rows of one unit per CTA (8 warps x 4 rows)
+constexpr int kFillTok = 2;     // missing tokens per pass (their LN1(y) in shared memory)
+constexpr int kFillThreads = 256;
+
+struct FillParams {
+  const uint16_t* y_side;    // [B][n_max][d]
+  const uint32_t* missing;   // [B][n_max][words]
+  const uint16_t *ln_g, *ln_b;
+  float eps;
+  const uint16_t *Wk, *bk, *Wv, *bv;
+  const int32_t* idx;        // selected units (NULL: all)
+  const int32_t* dev_count;
+  int k, h_kv, dh, d, n, n_max;
+  uint16_t *K, *V;           // [B][h_kv][n_max][dh]
+  int* st;
+};
+
+__global__ void __launch_bounds__(kFillThreads) k_kv_fill(const FillParams p) {
+  extern __shared__ __align__(16) float zs[];  // [kFillTok][d]: LN1 of the pass's tokens
+  __shared__ float red[kFillThreads / 32][kFillTok];
+  __shared__ float stat[kFillTok][2];
+  __shared__ int depth_s;
+  // The marks, the kept inputs and the index list come from earlier kernels.
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_launch_dependents();
+
+  const int rb = blockIdx.x, e = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int kk = p.k;
+  if (p.dev_count) kk = min(kk, *p.dev_count);
+  if (e >= kk) return;
+  const int u = p.idx ? p.idx[e] : e;
+  if (u < 0 || u >= p.h_kv) {
+    if (threadIdx.x == 0) flag(p.st, DV_DEV_BAD_INDEX);
+    return;
+  }
+  const int words = (p.h_kv + 31) >> 5;
+  const uint32_t* marks = p.missing + (size_t)b * p.n_max * words + (u >> 5);
+  const uint32_t bit = 1u << (u & 31);
+  if (warp == 0) {
+    int depth = 0;
+    for (int top = p.n - 1; top >= 0; top -= 32) {
+      const int t = top - lane;
+      const bool miss = t >= 0 && (marks[(size_t)t * words] & bit);
+      const unsigned present = __ballot_sync(0xffffffffu, !miss);
+      if (present) {
+        depth += __ffs(present) - 1;
+        break;
+      }
+      depth += 32;
+    }
+    if (lane == 0) depth_s = depth;
+  }
+  __syncthreads();
+  const int depth = depth_s;
+  if (depth == 0) return;
+
+  const int d = p.d, nvec = d >> 3;
+  // This warp's 4 rows of the unit's [W^K; W^V] (2 dh rows).
+  const uint16_t* wrow[4];
+  int rrow[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    int row = rb * kFillRows + warp * 4 + r;
+    rrow[r] = row;
+    if (row >= 2 * p.dh) row = 0;  // (no such row: computed, never stored)
+    const bool isk = row < p.dh;
+    const int c = isk ? row : row - p.dh;
+    wrow[r] = (isk ? p.Wk : p.Wv) + ((size_t)u * p.dh + c) * d;
+  }
+
+  for (int t0 = p.n - depth; t0 < p.n; t0 += kFillTok) {
+    const int nt = min(kFillTok, p.n - t0);
+    // --- LN1 of the kept inputs (two passes, fp32: the QKV launch's form)
+    float s1[kFillTok];
+#pragma unroll
+    for (int j = 0; j < kFillTok; ++j) {
+      s1[j] = 0.f;
+      if (j < nt) {
+        const uint16_t* y = p.y_side + ((size_t)b * p.n_max + t0 + j) * d;
+        for (int v = threadIdx.x; v < nvec; v += kFillThreads) {
+          float f[8];
+          h8_to_f8(*reinterpret_cast<const uint4*>(y + v * 8), f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            zs[(size_t)j * d + v * 8 + i] = f[i];
+            s1[j] += f[i];
+          }
+        }
+      }
+      s1[j] = warp_sum(s1[j]);
+      if (lane == 0) red[warp][j] = s1[j];
+    }
+    __syncthreads();
+    if (threadIdx.x < kFillTok) {
+      float t = 0.f;
+      for (int w = 0; w < kFillThreads / 32; ++w) t += red[w][threadIdx.x];
+      stat[threadIdx.x][0] = t / d;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kFillTok; ++j) {
+      float s2 = 0.f;
+      if (j < nt) {
+        const float mu = stat[j][0];
+        for (int i = threadIdx.x; i < d; i += kFillThreads) {
+          const float c = zs[(size_t)j * d + i] - mu;
+          s2 = fmaf(c, c, s2);
+        }
+      }
+      s2 = warp_sum(s2);
+      if (lane == 0) red[warp][j] = s2;
+    }
+    __syncthreads();
+    if (threadIdx.x < kFillTok) {
+      float t = 0.f;
+      for (int w = 0; w < kFillThreads / 32; ++w) t += red[w][threadIdx.x];
+      stat[threadIdx.x][1] = 1.0f / sqrtf(t / d + p.eps);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nt * d; i += kFillThreads) {
+      const int j = i / d, c = i - j * d;
+      const float g = p.ln_g ? h2f(p.ln_g[c]) : 1.f;
+      const float bb = p.ln_b ? h2f(p.ln_b[c]) : 0.f;
+      zs[i] = (zs[i] - stat[j][0]) * stat[j][1] * g + bb;
+    }
+    __syncthreads();
+
+    // --- 4 rows x nt tokens per warp: lanes stride over d, 16 bytes per row
+    float acc[4][kFillTok];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int j = 0; j < kFillTok; ++j) acc[r][j] = 0.f;
+    for (int v = lane; v < nvec; v += 32) {
+      uint4 w[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) w[r] = ld_nc_v4(wrow[r] + v * 8);
+#pragma unroll
+      for (int j = 0; j < kFillTok; ++j) {
+        if (j >= nt) break;
+        const float4 z0 = *reinterpret_cast<const float4*>(zs + (size_t)j * d + v * 8);
+        const float4 z1 = *reinterpret_cast<const float4*>(zs + (size_t)j * d + v * 8 + 4);
+        const float z[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          float f[8];
+          h8_to_f8(w[r], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[r][j] = fmaf(z[i], f[i], acc[r][j]);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int j = 0; j < kFillTok; ++j) acc[r][j] = warp_sum(acc[r][j]);
+    if (lane == 0) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        if (rrow[r] >= 2 * p.dh) continue;
+        const bool isk = rrow[r] < p.dh;
+        const int c = isk ? rrow[r] : rrow[r] - p.dh;
+        const uint16_t* bias = isk ? p.bk : p.bv;
+        const float bv = bias ? h2f(bias[u * p.dh + c]) : 0.f;
+        uint16_t* cache = isk ? p.K : p.V;
+        for (int j = 0; j < nt; ++j)
+          cache[(((size_t)b * p.h_kv + u) * p.n_max + t0 + j) * p.dh + c] = f2h(acc[r][j] + bv);
+      }
+    }
+    __syncthreads();  // the next pass overwrites zs
+  }
+}
+
+int launch_kv_fill(const uint16_t* y_side, const uint32_t* missing, int B, int d, int h_kv,
+                   int dh, const uint16_t* ln_g, const uint16_t* ln_b, float eps,
+                   const uint16_t* Wk, const uint16_t* bk, const uint16_t* Wv,
+                   const uint16_t* bv, const int32_t* idx, int k, const int32_t* dev_count,
+                   uint16_t* K, uint16_t* V, int n, int n_max, int* st, cudaStream_t stream,
+                   bool pdl) {
+  FillParams p{};
+  p.y_side = y_side; p.missing = missing; p.ln_g = ln_g; p.ln_b = ln_b; p.eps = eps;
+  p.Wk = Wk; p.bk = bk; p.Wv = Wv; p.bv = bv; p.idx = idx; p.dev_count = dev_count;
+  p.k = k; p.h_kv = h_kv; p.dh = dh; p.d = d; p.n = n; p.n_max = n_max; p.K = K; p.V = V;
+  p.st = st;
+  const size_t smem = (size_t)kFillTok * d * sizeof(float);
+  if (cudaFuncSetAttribute((const void*)k_kv_fill, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return DV_ERR_LAUNCH;
+  dim3 grid((2 * dh + kFillRows - 1) / kFillRows, k, B);
+  void* args[] = {&p};
+  note_launch(DV_TAG_KVFILL, 0, stream);
+  const cudaError_t e =
+      launch_k((const void*)k_kv_fill, grid, dim3(kFillThreads), smem, stream, args, pdl);
+  note_launch(DV_TAG_KVFILL, 1, stream);
+  return e == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
+}
+
+}  // namespace dv

@@ -92,6 +92,7 @@ struct StreamParams {
   int b_max;
   uint16_t* y_side;
   uint32_t* kv_missing;
+  int fill_clear;         // QKV: the selected units' missing K/V were just recomputed
   // predictor first layer: P1 rows streamed after the QKV rows (look-ahead,
   // on the raw layer input) or alone (KIND_P1)
   const uint16_t* P1;
@@ -514,6 +515,25 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
           }
       }
     }
+    if (KIND == KIND_QKV && blockIdx.x == 0 && p.fill_clear && p.kv_missing) {
+      // The recompute that ran right before this launch filled every marked
+      // position of the selected units ("Deja Vu" §4.2): clear those marks.
+      // A unit's marks are a suffix of the positions; scan back from n - 1.
+      const int words = (p.h_kv + 31) / 32;
+      for (int be = warp; be < p.B * kk; be += nwc) {
+        const int b = be / kk, e = be % kk;
+        const int u = p.idx ? p.idx[e] : e;
+        if (u < 0 || u >= p.h_kv) continue;
+        uint32_t* marks = p.kv_missing + (size_t)b * p.n_max * words + (u >> 5);
+        const uint32_t bit = 1u << (u & 31);
+        for (int top = p.n - 1; top >= 0; top -= 32) {
+          const int t = top - lane;
+          const bool miss = t >= 0 && (marks[(size_t)t * words] & bit);
+          if (miss) atomicAnd(&marks[(size_t)t * words], ~bit);
+          if (__ballot_sync(0xffffffffu, !miss)) break;
+        }
+      }
+    }
     if (skip) {
       consumer_sync(T);
       if (tid == 0) {
@@ -868,9 +888,11 @@ int launch_qkv(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const u
                const int32_t* idx, int k, const int32_t* dev_count, float scale, float* qbuf,
                uint16_t* K, uint16_t* V, int n, int n_max, uint16_t* Kr, uint16_t* Vr,
                const int32_t* kept_count, int b_max, uint16_t* y_side, uint32_t* kv_missing,
-               int* zero_cnt, int n_zero, const uint16_t* P1, int n_pred, int relu, float* u_out,
-               int* st, int target_ctas, int ring_budget, cudaStream_t stream, bool pdl) {
+               int fill_clear, int* zero_cnt, int n_zero, const uint16_t* P1, int n_pred,
+               int relu, float* u_out, int* st, int target_ctas, int ring_budget,
+               cudaStream_t stream, bool pdl) {
   StreamParams p{};
+  p.fill_clear = fill_clear;
   p.zero_cnt = zero_cnt; p.n_zero = n_zero;
   p.P1 = P1; p.n_pred = P1 ? n_pred : 0; p.relu = relu; p.u_out = u_out;
   p.d = d; p.B = B; p.x = x; p.ln_g = ln_g; p.ln_b = ln_b; p.eps = eps;

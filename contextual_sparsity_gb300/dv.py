@@ -30,6 +30,7 @@ DV_KV_RETAINED = 1 << 6
 DV_KV_ADVANCE = 1 << 7
 DV_JOIN = 1 << 8
 DV_NO_RESIDUAL = 1 << 9
+DV_KV_FILL = 1 << 10
 
 _p = ctypes.c_void_p
 _i = ctypes.c_int
@@ -315,7 +316,7 @@ def decode_step(D: Dims, keep: Keep, Ws: list, kvs: list, n, sets2: list, y_in, 
 # Launch accounting (aux)
 # ---------------------------------------------------------------------------
 TAGS = {0: "qkv", 1: "splitk", 2: "wo", 3: "reduce", 4: "mlp", 5: "pred1", 6: "pred2", 7: "topk",
-        8: "union", 9: "combine", 10: "kvsel", 11: "kvappend", 12: "kvadvance"}
+        8: "union", 9: "combine", 10: "kvsel", 11: "kvappend", 12: "kvadvance", 13: "kvfill"}
 
 
 class Profiler:

@@ -79,6 +79,8 @@ extern "C" {
 #define DV_NO_RESIDUAL (1u << 9)   /* MLP / attention block: out = block output, without
                                       the residual x (the parallel form of [DV] App. C.3,
                                       y + MHA(y) + MLP(y), sums block outputs) */
+#define DV_KV_FILL (1u << 10)      /* attention: first recompute the missing k, v of the
+                                      selected units from y_side ([DV] §4.2) */
 
 /* ---- shapes ------------------------------------------------------------ */
 typedef struct {
@@ -182,6 +184,7 @@ int dv_set_tuning(int main_ctas, int side_ctas, int main_ring_kb, int side_ring_
 #define DV_TAG_KVSEL 10
 #define DV_TAG_KVAPPEND 11
 #define DV_TAG_KVADVANCE 12
+#define DV_TAG_KVFILL 13
 int dv_profile(cudaEvent_t* events, int* tags, int cap);
 long long dv_launch_count(void);
 
@@ -241,6 +244,15 @@ int dv_sparse_mlp_noalloc(const uint16_t* x, int B, const dv_dims* dims,
  * out[b] = x[b] + sum_{query heads j of selected units} H_j WoT_j + bo.
  * Unselected units get no k, v at slot n: their kv_missing bit is set and
  * y_side[b][n] = x[b] (when those pointers are given).
+ * With DV_KV_FILL (y_side and kv_missing required; not with DV_KV_RETAINED or
+ * DV_KV_RESELECT): before the step reads the cache, every selected unit u
+ * gets, for each position t < n whose kv_missing bit of u is set, k and v
+ * recomputed from the kept input: z = LN1(y_side[b][t]), K[b][u][t] =
+ * fp16(z W^K_u^T + bk_u), V likewise ([DV] §4.2: load the stored embeddings
+ * and compute the missing keys and values); the bits are then cleared. A
+ * unit's set bits must form a suffix t0..n-1 of the positions, which holds
+ * when every step since the cache was complete ran with DV_KV_FILL (a step
+ * that selects a unit fills all of its holes).
  * With DV_KV_RETAINED (batch 1): the new k, v also go to Kr/Vr[u][kept_count[u]]
  * and attention reads Kr/Vr[u][0..kept_count[u]] instead of the cache; with
  * DV_KV_ADVANCE the kept counts then grow by one.

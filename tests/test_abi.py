@@ -118,6 +118,10 @@ def test_attention_and_layer_validation(L):
     assert a(*args(n=-1)) == dv.DV_ERR_DIMS
     assert a(*args(k=5)) == dv.DV_ERR_K
     assert a(*args(flags=dv.DV_KV_RETAINED)) == dv.DV_ERR_NULL   # no retained buffers
+    assert a(*args(flags=dv.DV_KV_FILL)) == dv.DV_ERR_NULL       # no kept inputs / marks
+    kv_f = dv.KvCache(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64)
+    assert a(*args(flags=dv.DV_KV_FILL | dv.DV_KV_RETAINED, kvp=kv_f)) == dv.DV_ERR_UNSUPPORTED
+    assert a(*args(flags=dv.DV_KV_FILL, kvp=kv_f)) == dv.DV_ERR_WORKSPACE
     assert a(*args()) == dv.DV_ERR_WORKSPACE
     keep = dv.Keep(0.0, 0.5, 1.0)
     lay = L.dv_decode_layer

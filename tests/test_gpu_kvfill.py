@@ -1,0 +1,118 @@
+"""Multi-step decode with head sparsity: the missing k, v of skipped units are
+recomputed from the kept inputs before a later step reads them ("Deja Vu"
+§4.2), through the C ABI (dv_sparse_attn with DV_KV_FILL), against the
+oracle's multi-step attention, which computes every past token's k, v from
+that token's own input."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from contextual_sparsity_gb300 import dv, synth
+from gpu_helpers import TOL, host, np16, npf, rel_err, setup_lib, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _schedule(kind, hkv, T, rng):
+    """Selected units of every step."""
+    if kind == "designed":
+        # unit 0 every step; unit 1 only at the last step; unit 2 every other
+        # step; unit 3 at steps 0, 5 and 6; the rest at random
+        sels = []
+        for t in range(T):
+            s = {0}
+            if t == T - 1:
+                s.add(1)
+            if t % 2 == 0:
+                s.add(2)
+            if t in (0, 5, 6):
+                s.add(3)
+            for u in range(4, hkv):
+                if rng.random() < 0.5:
+                    s.add(u)
+            sels.append(sorted(s))
+        return sels
+    if kind == "deep":
+        # unit 1 at step 0 and then only at the last step (a hole run longer
+        # than 32 positions); unit 2 first selected at the last step
+        sels = [[0, 1] if t == 0 else [0] for t in range(T)]
+        sels[-1] = [0, 1, 2]
+        return sels
+    k = max(1, hkv // 2)
+    return [sorted(rng.choice(hkv, k, replace=False).tolist()) for _ in range(T)]
+
+
+@pytest.mark.parametrize("wl,over,n0,T,kind", [
+    ("tiny", {}, 40, 12, "designed"),
+    ("tiny", {}, 10, 45, "deep"),
+    ("compose", dict(d=512, h=8, h_kv=2, F=64), 100, 8, "random"),      # GQA, 4 heads per unit
+    ("opt-6.7b", dict(F=64), 200, 6, "random"),                          # d 4096, 32 units
+    ("opt-6.7b", dict(d=1024, h=40, h_kv=40, dh=64, F=64), 60, 10, "random"),  # two mark words
+    ("tiny", {}, 0, 9, "designed"),                                      # no prefill at all
+])
+def test_multistep_missing_kv_recompute(wl, over, n0, T, kind):
+    setup_lib()
+    w = synth.workload(wl, **over)
+    rng = np.random.default_rng(n0 + T)
+    W = synth.layer_weights(w, 0, seed=3, full_bias=True)
+    n_max = n0 + T + 3
+    K, V = synth.kv_cache(w, 0, n_max, B=1, seed=3)
+    ys = [synth.hidden(w, B=1, seed=100 + t) for t in range(T)]
+    sels = _schedule(kind, w.h_kv, T, rng)
+
+    D = dv.dims(w.d, w.h, w.h_kv, w.dh, w.F, w.r, n_max)
+    ws = dv.workspace(D, 1)
+    Kd, Vd = K.cuda(), V.cuda()
+    y_side = torch.zeros(1, n_max, w.d, dtype=torch.float16, device="cuda")
+    words = (w.h_kv + 31) // 32
+    miss = torch.zeros(1, n_max, words, dtype=torch.int32, device="cuda")
+    kv = dv.kv_cache(Kd, Vd, y_side=y_side, kv_missing=miss)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Wd = to_dev(W)
+    outs = []
+    for t in range(T):
+        out = torch.empty(1, w.d, dtype=torch.float16, device="cuda")
+        sd = torch.tensor(sels[t], dtype=torch.int32, device="cuda")
+        dv.sparse_attn(ys[t].cuda(), D, Wd, sd, len(sels[t]), kv, n0 + t, out, ws,
+                       flags=dv.DV_NO_RESIDUAL | dv.DV_KV_FILL, dev_status=st)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+
+    Wh = host(W)
+    ref, Kf, Vf = oracle.attn_steps([np16(y[0]) for y in ys], Wh, np16(K[0]), np16(V[0]), n0,
+                                    sels)
+    for t in range(T):
+        assert rel_err(npf(outs[t][0]), ref[t].delta) < TOL, t
+
+    # marks: after the last step, unit u is marked exactly on the positions
+    # after its last selection; everything else holds its own token's k, v
+    bits = miss[0].cpu().numpy().view(np.uint32)
+    Kg, Vg = Kd[0].cpu().numpy(), Vd[0].cpu().numpy()
+    n_end = n0 + T
+    for u in range(w.h_kv):
+        last = max([t for t in range(T) if u in sels[t]], default=-1)
+        marked = [(bits[p, u // 32] >> (u % 32)) & 1 for p in range(n_end)]
+        want = [1 if p >= n0 + last + 1 else 0 for p in range(n_end)]
+        want[:n0] = [0] * n0
+        assert marked == want, u
+        filled = list(range(n0 + last + 1)) if last >= 0 else list(range(n0))
+        if filled:
+            assert rel_err(Kg[u, filled].astype(float), Kf[u, filled].astype(float)) < TOL, u
+            assert rel_err(Vg[u, filled].astype(float), Vf[u, filled].astype(float)) < TOL, u
+
+
+def test_fill_needs_the_kept_inputs_and_the_full_cache():
+    setup_lib()
+    w = synth.workload("tiny")
+    D = dv.dims(w.d, w.h, w.h_kv, w.dh, w.F, w.r, 16)
+    ws = dv.workspace(D, 1)
+    K = torch.zeros(1, w.h_kv, 16, w.dh, dtype=torch.float16, device="cuda")
+    x = torch.zeros(1, w.d, dtype=torch.float16, device="cuda")
+    out = torch.empty_like(x)
+    W = to_dev(synth.layer_weights(w, 0))
+    kv = dv.kv_cache(K, K.clone())
+    with pytest.raises(dv.DvError) as e:
+        dv.sparse_attn(x, D, W, None, w.h_kv, kv, 4, out, ws, flags=dv.DV_KV_FILL)
+    assert e.value.code in (dv.DV_ERR_NULL, dv.DV_ERR_ALIGN)
