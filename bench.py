@@ -62,6 +62,9 @@ def parse():
                     help="main,side,main_ring_kb,side_ring_kb,attn,pdl,stage_kb (see dv_set_tuning)")
     ap.add_argument("--timeline", type=int, default=0,
                     help="print start/end of the first N launches of a profiled step to stderr")
+    ap.add_argument("--decode-steps", type=int, default=0,
+                    help="time T steps with a growing context, with and without the missing-KV "
+                         "recompute")
     ap.add_argument("--gate", action="store_true",
                     help="calibrate the latency gate on a context sweep and validate it")
     ap.add_argument("--gate-ctx", default="2048,8192,32768,131072",
@@ -206,11 +209,12 @@ class ClockSampler:
 # the workload on the GPU
 # ---------------------------------------------------------------------------
 class Model:
-    def __init__(self, w, device, lookahead=True, seed=0, kv_dense=False):
+    def __init__(self, w, device, lookahead=True, seed=0, kv_dense=False, kept_inputs=False,
+                 fill=False, extra_slots=0):
         self.w = w
         self.L = w.layers
         self.n = w.n
-        self.n_max = w.n + 8
+        self.n_max = w.n + 8 + extra_slots
         self.D = dv.dims(w.d, w.h, w.h_kv, w.dh, w.F, w.r, self.n_max)
         self.keep = dv.Keep(w.keep_N, w.keep_H, w.keep_KV)
         self.kN = traffic.k_of(w.keep_N, w.F)
@@ -255,6 +259,16 @@ class Model:
             e1.record()
             torch.cuda.synchronize()
             self.select_ms = e0.elapsed_time(e1)
+        elif kept_inputs or fill:
+            # "Deja Vu" 4.2: a copy of each token's input and the missing-K/V
+            # marks, so that later steps can recompute what this one skipped
+            words = (w.h_kv + 31) // 32
+            self.y_side = [torch.zeros(w.B, self.n_max, w.d, dtype=torch.float16, device=device)
+                           for _ in range(self.L)]
+            self.kv_miss = [torch.zeros(w.B, self.n_max, words, dtype=torch.int32, device=device)
+                            for _ in range(self.L)]
+            self.kvs = [dv.kv_cache(self.K[l], self.V[l], y_side=self.y_side[l],
+                                    kv_missing=self.kv_miss[l]) for l in range(self.L)]
         else:
             self.kvs = [dv.kv_cache(self.K[l], self.V[l]) for l in range(self.L)]
         self.sets = [dv.sets(w.B, w.F, w.h_kv, self.kN, self.kH, device=device) for _ in range(2)]
@@ -266,22 +280,28 @@ class Model:
         self.evj = dv.event()
         self.st = torch.zeros(1, dtype=torch.int32, device=device)
         flags = (dv.DV_LOOKAHEAD if lookahead else 0) | self.kv_flags
+        if fill:
+            assert not self.retained, "the recompute reads the full cache"
+            flags |= dv.DV_KV_FILL
         self.step = dv.Step(self.D, self.keep, self.W, self.kvs, [s for s, _ in self.sets],
                             self.ws, flags, self.side, self.evf, self.evj, dev_status=self.st)
         # the seeded draws above ran on the current stream; the step runs on others
         torch.cuda.synchronize()
 
-    def capture(self, stream, profiler=None):
+    def capture(self, stream, profiler=None, x=None, n=None, warm=True):
+        x = self.x if x is None else x
+        n = self.n if n is None else n
         g = torch.cuda.CUDAGraph()
         stream.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(stream):
-            self.step(self.x, self.y_tmp, self.y_out, self.n, stream=stream)  # warm, outside capture
+            if warm:
+                self.step(x, self.y_tmp, self.y_out, n, stream=stream)  # warm, outside capture
             torch.cuda.synchronize()
             n0 = dv.launch_count()
             if profiler:
                 profiler.start()
             with torch.cuda.graph(g, stream=stream):
-                self.step(self.x, self.y_tmp, self.y_out, self.n, stream=stream)
+                self.step(x, self.y_tmp, self.y_out, n, stream=stream)
             if profiler:
                 profiler.stop()
             per_step = dv.launch_count() - n0
@@ -628,6 +648,62 @@ def _measured_crossing(ctx, ta, tb):
     return None
 
 
+def run_multistep(a):
+    """T decode steps with a growing context (n, n + 1, ..., n + T - 1), a new
+    input per step, the look-ahead predictor choosing every step's sets: with
+    and without the recompute of the missing K/V ("Deja Vu" 4.2)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dvbuild.build()
+    dv.lib()
+    w = workload(a)
+    T = a.decode_steps
+    xs = [synth.hidden(w, seed=1000 + t, device=dev) for t in range(T)]
+    passes = max(1, a.steps // T)
+    res = {}
+    for fill in (False, True):
+        m = Model(w, dev, lookahead=not a.sync, kept_inputs=True, fill=fill, extra_slots=T)
+        stream = torch.cuda.Stream(device=dev)
+        graphs = [m.capture(stream, x=xs[t], n=w.n + t, warm=(t == 0))[0] for t in range(T)]
+        for _ in range(max(1, a.warmup // T + 1)):
+            for g in graphs:
+                g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(passes):
+                for g in graphs:
+                    g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        assert m.st.item() == 0, f"device status {m.st.item()}"
+        res["fill" if fill else "no_fill"] = e0.elapsed_time(e1) * 1e3 / (passes * T * w.layers)
+        # per-kernel times of the last step, replayed after the T - 1 before it
+        prof = dv.Profiler(cap=64 * w.layers + 64)
+        gp, _ = m.capture(stream, profiler=prof, x=xs[T - 1], n=w.n + T - 1, warm=False)
+        for _ in range(3):
+            for g in graphs[:-1]:
+                g.replay()
+            gp.replay()
+        torch.cuda.synchronize()
+        per_kind = {}
+        for tag, ms in prof.durations_ms():
+            per_kind.setdefault(tag, []).append(ms * 1e3)
+        res["kernel_us_" + ("fill" if fill else "no_fill")] = {
+            k: round(sum(v) / len(v), 2) for k, v in per_kind.items()}
+        del m, graphs, gp
+        torch.cuda.empty_cache()
+        print(f"[multistep] {'fill' if fill else 'no fill'}: "
+              f"{res['fill' if fill else 'no_fill']:.2f} us/layer", file=sys.stderr, flush=True)
+    out = {"metric": "decode_steps_missing_kv", "workload": workload_name(w, not a.sync),
+           "data": "synthetic", "decode_steps": T, "passes": passes,
+           "us_per_layer": {"no_fill": round(res["no_fill"], 2), "fill": round(res["fill"], 2)},
+           "fill_cost_us_per_layer": round(res["fill"] - res["no_fill"], 2),
+           "kernel_us": {"no_fill": res["kernel_us_no_fill"], "fill": res["kernel_us_fill"]}}
+    print(json.dumps(out))
+
+
 def run_gate(a):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -706,6 +782,8 @@ def main():
         run_reference(a)
     elif a.gate:
         run_gate(a)
+    elif a.decode_steps:
+        run_multistep(a)
     else:
         run_ours(a)
 

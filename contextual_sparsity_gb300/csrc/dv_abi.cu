@@ -178,11 +178,11 @@ static T* at(void* ws, size_t off) {
 static int attn_qkv(const uint16_t* x, int B, const dv_dims* D, const dv_layer_weights* w,
                     const int32_t* sel, int k, const int32_t* dev_count, dv_kv_cache* kv, int n,
                     float scale, int flags, const uint16_t* P1n, float* u_out, int* st, void* ws,
-                    const WsLayout& L, cudaStream_t s, bool pdl) {
+                    const WsLayout& L, cudaStream_t s, bool pdl, bool fill_done = false) {
   const int G = D->h / D->h_kv;
   const bool ret = (flags & DV_KV_RETAINED) != 0;
   const bool fill = (flags & DV_KV_FILL) != 0;
-  if (fill) {
+  if (fill && !fill_done) {
     // [DV] 4.2: the selected units' missing k, v first, from the kept inputs
     // (the QKV launch below then clears their marks).
     int rc = launch_kv_fill(kv->y_side, kv->kv_missing, B, D->d, D->h_kv, D->d_h, w->ln1_g,
@@ -492,12 +492,18 @@ int dv_kv_select_attn(const float* q, const dv_dims* dims, dv_kv_cache* kv, int 
   return rc;
 }
 
-int dv_decode_layer(const dv_dims* dims, const dv_keep* keep, int B, const dv_layer_weights* w,
-                    const uint16_t* P1_next, const uint16_t* P2_next, dv_kv_cache* kv, int n,
-                    float softmax_scale, dv_sets* cur, dv_sets* next, const uint16_t* y_in,
-                    uint16_t* y_out, int flags, int* dev_status, void* ws, size_t ws_bytes,
-                    cudaStream_t main, cudaStream_t side, cudaEvent_t ev_fork,
-                    cudaEvent_t ev_join) {
+// One decode layer. With w_next / kv_next (the stacked driver), the missing
+// K/V of the next layer are recomputed on the side stream as soon as its
+// look-ahead sets exist (*side_filled is set), so that work leaves the main
+// stream's path; fill_done says this layer's own recompute already ran there.
+static int decode_layer(const dv_dims* dims, const dv_keep* keep, int B, const dv_layer_weights* w,
+                        const uint16_t* P1_next, const uint16_t* P2_next, dv_kv_cache* kv, int n,
+                        float softmax_scale, dv_sets* cur, dv_sets* next, const uint16_t* y_in,
+                        uint16_t* y_out, int flags, int* dev_status, void* ws, size_t ws_bytes,
+                        cudaStream_t main, cudaStream_t side, cudaEvent_t ev_fork,
+                        cudaEvent_t ev_join, const dv_layer_weights* w_next,
+                        dv_kv_cache* kv_next, bool fill_done, bool* side_filled) {
+  if (side_filled) *side_filled = false;
   int rc = check_dims(dims);
   if (rc != DV_OK) return rc;
   REQ(keep, DV_ERR_NULL);
@@ -553,9 +559,14 @@ int dv_decode_layer(const dv_dims* dims, const dv_keep* keep, int B, const dv_la
   // At batch 1 the next layer's P1 rows ride in this QKV launch; at B > 1
   // they run on the side stream (the fused form would spill registers).
   const bool fuse_p1 = look && B == 1;
+  const bool fill_next = look && w_next && kv_next && (flags & DV_KV_FILL);
+  if (fill_next) {
+    if ((rc = check_kv(dims, kv_next, B, n, flags)) != DV_OK) return rc;
+    if ((rc = check_weights_attn(w_next)) != DV_OK) return rc;
+  }
   rc = attn_qkv(y_in, B, dims, w, selH, kHe, cntH, kv, n, softmax_scale, flags,
                 fuse_p1 ? P1_next : nullptr, at<float>(ws, L.u_side), dev_status, ws, L, main,
-                pdl_qkv);
+                pdl_qkv, fill_done);
   if (rc != DV_OK) return rc;
   if (look) {
     if (cudaEventRecord(ev_fork, main) != cudaSuccess) return DV_ERR_LAUNCH;
@@ -568,6 +579,19 @@ int dv_decode_layer(const dv_dims* dims, const dv_keep* keep, int B, const dv_la
     rc = sets_from_u(dims, B, at<float>(ws, L.u_side), P2_next, kN, nd, kH, hd, next, dev_status,
                      side_ctas(), side);
     if (rc != DV_OK) return rc;
+    if (fill_next) {
+      // [DV] 4.2 + 4.3: the next layer's missing k, v, from its kept inputs,
+      // for the units its look-ahead just selected (small CTAs that fit
+      // beside this layer's streaming CTAs).
+      const int32_t* selHn = hd ? nullptr : (B == 1 ? next->idx_H : next->uH);
+      const int32_t* cntHn = (hd || B == 1) ? nullptr : next->ucnt + 1;
+      rc = launch_kv_fill(kv_next->y_side, kv_next->kv_missing, B, dims->d, dims->h_kv,
+                          dims->d_h, w_next->ln1_g, w_next->ln1_b, dims->ln_eps, w_next->Wk,
+                          w_next->bk, w_next->Wv, w_next->bv, selHn, kHe, cntHn, kv_next->K,
+                          kv_next->V, n, dims->n_max, dev_status, side, false);
+      if (rc != DV_OK) return rc;
+      if (side_filled) *side_filled = true;
+    }
     if (cudaEventRecord(ev_join, side) != cudaSuccess) return DV_ERR_LAUNCH;
   }
   const int32_t* selN = nd ? nullptr : (B == 1 ? cur->idx_N : cur->uN);
@@ -581,6 +605,17 @@ int dv_decode_layer(const dv_dims* dims, const dv_keep* keep, int B, const dv_la
   return launch_status();
 }
 
+int dv_decode_layer(const dv_dims* dims, const dv_keep* keep, int B, const dv_layer_weights* w,
+                    const uint16_t* P1_next, const uint16_t* P2_next, dv_kv_cache* kv, int n,
+                    float softmax_scale, dv_sets* cur, dv_sets* next, const uint16_t* y_in,
+                    uint16_t* y_out, int flags, int* dev_status, void* ws, size_t ws_bytes,
+                    cudaStream_t main, cudaStream_t side, cudaEvent_t ev_fork,
+                    cudaEvent_t ev_join) {
+  return decode_layer(dims, keep, B, w, P1_next, P2_next, kv, n, softmax_scale, cur, next, y_in,
+                      y_out, flags, dev_status, ws, ws_bytes, main, side, ev_fork, ev_join,
+                      nullptr, nullptr, false, nullptr);
+}
+
 int dv_decode_step(const dv_dims* dims, const dv_keep* keep, int B, int L,
                    const dv_layer_weights* w, dv_kv_cache* kv, int n, float softmax_scale,
                    dv_sets* sets, const uint16_t* y_in, uint16_t* y_tmp, uint16_t* y_out, int flags,
@@ -592,6 +627,7 @@ int dv_decode_step(const dv_dims* dims, const dv_keep* keep, int B, int L,
   if (L > 1) REQ_PTR(y_tmp);
   const bool look = (flags & DV_LOOKAHEAD) != 0;
   const uint16_t* cur_in = y_in;
+  bool filled = false;  // this layer's missing K/V were recomputed on the side stream
   for (int l = 0; l < L; ++l) {
     uint16_t* dst = (l == L - 1) ? y_out : y_tmp + (size_t)(l & 1) * B * dims->d;
     int f = flags & ~(DV_SYNC_PREDICT | DV_JOIN | DV_LOOKAHEAD);
@@ -599,11 +635,14 @@ int dv_decode_step(const dv_dims* dims, const dv_keep* keep, int B, int L,
     if (look && l > 0) f |= DV_JOIN;
     const bool has_next = look && (l + 1 < L);
     if (has_next) f |= DV_LOOKAHEAD;
-    int rc = dv_decode_layer(dims, keep, B, &w[l], has_next ? w[l + 1].P1 : nullptr,
-                             has_next ? w[l + 1].P2 : nullptr, &kv[l], n, softmax_scale,
-                             &sets[l & 1], &sets[(l + 1) & 1], cur_in, dst, f, dev_status, ws,
-                             ws_bytes, main, side, ev_fork, ev_join);
+    bool filled_next = false;
+    int rc = decode_layer(dims, keep, B, &w[l], has_next ? w[l + 1].P1 : nullptr,
+                          has_next ? w[l + 1].P2 : nullptr, &kv[l], n, softmax_scale,
+                          &sets[l & 1], &sets[(l + 1) & 1], cur_in, dst, f, dev_status, ws,
+                          ws_bytes, main, side, ev_fork, ev_join, has_next ? &w[l + 1] : nullptr,
+                          has_next ? &kv[l + 1] : nullptr, filled, &filled_next);
     if (rc != DV_OK) return rc;
+    filled = filled_next;
     cur_in = dst;
   }
   return DV_OK;

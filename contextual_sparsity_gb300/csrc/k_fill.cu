@@ -6,7 +6,9 @@
 // When a later step selects such a unit, the missing rows are computed from
 // the kept inputs before that step's attention reads them:
 //   k_t = LN1(y_t) W^K_u^T + b^K_u,  v_t = LN1(y_t) W^V_u^T + b^V_u  (fp16),
-// for every position t of the unit still marked missing.
+// for every position t of the unit still marked missing. LN1(y_t) is held in
+// shared memory as fp16 (two tokens per pass), so the recomputed rows can
+// differ from the QKV launch's fp32 form in the last bit.
 //
 // A unit's missing positions are always a suffix [n - depth, n) of the cache:
 // positions are marked when the unit is skipped, and a step that selects the
@@ -17,8 +19,11 @@
 
 namespace dv {
 
-constexpr int kFillRows = 32;   // K/V rows of one unit per CTA (8 warps x 4 rows)
-constexpr int kFillTok = 2;     // missing tokens per pass (their LN1(y) in shared memory)
+constexpr int kFillRows = 16;   // K/V rows of one unit per CTA (8 warps x 2 rows)
+constexpr int kFillRowsW = 2;   // rows per warp
+constexpr int kFillUnroll = 4;  // 16-byte loads per row in flight per lane
+constexpr int kFillTok = 2;     // missing tokens per pass (their LN1(y) in shared memory, fp16)
+constexpr int kFillGroups = 4;  // CTAs that split a unit's passes between them
 constexpr int kFillThreads = 256;
 
 struct FillParams {
@@ -34,8 +39,11 @@ struct FillParams {
   int* st;
 };
 
-__global__ void __launch_bounds__(kFillThreads) k_kv_fill(const FillParams p) {
-  extern __shared__ __align__(16) float zs[];  // [kFillTok][d]: LN1 of the pass's tokens
+// <= 64 registers and 2 d bytes of shared memory per token slot (48 KB at
+// d = 12288), so that a CTA fits beside a weight-streaming CTA when the
+// recompute runs on the side stream.
+__global__ void __launch_bounds__(kFillThreads, 4) k_kv_fill(const FillParams p) {
+  extern __shared__ __align__(16) uint16_t zs[];  // [kFillTok][d]: LN1 of the pass's tokens
   __shared__ float red[kFillThreads / 32][kFillTok];
   __shared__ float stat[kFillTok][2];
   __shared__ int depth_s;
@@ -43,7 +51,8 @@ __global__ void __launch_bounds__(kFillThreads) k_kv_fill(const FillParams p) {
   pdl_wait();
   if (threadIdx.x == 0) pdl_launch_dependents();
 
-  const int rb = blockIdx.x, e = blockIdx.y, b = blockIdx.z;
+  const int rb = blockIdx.x, e = blockIdx.y;
+  const int b = blockIdx.z / kFillGroups, grp = blockIdx.z % kFillGroups;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int kk = p.k;
   if (p.dev_count) kk = min(kk, *p.dev_count);
@@ -75,12 +84,12 @@ __global__ void __launch_bounds__(kFillThreads) k_kv_fill(const FillParams p) {
   if (depth == 0) return;
 
   const int d = p.d, nvec = d >> 3;
-  // This warp's 4 rows of the unit's [W^K; W^V] (2 dh rows).
-  const uint16_t* wrow[4];
-  int rrow[4];
+  // This warp's rows of the unit's [W^K; W^V] (2 dh rows).
+  const uint16_t* wrow[kFillRowsW];
+  int rrow[kFillRowsW];
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    int row = rb * kFillRows + warp * 4 + r;
+  for (int r = 0; r < kFillRowsW; ++r) {
+    int row = rb * kFillRows + warp * kFillRowsW + r;
     rrow[r] = row;
     if (row >= 2 * p.dh) row = 0;  // (no such row: computed, never stored)
     const bool isk = row < p.dh;
@@ -88,9 +97,11 @@ __global__ void __launch_bounds__(kFillThreads) k_kv_fill(const FillParams p) {
     wrow[r] = (isk ? p.Wk : p.Wv) + ((size_t)u * p.dh + c) * d;
   }
 
-  for (int t0 = p.n - depth; t0 < p.n; t0 += kFillTok) {
+  // Passes of kFillTok tokens; the kFillGroups CTAs of a row block take
+  // every kFillGroups-th pass.
+  for (int t0 = p.n - depth + grp * kFillTok; t0 < p.n; t0 += kFillGroups * kFillTok) {
     const int nt = min(kFillTok, p.n - t0);
-    // --- LN1 of the kept inputs (two passes, fp32: the QKV launch's form)
+    // --- LN1 of the kept inputs (two passes over the stored fp16 rows)
     float s1[kFillTok];
 #pragma unroll
     for (int j = 0; j < kFillTok; ++j) {
@@ -98,13 +109,12 @@ __global__ void __launch_bounds__(kFillThreads) k_kv_fill(const FillParams p) {
       if (j < nt) {
         const uint16_t* y = p.y_side + ((size_t)b * p.n_max + t0 + j) * d;
         for (int v = threadIdx.x; v < nvec; v += kFillThreads) {
+          const uint4 yv = *reinterpret_cast<const uint4*>(y + v * 8);
+          *reinterpret_cast<uint4*>(zs + (size_t)j * d + v * 8) = yv;
           float f[8];
-          h8_to_f8(*reinterpret_cast<const uint4*>(y + v * 8), f);
+          h8_to_f8(yv, f);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            zs[(size_t)j * d + v * 8 + i] = f[i];
-            s1[j] += f[i];
-          }
+          for (int i = 0; i < 8; ++i) s1[j] += f[i];
         }
       }
       s1[j] = warp_sum(s1[j]);
@@ -122,9 +132,14 @@ __global__ void __launch_bounds__(kFillThreads) k_kv_fill(const FillParams p) {
       float s2 = 0.f;
       if (j < nt) {
         const float mu = stat[j][0];
-        for (int i = threadIdx.x; i < d; i += kFillThreads) {
-          const float c = zs[(size_t)j * d + i] - mu;
-          s2 = fmaf(c, c, s2);
+        for (int v = threadIdx.x; v < nvec; v += kFillThreads) {
+          float f[8];
+          h8_to_f8(*reinterpret_cast<const uint4*>(zs + (size_t)j * d + v * 8), f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float c = f[i] - mu;
+            s2 = fmaf(c, c, s2);
+          }
         }
       }
       s2 = warp_sum(s2);
@@ -141,42 +156,52 @@ __global__ void __launch_bounds__(kFillThreads) k_kv_fill(const FillParams p) {
       const int j = i / d, c = i - j * d;
       const float g = p.ln_g ? h2f(p.ln_g[c]) : 1.f;
       const float bb = p.ln_b ? h2f(p.ln_b[c]) : 0.f;
-      zs[i] = (zs[i] - stat[j][0]) * stat[j][1] * g + bb;
+      zs[i] = f2h((h2f(zs[i]) - stat[j][0]) * stat[j][1] * g + bb);
     }
     __syncthreads();
 
-    // --- 4 rows x nt tokens per warp: lanes stride over d, 16 bytes per row
-    float acc[4][kFillTok];
+    // --- kFillRowsW rows x nt tokens per warp: lanes stride over d, 16 bytes
+    // per row per step, kFillUnroll steps of loads in flight
+    float acc[kFillRowsW][kFillTok];
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int r = 0; r < kFillRowsW; ++r)
 #pragma unroll
       for (int j = 0; j < kFillTok; ++j) acc[r][j] = 0.f;
-    for (int v = lane; v < nvec; v += 32) {
-      uint4 w[4];
+    for (int v0 = lane; v0 < nvec; v0 += 32 * kFillUnroll) {
+      uint4 w[kFillUnroll][kFillRowsW];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) w[r] = ld_nc_v4(wrow[r] + v * 8);
+      for (int q = 0; q < kFillUnroll; ++q) {
+        const int v = v0 + q * 32;
 #pragma unroll
-      for (int j = 0; j < kFillTok; ++j) {
-        if (j >= nt) break;
-        const float4 z0 = *reinterpret_cast<const float4*>(zs + (size_t)j * d + v * 8);
-        const float4 z1 = *reinterpret_cast<const float4*>(zs + (size_t)j * d + v * 8 + 4);
-        const float z[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+        for (int r = 0; r < kFillRowsW; ++r)
+          w[q][r] = v < nvec ? ld_nc_v4(wrow[r] + v * 8) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          float f[8];
-          h8_to_f8(w[r], f);
+      for (int q = 0; q < kFillUnroll; ++q) {
+        const int v = v0 + q * 32;
+        if (v >= nvec) break;
+        float wf[kFillRowsW][8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[r][j] = fmaf(z[i], f[i], acc[r][j]);
+        for (int r = 0; r < kFillRowsW; ++r) h8_to_f8(w[q][r], wf[r]);
+#pragma unroll
+        for (int j = 0; j < kFillTok; ++j) {
+          if (j >= nt) break;
+          float z[8];
+          h8_to_f8(*reinterpret_cast<const uint4*>(zs + (size_t)j * d + v * 8), z);
+#pragma unroll
+          for (int r = 0; r < kFillRowsW; ++r)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[r][j] = fmaf(z[i], wf[r][i], acc[r][j]);
         }
       }
     }
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int r = 0; r < kFillRowsW; ++r)
 #pragma unroll
       for (int j = 0; j < kFillTok; ++j) acc[r][j] = warp_sum(acc[r][j]);
     if (lane == 0) {
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < kFillRowsW; ++r) {
         if (rrow[r] >= 2 * p.dh) continue;
         const bool isk = rrow[r] < p.dh;
         const int c = isk ? rrow[r] : rrow[r] - p.dh;
@@ -202,11 +227,11 @@ int launch_kv_fill(const uint16_t* y_side, const uint32_t* missing, int B, int d
   p.Wk = Wk; p.bk = bk; p.Wv = Wv; p.bv = bv; p.idx = idx; p.dev_count = dev_count;
   p.k = k; p.h_kv = h_kv; p.dh = dh; p.d = d; p.n = n; p.n_max = n_max; p.K = K; p.V = V;
   p.st = st;
-  const size_t smem = (size_t)kFillTok * d * sizeof(float);
+  const size_t smem = (size_t)kFillTok * d * sizeof(uint16_t);
   if (cudaFuncSetAttribute((const void*)k_kv_fill, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return DV_ERR_LAUNCH;
-  dim3 grid((2 * dh + kFillRows - 1) / kFillRows, k, B);
+  dim3 grid((2 * dh + kFillRows - 1) / kFillRows, k, B * kFillGroups);
   void* args[] = {&p};
   note_launch(DV_TAG_KVFILL, 0, stream);
   const cudaError_t e =
