@@ -118,3 +118,33 @@ def test_multistep_pins_catch_mutant(name, tmp_path):
                         "tests/test_oracle_pins.py", "-k", "token_kv or attn_steps"],
                        cwd=tmp_path, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
+
+
+W4_MUTANTS = {
+    "w4_scale_over_8": ("amax / np.float32(7.0)", "amax / np.float32(8.0)"),
+    "w4_round_half_up": ("np.rint(r)", "np.floor(r + np.float32(0.5))"),
+    "w4_scale_unrounded": ("s32 = s16.astype(np.float32)", "s32 = amax / np.float32(7.0)"),
+    "w4_nibbles_swapped": ("(u[:, 0::2] | (u[:, 1::2] << 4))", "(u[:, 1::2] | (u[:, 0::2] << 4))"),
+    "w4_dequant_no_scale": ("* s16.astype(np.float64)[..., None]).reshape(rows, d)",
+                            "* 1.0).reshape(rows, d)"),
+    "w4_mlp_no_relu": ("a = np.maximum(pre, 0.0)", "a = pre"),
+    "w4_mlp_no_b1": ("pre = pre + np.asarray(b1", "pre = pre + 0 * np.asarray(b1"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(W4_MUTANTS))
+def test_w4_pins_catch_mutant(name, tmp_path):
+    old, new = W4_MUTANTS[name]
+    src = open(os.path.join(ROOT, "oracle", "w4.py")).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    shutil.copytree(os.path.join(ROOT, "oracle"), tmp_path / "oracle",
+                    ignore=shutil.ignore_patterns("*.so", "__pycache__"))
+    (tmp_path / "oracle" / "w4.py").write_text(src.replace(old, new))
+    os.makedirs(tmp_path / "tests")
+    for f in ("conftest.py", "test_w4_pins.py"):
+        shutil.copy(os.path.join(ROOT, "tests", f), tmp_path / "tests" / f)
+    env = dict(os.environ, PYTHONPATH=str(tmp_path))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        "tests/test_w4_pins.py"], cwd=tmp_path, env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
