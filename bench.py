@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--decode-steps", type=int, default=0,
                     help="time T steps with a growing context, with and without the missing-KV "
                          "recompute")
+    ap.add_argument("--w4", action="store_true",
+                    help="time the MLP block with fp16 and with 4-bit weight rows")
     ap.add_argument("--gate", action="store_true",
                     help="calibrate the latency gate on a context sweep and validate it")
     ap.add_argument("--gate-ctx", default="2048,8192,32768,131072",
@@ -704,6 +706,80 @@ def run_multistep(a):
     print(json.dumps(out))
 
 
+def run_w4(a):
+    """The MLP block with fp16 rows and with 4-bit rows (W4A16, "Deja Vu"
+    5.2, Table 7) at the workload's neuron keep, over several layers' weights
+    in turn (so that every launch reads from HBM)."""
+    import numpy as np
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dvbuild.build()
+    dv.lib()
+    w = workload(a)
+    L = min(w.layers, 6)
+    kN = traffic.k_of(w.keep_N, w.F)
+    D = dv.dims(w.d, w.h, w.h_kv, w.dh, w.F, w.r, 8)
+    ws = dv.workspace(D, w.B)
+    x = synth.hidden(w, device=dev)
+    out = torch.empty(w.B, w.d, dtype=torch.float16, device=dev)
+    layers = []
+    for l in range(L):
+        W = synth.layer_weights(w, l, device=dev)
+        W = {k: W[k] for k in ("fc1", "fc2T", "b1", "ln2_g", "ln2_b") if k in W}
+        idx = np.sort(np.random.default_rng(l).choice(w.F, kN, replace=False)).astype(np.int32)
+        layers.append((W, dv.quantize_w4(W["fc1"]), dv.quantize_w4(W["fc2T"]),
+                       torch.from_numpy(idx).to(dev)))
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    stream = torch.cuda.Stream(device=dev)
+    prof_n = 0
+    res = {}
+    for name in ("fp16", "w4"):
+        def one(l):
+            W, q1, q2, idx = layers[l % L]
+            if name == "fp16":
+                dv.sparse_mlp(x, D, W, idx, kN, out, ws, stream=stream)
+            else:
+                dv.sparse_mlp_w4(x, D, W, q1, q2, idx, kN, out, ws, stream=stream)
+        with torch.cuda.stream(stream):
+            for l in range(max(3, a.warmup) * L):
+                one(l)
+        torch.cuda.synchronize()
+        reps = max(L, (a.steps // L) * L)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for l in range(reps):
+                one(l)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        # the streaming kernel alone, event-bracketed
+        prof = dv.Profiler(cap=8 * L + 16)
+        with torch.cuda.stream(stream):
+            prof.start()
+            for l in range(L):
+                one(l)
+            prof.stop()
+        torch.cuda.synchronize()
+        ks = [ms * 1e3 for tag, ms in prof.durations_ms() if tag == "mlp"]
+        res[name] = {"us_per_block": e0.elapsed_time(e1) * 1e3 / reps,
+                     "kernel_us": sum(ks) / len(ks)}
+    pk, pk_src = peaks()
+    row = {"fp16": 2 * w.d, "w4": dv.w4_row_bytes(w.d)}
+    out_j = {"metric": "mlp_block_w4a16", "workload": workload_name(w), "data": "synthetic",
+             "neurons": kN, "layers_rotated": L}
+    for name in ("fp16", "w4"):
+        by = 2 * kN * row[name]
+        kus = res[name]["kernel_us"]
+        out_j[name] = {"us_per_block": round(res[name]["us_per_block"], 2),
+                       "stream_kernel_us": round(kus, 2), "weight_bytes": by,
+                       "gbs": round(by / kus / 1e3, 1),
+                       "frac": round(by / kus / 1e3 / pk, 3), "peak_gbs": pk,
+                       "peak_source": pk_src}
+    out_j["speedup"] = round(res["fp16"]["us_per_block"] / res["w4"]["us_per_block"], 3)
+    print(json.dumps(out_j))
+
+
 def run_gate(a):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -784,6 +860,8 @@ def main():
         run_gate(a)
     elif a.decode_steps:
         run_multistep(a)
+    elif a.w4:
+        run_w4(a)
     else:
         run_ours(a)
 

@@ -423,6 +423,37 @@ int dv_sparse_mlp(const uint16_t* x, int B, const dv_dims* dims, const dv_layer_
   return run_mlp(x, B, dims, w, idx, k, dev_count, flags, out, dev_status, ws, L, stream, false);
 }
 
+size_t dv_w4_row_bytes(int d) { return (d >= 128 && d % 128 == 0) ? w4_row_bytes_host(d) : 0; }
+
+int dv_quantize_w4(const uint16_t* W, int rows, int d, uint8_t* out, cudaStream_t stream) {
+  REQ_PTR(W); REQ_PTR(out);
+  REQ(rows >= 1 && rows <= 65535 && d >= 128 && d % 128 == 0 && d <= 16384, DV_ERR_DIMS);
+  return launch_quant_w4(W, rows, d, out, stream);
+}
+
+int dv_sparse_mlp_w4(const uint16_t* x, int B, const dv_dims* dims, const dv_layer_weights* w,
+                     const uint8_t* fc1_w4, const uint8_t* fc2T_w4, const int32_t* idx, int k,
+                     const int32_t* dev_count, int flags, uint16_t* out, int* dev_status,
+                     void* ws, size_t ws_bytes, cudaStream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != DV_OK) return rc;
+  REQ(dims->d % 128 == 0, DV_ERR_DIMS);
+  REQ_PTR(x); REQ_PTR(out); REQ(ws, DV_ERR_NULL); REQ(aligned(ws, 256), DV_ERR_ALIGN);
+  REQ(w, DV_ERR_NULL);
+  REQ_PTR(fc1_w4); REQ_PTR(fc2T_w4);
+  OPT_PTR(w->b1); OPT_PTR(w->b2); OPT_PTR(w->ln2_g); OPT_PTR(w->ln2_b);
+  REQ(B >= 1 && B <= 4, DV_ERR_DIMS);
+  if (!idx) k = dims->F;
+  REQ(k >= 1 && k <= dims->F, DV_ERR_K);
+  REQ(x != out, DV_ERR_DIMS);
+  const WsLayout L = ws_layout(dims, B, 0);
+  REQ(ws_bytes >= L.total, DV_ERR_WORKSPACE);
+  return launch_mlp_w4(x, B, dims->d, dims->F, w->ln2_g, w->ln2_b, dims->ln_eps, fc1_w4, w->b1,
+                       fc2T_w4, w->b2, idx, k, dev_count,
+                       flags & (DV_SKIP_INACTIVE | DV_NO_RESIDUAL), out, dev_status,
+                       at<float>(ws, L.part), main_ctas(), g_tune.main_ring, stream, false);
+}
+
 int dv_sparse_attn(const uint16_t* x, int B, const dv_dims* dims, const dv_layer_weights* w,
                    const int32_t* head_idx, int k_heads, const int32_t* dev_count,
                    dv_kv_cache* kv, int n, float softmax_scale, int flags, uint16_t* out,

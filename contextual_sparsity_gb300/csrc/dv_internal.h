@@ -26,6 +26,16 @@ int launch_qkv(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const u
                int relu, float* u_out, int* st, int target_ctas, int ring_budget,
                cudaStream_t stream, bool pdl);
 
+int launch_mlp_w4(const uint16_t* x, int B, int d, int F, const uint16_t* ln_g,
+                  const uint16_t* ln_b, float eps, const uint8_t* fc1q, const uint16_t* b1,
+                  const uint8_t* fc2Tq, const uint16_t* b2, const int32_t* idx, int k,
+                  const int32_t* dev_count, int flags, uint16_t* out, int* st, float* part,
+                  int target_ctas, int ring_budget, cudaStream_t stream, bool pdl);
+
+// k_w4.cu ---------------------------------------------------------------------
+size_t w4_row_bytes_host(int d);
+int launch_quant_w4(const uint16_t* W, int rows, int d, uint8_t* out, cudaStream_t stream);
+
 // k_fill.cu -------------------------------------------------------------------
 // Missing K/V of the selected units recomputed from the kept inputs.
 int launch_kv_fill(const uint16_t* y_side, const uint32_t* missing, int B, int d, int h_kv,

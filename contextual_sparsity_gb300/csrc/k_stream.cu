@@ -61,7 +61,40 @@ __host__ __device__ inline void stream_layout(StreamGeom& g) {
 // ---------------------------------------------------------------------------
 // Kernel parameters
 // ---------------------------------------------------------------------------
-enum StreamKind { KIND_MLP = 0, KIND_QKV = 1, KIND_P1 = 2, KIND_WO = 3 };
+enum StreamKind { KIND_MLP = 0, KIND_QKV = 1, KIND_P1 = 2, KIND_WO = 3, KIND_MLP4 = 4 };
+// KIND_MLP4: the MLP with 4-bit weight rows ("Deja Vu" §5.2, Table 7: W4A16).
+// A packed row holds d/2 bytes of codes (column 2i in the low nibble of byte
+// i, code + 8), then the d/128 fp16 group scales, padded to 16 bytes.
+__host__ __device__ constexpr bool is_mlp(int k) { return k == KIND_MLP || k == KIND_MLP4; }
+constexpr int kW4StageRows = 8;  // rows per ring stage for 4-bit rows
+constexpr int kW4Ilp = 4;        // 4-bit rows a consumer works on at once
+constexpr int kW4Threads = 992;  // consumer threads at B = 1 (31 warps + the producer)
+__host__ __device__ inline uint32_t w4_row_bytes(int d) { return (uint32_t)((d / 2 + d / 64 + 15) / 16 * 16); }
+
+// The 8 codes of one 32-bit word as exact floats (q = nibble - 8), in column
+// order: (w >> 4k) & 0x000F000F puts nibbles k and k + 4 into the two halves
+// of a half2 whose bits 0x6400 | n read as 1024 + n; subtracting 1032 leaves
+// n - 8 exactly.
+// The same codes as exact fp16 pairs: h[k] = {q_k, q_{k+4}}.
+DV_DEV void w4_decode_h2(uint32_t w, __half2* h) {
+  const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t b = ((w >> (4 * k)) & 0x000F000Fu) | 0x64006400u;
+    h[k] = __hsub2(*reinterpret_cast<const __half2*>(&b), off);
+  }
+}
+
+DV_DEV void w4_decode(uint32_t w, float* f) {
+  const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t h = ((w >> (4 * k)) & 0x000F000Fu) | 0x64006400u;
+    const float2 t = __half22float2(__hsub2(*reinterpret_cast<const __half2*>(&h), off));
+    f[k] = t.x;
+    f[k + 4] = t.y;
+  }
+}
 
 struct StreamParams {
   StreamGeom g;
@@ -137,11 +170,14 @@ DV_DEV const uint16_t* row_addr(const StreamParams& p, int kind, int phase, int 
     bad = false;
     return p.P1 + (size_t)(v - qkv_rows) * d;
   }
-  if (kind == KIND_MLP || kind == KIND_P1) {
+  if (is_mlp(kind) || kind == KIND_P1) {
     int j = p.idx ? p.idx[v] : v;
     bad = (j < 0 || j >= p.n_rows_total);
     if (bad) j = 0;
-    const uint16_t* base = (kind == KIND_MLP && phase == 1) ? p.W1 : p.W0;
+    const uint16_t* base = (is_mlp(kind) && phase == 1) ? p.W1 : p.W0;
+    if (kind == KIND_MLP4)
+      return reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(base) +
+                                               (size_t)j * w4_row_bytes(p.d));
     return base + (size_t)j * d;
   }
   const int per = rows_per_entry(p, kind);
@@ -158,6 +194,19 @@ DV_DEV const uint16_t* row_addr(const StreamParams& p, int kind, int phase, int 
   return p.W2 + ((size_t)u * p.dh + (r - qrows - p.dh)) * d;
 }
 
+// Vector v (8 columns) of a staged row: 16 bytes of fp16, or for 4-bit rows
+// {the 32-bit word of its 8 codes, its group's fp16 scale}.
+template <int KIND>
+DV_DEV uint4 stage_vec(const uint8_t* row, int v, int d) {
+  if constexpr (KIND == KIND_MLP4) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(row + v * 4);
+    const uint32_t sc = *reinterpret_cast<const uint16_t*>(row + d / 2 + (v >> 4) * 2);
+    return make_uint4(w, sc, 0u, 0u);
+  } else {
+    return *reinterpret_cast<const uint4*>(row + v * 16);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -169,7 +218,8 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
                     const bool has_dot, const bool has_axpy, const bool skip);
 
 template <int KIND, int B, int V>
-__global__ void __launch_bounds__(B == 1 ? 544 : 416, 1) k_stream(const StreamParams p) {
+__global__ void __launch_bounds__((KIND == KIND_MLP4 && B == 1) ? 1024 : (B == 1 ? 544 : 416), 1)
+    k_stream(const StreamParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const StreamGeom& g = p.g;
   const int T = g.T, nwc = T / 32;
@@ -195,8 +245,8 @@ __global__ void __launch_bounds__(B == 1 ? 544 : 416, 1) k_stream(const StreamPa
   const int r1 = (int)(tot_rows * (blockIdx.x + 1) / gridDim.x);
   const int nrows = r1 - r0;
   const bool has_dot = (KIND != KIND_WO);
-  const bool has_axpy = (KIND == KIND_MLP || KIND == KIND_WO);
-  const bool skip = (KIND == KIND_MLP) && (p.flags & DV_SKIP_INACTIVE);
+  const bool has_axpy = (is_mlp(KIND) || KIND == KIND_WO);
+  const bool skip = is_mlp(KIND) && (p.flags & DV_SKIP_INACTIVE);
 
   if (tid == 0) {
     for (int s = 0; s < g.NS; ++s) {
@@ -211,7 +261,64 @@ __global__ void __launch_bounds__(B == 1 ? 544 : 416, 1) k_stream(const StreamPa
   __syncthreads();
 
   // ======================= producer warp =======================
-  if (warp == nwc) {
+  if (warp == nwc && KIND == KIND_MLP4) {
+    // 4-bit rows are short, so one thread fetching each row's index before
+    // its copy would set the pace: the warp's lanes issue a stage's rows
+    // together (lane c: row c), after lane 0 has claimed the slot.
+    const uint64_t pol = policy_evict_first();
+    int it = 0;
+    bool bad_any = false, stop = false;
+    for (int phase = 0; phase < 2 && !stop; ++phase) {
+      if (phase == 0 && !has_dot) continue;
+      if (phase == 1 && !has_axpy) continue;
+      int n_this = nrows;
+      if (phase == 1 && skip) {
+        const bool got = mbar_wait(act_ready, 0);  // every lane reads the list below
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            flag(p.st, DV_DEV_TIMEOUT);
+          }
+          break;
+        }
+        n_this = *list_count;
+      }
+      for (int q0 = 0; q0 < n_this; q0 += g.R, ++it) {
+        const int cnt = min(g.R, n_this - q0);
+        const int s = it % g.NS;
+        const uint32_t ph = (it / g.NS) & 1;
+        int go = 1;
+        if (lane == 0) {
+          if (*abort_flag) {
+            go = 0;
+          } else if (it >= g.NS && !mbar_wait(&empty[s], ph ^ 1)) {
+            *abort_flag = 1;
+            flag(p.st, DV_DEV_TIMEOUT);
+            go = 0;
+          }
+          if (go) mbar_arrive_expect_tx(&full[s], cnt * g.row_bytes);
+        }
+        if (!__shfl_sync(0xffffffffu, go, 0)) {
+          stop = true;
+          break;
+        }
+        if (lane < cnt) {
+          const int local = (phase == 1 && skip) ? list[q0 + lane] : (q0 + lane);
+          bool bad;
+          const uint16_t* src = row_addr(p, KIND, phase, r0 + local, qkv_rows, bad);
+          bad_any |= bad;
+          bulk_g2s(smem + (size_t)s * g.stage_bytes + (size_t)lane * g.row_bytes, src,
+                   g.row_bytes, &full[s], pol);
+        }
+        __syncwarp();
+      }
+    }
+    if (__any_sync(0xffffffffu, bad_any) && lane == 0) flag(p.st, DV_DEV_BAD_INDEX);
+    if (lane == 0)  // drain: every issued copy must land before the CTA exits
+      for (int j = (it > g.NS ? it - g.NS : 0); j < it; ++j)
+        if (!mbar_wait(&full[j % g.NS], (j / g.NS) & 1)) flag(p.st, DV_DEV_TIMEOUT);
+    __syncwarp();
+  } else if (warp == nwc) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       int it = 0;
@@ -279,6 +386,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
   if (tid == 0) pdl_launch_dependents();
   // Activation columns of this thread: vectors v_m = tid + m T (8 columns each).
   float z[B][V][8];
+  __half2 zh[KIND == KIND_MLP4 ? B : 1][KIND == KIND_MLP4 ? V : 1][4];
   // The raw fp16 input, for predictor rows fused into a QKV launch (they read
   // y, not LN(y)); batch-1 launches only (at B = 4 the extra registers would
   // spill: the predictor's first layer then runs as its own launch).
@@ -372,6 +480,15 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
       }
     }
 
+    if constexpr (KIND == KIND_MLP4) {
+      // fp16 pairs of the activations in the codes' order: {z_k, z_{k+4}}
+#pragma unroll
+      for (int b = 0; b < B; ++b)
+#pragma unroll
+        for (int m = 0; m < V; ++m)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) zh[b][m][k] = __floats2half2_rn(z[b][m][k], z[b][m][k + 4]);
+    }
     // --- dot phase: red[row][b][warp] = warp's share of z . W[row]. A warp
     // copies its columns of the stage's rows into registers, releases the
     // slot, then computes (the slot is held only for the shared-memory reads).
@@ -386,6 +503,61 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         ok = false;
       }
       ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the row sums below shuffle
+      if constexpr (KIND == KIND_MLP4) {
+        // 4-bit rows: decode straight from the stage, release it afterwards
+        if (ok) {
+          const uint8_t* st0 = smem + (size_t)s * g.stage_bytes;
+          // kW4Ilp rows at a time: independent chains, and their row sums
+          // shuffle together. The 16-bit activations ("A16") times the exact
+          // codes are summed in fp16 pairs over each 8 columns, then scaled
+          // and accumulated in fp32.
+          for (int c0 = 0; c0 < cnt; c0 += kW4Ilp) {
+            float acc[kW4Ilp][B];
+#pragma unroll
+            for (int r = 0; r < kW4Ilp; ++r)
+#pragma unroll
+              for (int b = 0; b < B; ++b) acc[r][b] = 0.f;
+#pragma unroll
+            for (int m = 0; m < V; ++m) {
+              const int v = tid + m * T;
+              if (v >= nvec) continue;
+#pragma unroll
+              for (int r = 0; r < kW4Ilp; ++r) {
+                if (c0 + r >= cnt) break;
+                const uint8_t* row = st0 + (size_t)(c0 + r) * g.row_bytes;
+                __half2 q2[4];
+                w4_decode_h2(*reinterpret_cast<const uint32_t*>(row + v * 4), q2);
+                const float sc =
+                    h2f(*reinterpret_cast<const uint16_t*>(row + p.d / 2 + (v >> 4) * 2));
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                  __half2 t = __hmul2(q2[0], zh[b][m][0]);
+#pragma unroll
+                  for (int k = 1; k < 4; ++k) t = __hfma2(q2[k], zh[b][m][k], t);
+                  const float2 tf = __half22float2(t);
+                  acc[r][b] = fmaf(sc, tf.x + tf.y, acc[r][b]);
+                }
+              }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+              for (int r = 0; r < kW4Ilp; ++r)
+#pragma unroll
+                for (int b = 0; b < B; ++b)
+                  acc[r][b] += __shfl_xor_sync(0xffffffffu, acc[r][b], off);
+            if (lane == 0)
+#pragma unroll
+              for (int r = 0; r < kW4Ilp; ++r)
+                if (c0 + r < cnt)
+#pragma unroll
+                  for (int b = 0; b < B; ++b) red[((q0 + c0 + r) * B + b) * nwc + warp] = acc[r][b];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        continue;
+      }
       uint4 wv[RM][V];
       if (ok) {
         const uint8_t* st0 = smem + (size_t)s * g.stage_bytes;
@@ -394,9 +566,8 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
 #pragma unroll
           for (int m = 0; m < V; ++m) {
             const int v = tid + m * T;
-            wv[c][m] = (c < cnt && v < nvec)
-                           ? *reinterpret_cast<const uint4*>(st0 + (size_t)c * g.row_bytes + v * 16)
-                           : make_uint4(0, 0, 0, 0);
+            wv[c][m] = (c < cnt && v < nvec) ? stage_vec<KIND>(st0 + (size_t)c * g.row_bytes, v, p.d)
+                                             : make_uint4(0, 0, 0, 0);
           }
       }
       __syncwarp();
@@ -412,6 +583,19 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
 #pragma unroll
           for (int m = 0; m < V; ++m) {
             float w[8];
+            if constexpr (KIND == KIND_MLP4) {
+              // codes times this group's scale: sum_e z_e q_e, then one FMA by s
+              w4_decode(wv[c][m].x, w);
+              const float sc = h2f((uint16_t)wv[c][m].y);
+#pragma unroll
+              for (int b = 0; b < B; ++b) {
+                float t = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) t = fmaf(z[b][m][e], w[e], t);
+                acc[b] = fmaf(sc, t, acc[b]);
+              }
+              continue;
+            }
             h8_to_f8(wv[c][m], w);
             if (kRaw && raw) {
 #pragma unroll
@@ -445,7 +629,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
       for (int b = 0; b < B; ++b) {
         float val = 0.f;
         for (int w = 0; w < nwc; ++w) val += red[(i * B + b) * nwc + w];
-        if (KIND == KIND_MLP) {
+        if (is_mlp(KIND)) {
           int j = p.idx ? p.idx[v] : v;
           const bool badj = (j < 0 || j >= p.n_rows_total);
           float a = val + ((p.bias0 && !badj) ? h2f(p.bias0[j]) : 0.f);
@@ -586,6 +770,48 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         ok = false;
       }
       ok = __all_sync(0xffffffffu, ok);
+      if constexpr (KIND == KIND_MLP4) {
+        if (ok) {
+          const uint8_t* st0 = smem + (size_t)s * g.stage_bytes;
+          // The stage's rows (at most kW4StageRows) are summed in fp16 pairs,
+          // each row's coefficient a_j s rounded to fp16, then added to the
+          // fp32 accumulators once per stage.
+#pragma unroll
+          for (int m = 0; m < V; ++m) {
+            const int v = tid + m * T;
+            if (v >= nvec) continue;
+            __half2 h[B][4];
+#pragma unroll
+            for (int b = 0; b < B; ++b)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) h[b][k] = __float2half2_rn(0.f);
+            for (int c = 0; c < cnt; ++c) {
+              const uint8_t* row = st0 + (size_t)c * g.row_bytes;
+              const int li = skip ? list[q0 + c] : (q0 + c);
+              __half2 q2[4];
+              w4_decode_h2(*reinterpret_cast<const uint32_t*>(row + v * 4), q2);
+              const float sc = h2f(*reinterpret_cast<const uint16_t*>(row + p.d / 2 + (v >> 4) * 2));
+#pragma unroll
+              for (int b = 0; b < B; ++b) {
+                const __half2 cf = __float2half2_rn(coef[b * g.CH + li] * sc);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) h[b][k] = __hfma2(q2[k], cf, h[b][k]);
+              }
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float2 f = __half22float2(h[b][k]);
+                acc[b][m][k] += f.x;
+                acc[b][m][k + 4] += f.y;
+              }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        continue;
+      }
       uint4 wv[RM][V];
       if (ok) {
         const uint8_t* st0 = smem + (size_t)s * g.stage_bytes;
@@ -594,9 +820,8 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
 #pragma unroll
           for (int m = 0; m < V; ++m) {
             const int v = tid + m * T;
-            wv[c][m] = (c < cnt && v < nvec)
-                           ? *reinterpret_cast<const uint4*>(st0 + (size_t)c * g.row_bytes + v * 16)
-                           : make_uint4(0, 0, 0, 0);
+            wv[c][m] = (c < cnt && v < nvec) ? stage_vec<KIND>(st0 + (size_t)c * g.row_bytes, v, p.d)
+                                             : make_uint4(0, 0, 0, 0);
           }
       }
       __syncwarp();
@@ -612,6 +837,17 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
 #pragma unroll
           for (int m = 0; m < V; ++m) {
             float w[8];
+            if constexpr (KIND == KIND_MLP4) {
+              w4_decode(wv[c][m].x, w);
+              const float sc = h2f((uint16_t)wv[c][m].y);
+#pragma unroll
+              for (int b = 0; b < B; ++b) {
+                const float ab = a[b] * sc;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[b][m][e] = fmaf(ab, w[e], acc[b][m][e]);
+              }
+              continue;
+            }
             h8_to_f8(wv[c][m], w);
 #pragma unroll
             for (int b = 0; b < B; ++b)
@@ -784,14 +1020,18 @@ static int pick_V(int nvec, int tmax) { return (nvec + tmax - 1) / tmax; }
 
 int g_stage_target = 48 * 1024;  // bytes per ring stage (rows are grouped up to this)
 
-static bool make_geom(StreamGeom& g, int d, int B, int ring_budget, int CH) {
+static bool make_geom(StreamGeom& g, int d, int B, int ring_budget, int CH, bool w4 = false) {
   const int nvec = d / 8;
-  const int tmax = (B == 1) ? 512 : 384;
+  // 4-bit rows cost more instructions per byte: up to 31 consumer warps at B = 1
+  const int tmax = (w4 && B == 1) ? kW4Threads : (B == 1) ? 512 : 384;
   const int V = pick_V(nvec, tmax);
   g.T = ((nvec + V - 1) / V + 31) / 32 * 32;
   g.B = B;
-  g.row_bytes = (uint32_t)d * 2;
-  g.R = std::min(rows_max(V == 7 ? 8 : V), std::max(1, (int)(g_stage_target / g.row_bytes)));
+  g.row_bytes = w4 ? w4_row_bytes(d) : (uint32_t)d * 2;
+  // 4-bit rows are read from the stage in place (no register copy), so a
+  // stage can hold more of them
+  g.R = std::min(w4 ? kW4StageRows : rows_max(V == 7 ? 8 : V),
+                 std::max(1, (int)(g_stage_target / g.row_bytes)));
   g.stage_bytes = g.R * g.row_bytes;
   g.NS = std::min(16, ring_budget / (int)g.stage_bytes);
   if (g.NS < 2) g.NS = 2;
@@ -830,11 +1070,12 @@ static int launch_stream(int kind, StreamParams& p, long long rows, int target_c
                          int ring_budget, cudaStream_t stream, int* grid_out, bool pdl) {
   const int Bt = p.B == 1 ? 1 : 4;
   const int CH = 256;
-  if (!make_geom(p.g, p.d, Bt, ring_budget, CH)) return DV_ERR_UNSUPPORTED;
-  const int V = pick_V(p.d / 8, Bt == 1 ? 512 : 384);
+  if (!make_geom(p.g, p.d, Bt, ring_budget, CH, kind == KIND_MLP4)) return DV_ERR_UNSUPPORTED;
+  const int V = pick_V(p.d / 8, (kind == KIND_MLP4 && Bt == 1) ? kW4Threads : (Bt == 1 ? 512 : 384));
   void* fn = nullptr;
   switch (kind) {
     case KIND_MLP: fn = stream_kernel<KIND_MLP>(Bt, V); break;
+    case KIND_MLP4: fn = stream_kernel<KIND_MLP4>(Bt, V); break;
     case KIND_QKV: fn = stream_kernel<KIND_QKV>(Bt, V); break;
     case KIND_WO: fn = stream_kernel<KIND_WO>(Bt, V); break;
     case KIND_P1: fn = stream_kernel<KIND_P1>(Bt, V); break;
@@ -847,7 +1088,7 @@ static int launch_stream(int kind, StreamParams& p, long long rows, int target_c
       cudaSuccess)
     return DV_ERR_LAUNCH;
   void* args[] = {&p};
-  static const int tags[4] = {DV_TAG_MLP, DV_TAG_QKV, DV_TAG_PRED1, DV_TAG_WO};
+  static const int tags[5] = {DV_TAG_MLP, DV_TAG_QKV, DV_TAG_PRED1, DV_TAG_WO, DV_TAG_MLP};
   note_launch(tags[kind], 0, stream);
   const cudaError_t e = launch_k(fn, dim3(grid), dim3(p.g.T + 32), p.g.total, stream, args, pdl);
   note_launch(tags[kind], 1, stream);
@@ -878,6 +1119,23 @@ int launch_mlp(const uint16_t* x, int B, int d, int F, const uint16_t* ln_g, con
   p.n_rows_total = F; p.flags = flags; p.part = part; p.st = st;
   int grid = 0;
   int rc = launch_stream(KIND_MLP, p, k, target_ctas, ring_budget, stream, &grid, pdl);
+  if (rc != DV_OK) return rc;
+  return reduce_launch(part, grid, B, d, resid, b2, out, stream);
+}
+
+int launch_mlp_w4(const uint16_t* x, int B, int d, int F, const uint16_t* ln_g,
+                  const uint16_t* ln_b, float eps, const uint8_t* fc1q, const uint16_t* b1,
+                  const uint8_t* fc2Tq, const uint16_t* b2, const int32_t* idx, int k,
+                  const int32_t* dev_count, int flags, uint16_t* out, int* st, float* part,
+                  int target_ctas, int ring_budget, cudaStream_t stream, bool pdl) {
+  const uint16_t* resid = (flags & DV_NO_RESIDUAL) ? nullptr : x;
+  StreamParams p{};
+  p.d = d; p.B = B; p.x = x; p.ln_g = ln_g; p.ln_b = ln_b; p.eps = eps;
+  p.W0 = reinterpret_cast<const uint16_t*>(fc1q); p.W1 = reinterpret_cast<const uint16_t*>(fc2Tq);
+  p.bias0 = b1; p.idx = idx; p.k = k; p.dev_count = dev_count;
+  p.n_rows_total = F; p.flags = flags; p.part = part; p.st = st;
+  int grid = 0;
+  int rc = launch_stream(KIND_MLP4, p, k, target_ctas, ring_budget, stream, &grid, pdl);
   if (rc != DV_OK) return rc;
   return reduce_launch(part, grid, B, d, resid, b2, out, stream);
 }

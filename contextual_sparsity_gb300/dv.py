@@ -124,6 +124,11 @@ def lib():
                                      ctypes.POINTER(LayerWeights), ctypes.POINTER(KvCache), _i, _f,
                                      ctypes.POINTER(Sets), _p, _p, _p, _i, _p, _p, _sz, _p, _p, _p,
                                      _p]
+        L.dv_w4_row_bytes.restype = _sz
+        L.dv_w4_row_bytes.argtypes = [_i]
+        L.dv_quantize_w4.argtypes = [_p, _i, _i, _p, _p]
+        L.dv_sparse_mlp_w4.argtypes = [_p, _i, ctypes.POINTER(Dims), ctypes.POINTER(LayerWeights),
+                                       _p, _p, _p, _i, _p, _i, _p, _p, _p, _sz, _p]
         _R, _C = ctypes.POINTER(Request), ctypes.POINTER(CostModel)
         _D, _K = ctypes.POINTER(Dims), ctypes.POINTER(Keep)
         L.dv_plan_bytes.argtypes = [_D, _K, _R, _d, ctypes.POINTER(_d)]
@@ -139,7 +144,8 @@ EXPORTED = ["dv_version", "dv_status_string", "dv_workspace_size", "dv_set_tunin
             "dv_launch_count", "dv_predict",
             "dv_select_topk", "dv_sparse_mlp", "dv_sparse_attn", "dv_kv_select_attn",
             "dv_decode_layer", "dv_decode_step", "dv_sparse_mlp_noalloc", "dv_plan_bytes",
-            "dv_cost_calibrate", "dv_plan_decode", "dv_plan_crossing"]
+            "dv_cost_calibrate", "dv_plan_decode", "dv_plan_crossing", "dv_w4_row_bytes",
+            "dv_quantize_w4", "dv_sparse_mlp_w4"]
 
 
 def status_string(code: int) -> str:
@@ -234,6 +240,29 @@ def sparse_mlp(x, D: Dims, W: dict, idx, k, out, ws, dev_count=None, flags=0, de
     _check(lib().dv_sparse_mlp(ptr(x), B, ctypes.byref(D), ctypes.byref(lw), ptr(idx), k,
                                ptr(dev_count), flags, ptr(out), ptr(dev_status), ptr(ws),
                                ws.numel(), _stream(stream)), "dv_sparse_mlp")
+
+
+def w4_row_bytes(d: int) -> int:
+    return lib().dv_w4_row_bytes(d)
+
+
+def quantize_w4(W, out=None, stream=None):
+    """Packed 4-bit rows [rows][w4_row_bytes(d)] (uint8) of fp16 rows W [rows][d]."""
+    import torch
+    rows, d = W.shape
+    if out is None:
+        out = torch.empty(rows, w4_row_bytes(d), dtype=torch.uint8, device=W.device)
+    _check(lib().dv_quantize_w4(ptr(W), rows, d, ptr(out), _stream(stream)), "dv_quantize_w4")
+    return out
+
+
+def sparse_mlp_w4(x, D: Dims, W: dict, fc1_w4, fc2T_w4, idx, k, out, ws, dev_count=None, flags=0,
+                  dev_status=None, stream=None):
+    lw = layer_weights(W)
+    _check(lib().dv_sparse_mlp_w4(ptr(x), x.shape[0], ctypes.byref(D), ctypes.byref(lw),
+                                  ptr(fc1_w4), ptr(fc2T_w4), ptr(idx), k, ptr(dev_count), flags,
+                                  ptr(out), ptr(dev_status), ptr(ws), ws.numel(), _stream(stream)),
+           "dv_sparse_mlp_w4")
 
 
 def kv_cache(K, V, y_side=None, kv_missing=None, Kr=None, Vr=None, kept_pos=None, kept_count=None,

@@ -235,6 +235,34 @@ int dv_sparse_mlp_noalloc(const uint16_t* x, int B, const dv_dims* dims,
                           const int32_t* dev_count, int flags, uint16_t* out, int* dev_status,
                           cudaStream_t stream);
 
+/* ---- W4A16: 4-bit weight rows for the sparse MLP ([DV] §5.2, Table 7) ------
+ * The pages name no format; this library's: groups of DV_W4_GROUP = 128
+ * columns of a row, scale s = fp16(max |w| / 7) (fp32 division), code
+ * q = clamp(rint(w / s), -8, 7) (fp32 division, ties to even; a zero group
+ * has s = 0, q = 0), weight q s. Packed row: d/2 bytes of codes (column 2i in
+ * the low nibble of byte i, stored as q + 8), the d/128 fp16 scales, then zero
+ * bytes up to dv_w4_row_bytes(d) (a multiple of 16). */
+#define DV_W4_GROUP 128
+
+/* Bytes of one packed row (0 unless d is a positive multiple of 128). Host. */
+size_t dv_w4_row_bytes(int d);
+
+/* Quantize rows W [rows][d] fp16 (finite values) into out [rows][dv_w4_row_bytes(d)]
+ * (device, 16-byte aligned). 128 <= d <= 16384, d % 128 == 0, rows <= 65535.
+ * Enqueued on stream. DV_OK, DV_ERR_NULL, DV_ERR_ALIGN, DV_ERR_DIMS. */
+int dv_quantize_w4(const uint16_t* W, int rows, int d, uint8_t* out, cudaStream_t stream);
+
+/* dv_sparse_mlp with packed 4-bit rows: fc1_w4 [F][row] and fc2T_w4 [F][row]
+ * (row = dv_w4_row_bytes(d)) replace w->fc1 and w->fc2T (ignored); the
+ * activations stay fp16 and LN2, b1, b2 come from w:
+ * out[b] = x[b] + sum_{j in S} relu(LN2(x[b]) . (q s)1_j + b1[j]) (q s)2_j + b2,
+ * accumulated in fp32. d % 128 == 0. Other arguments, flags and errors as
+ * dv_sparse_mlp; the workspace is dv_workspace_size(dims, B, 0). */
+int dv_sparse_mlp_w4(const uint16_t* x, int B, const dv_dims* dims, const dv_layer_weights* w,
+                     const uint8_t* fc1_w4, const uint8_t* fc2T_w4, const int32_t* idx, int k,
+                     const int32_t* dev_count, int flags, uint16_t* out, int* dev_status,
+                     void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* ---- a5-a7: head-sparse attention block ([DV] §2.3 Eq. 2, §4.2, §4.4) ------
  * For each selected unit u in head_idx[0..k_heads-1] (or *dev_count of them;
  * head_idx == NULL: all h_kv units): project z = LN1(x[b]) to q (every query

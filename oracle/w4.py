@@ -17,7 +17,8 @@ project's own choice, written out as its definition:
 
 Packed row (the library's layout): d/2 bytes of codes, byte i holding columns
 2i (low nibble) and 2i + 1 (high nibble) as q + 8 in 0..15, then the d/G
-scales as fp16, all in one contiguous row of d/2 + d/64 bytes.
+scales as fp16, then zero bytes up to a multiple of 16 (every row then starts
+on a 16-byte boundary).
 
 The MLP is "Deja Vu" Eq. 1 over the selected neurons S with the dequantized
 weights: a_j = max(0, W1'_j . LN2(x) + b1_j), out = sum_j a_j W2'_j + b2,
@@ -57,13 +58,18 @@ def dequantize(q, s16):
             * s16.astype(np.float64)[..., None]).reshape(rows, d)
 
 
+def row_bytes(d):
+    return (d // 2 + d // 64 + 15) // 16 * 16
+
+
 def pack(q, s16):
-    """Packed rows (uint8 [rows][d/2 + d/64]) in the library's layout."""
+    """Packed rows (uint8 [rows][row_bytes(d)]) in the library's layout."""
     rows, d = q.shape
     u = (q.astype(np.int16) + 8).astype(np.uint8)
     codes = (u[:, 0::2] | (u[:, 1::2] << 4)).astype(np.uint8)
     scales = np.ascontiguousarray(s16, dtype=np.float16).view(np.uint8).reshape(rows, -1)
-    return np.concatenate([codes, scales], axis=1)
+    pad = np.zeros((rows, row_bytes(d) - d // 2 - d // 64), np.uint8)
+    return np.concatenate([codes, scales, pad], axis=1)
 
 
 def unpack(rows_u8, d):
@@ -74,7 +80,8 @@ def unpack(rows_u8, d):
     q = np.empty((rows, d), np.int8)
     q[:, 0::2] = (codes & 0xF).astype(np.int8) - 8
     q[:, 1::2] = (codes >> 4).astype(np.int8) - 8
-    s16 = np.ascontiguousarray(rows_u8[:, d // 2:]).view(np.float16).reshape(rows, d // GROUP)
+    s16 = np.ascontiguousarray(rows_u8[:, d // 2: d // 2 + d // 64]).view(np.float16)
+    s16 = s16.reshape(rows, d // GROUP)
     return q, s16
 
 

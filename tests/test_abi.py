@@ -149,3 +149,25 @@ def test_kv_select_validation(L):
     assert call(keep=0.0) == dv.DV_ERR_KEEP
     assert call(keep=1.5) == dv.DV_ERR_KEEP
     assert call(n=300) == dv.DV_ERR_DIMS
+
+
+def test_w4_validation(L):
+    assert dv.w4_row_bytes(12288) == 6336 and dv.w4_row_bytes(256) == 144
+    assert dv.w4_row_bytes(4096) == 2112 and dv.w4_row_bytes(100) == 0 and dv.w4_row_bytes(0) == 0
+    q = L.dv_quantize_w4
+    assert q(None, 4, 256, FAKE, None) == dv.DV_ERR_NULL
+    assert q(MISALIGNED, 4, 256, FAKE, None) == dv.DV_ERR_ALIGN
+    assert q(FAKE, 4, 200, FAKE, None) == dv.DV_ERR_DIMS
+    assert q(FAKE, 0, 256, FAKE, None) == dv.DV_ERR_DIMS
+    D = _dims()
+    w = _w()
+    m = L.dv_sparse_mlp_w4
+    args = lambda fc1=FAKE, k=4, B=1, dd=D, ws_bytes=16: (
+        FAKE, B, ctypes.byref(dd), ctypes.byref(w), fc1, FAKE + 8192, FAKE, k, None, 0,
+        FAKE + 4096, None, FAKE * 2, ws_bytes, None)
+    assert m(*args(fc1=None)) == dv.DV_ERR_NULL
+    assert m(*args(fc1=MISALIGNED)) == dv.DV_ERR_ALIGN
+    assert m(*args(k=0)) == dv.DV_ERR_K
+    assert m(*args(B=5)) == dv.DV_ERR_DIMS
+    assert m(*args(dd=_dims(d=264))) == dv.DV_ERR_DIMS      # not a multiple of 128
+    assert m(*args()) == dv.DV_ERR_WORKSPACE

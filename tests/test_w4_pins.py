@@ -69,9 +69,9 @@ def test_pack_layout_and_round_trip():
     q[0, 0], q[0, 1], q[0, 2], q[0, 3] = -8, 7, 3, -1
     s = np.array([[0.5, 2.0]], F16)
     p = w4.pack(q, s)
-    assert p.shape == (1, 128 + 4)
+    assert p.shape == (1, 144)                      # 128 + 4 bytes, padded to 16
     assert p[0, 0] == 0xF0 and p[0, 1] == (11 | (7 << 4))
-    assert p[0, 128:].view(F16).tolist() == [0.5, 2.0]
+    assert p[0, 128:132].view(F16).tolist() == [0.5, 2.0] and not p[0, 132:].any()
     rng = np.random.default_rng(1)
     q = rng.integers(-8, 8, (3, 384)).astype(np.int8)
     s = rng.uniform(0.001, 3, (3, 3)).astype(F16)
