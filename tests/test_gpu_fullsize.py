@@ -113,18 +113,20 @@ def test_composition_dense_split_k_baseline():
     _check_last_layer(m)
 
 
-def test_opt67b_decode_steps_recompute_missing_kv():
+@pytest.mark.parametrize("B", [1, 4])
+def test_opt67b_decode_steps_recompute_missing_kv(B):
     # five decode steps of a 3-layer opt-6.7b stack with a growing context,
     # a new input each step and the look-ahead predictor choosing the sets;
     # the last layer of every step is checked against the oracle's multi-step
-    # attention ("Deja Vu" §4.2: every past token's k, v from its own input)
+    # attention ("Deja Vu" §4.2: every past token's k, v from its own input).
+    # At batch 4 the sets are the unions of the four sequences' sets.
     setup_lib()
     dv.set_tuning()
-    w = synth.workload("opt-6.7b", layers=3)
+    w = synth.workload("opt-6.7b", layers=3, B=B)
     T, L = 5, 3
     dev = torch.device("cuda", 0)
     m = bench.Model(w, dev, lookahead=True, kept_inputs=True, fill=True, extra_slots=T)
-    K0, V0 = np16(m.K[L - 1][0]).copy(), np16(m.V[L - 1][0]).copy()
+    K0, V0 = np16(m.K[L - 1]).copy(), np16(m.V[L - 1]).copy()
     xs = [synth.hidden(w, seed=500 + t, device=dev) for t in range(T)]
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -135,16 +137,22 @@ def test_opt67b_decode_steps_recompute_missing_kv():
         torch.cuda.synchronize()
         assert m.st.item() == 0
         sets_t = m.sets[(L - 1) & 1][1]
-        y_in.append(np16(m.y_tmp[(L - 2) & 1][0]).copy())
-        selH.append(sets_t["idx_H"][0].cpu().numpy().copy())
-        selN.append(sets_t["idx_N"][0].cpu().numpy().copy())
-        y_out.append(npf(m.y_out[0]))
+        y_in.append(np16(m.y_tmp[(L - 2) & 1]).copy())
+        if B == 1:
+            selH.append(sets_t["idx_H"][0].cpu().numpy().copy())
+            selN.append(sets_t["idx_N"][0].cpu().numpy().copy())
+        else:
+            c = sets_t["ucnt"].cpu().numpy()
+            selH.append(sets_t["uH"][: c[1]].cpu().numpy().copy())
+            selN.append(sets_t["uN"][: c[0]].cpu().numpy().copy())
+        y_out.append(npf(m.y_out))
     # the sets change from step to step, so some units have holes to fill
-    assert any(set(selH[t]) - set(selH[t - 1]) for t in range(1, T))
+    assert B > 1 or any(set(selH[t]) - set(selH[t - 1]) for t in range(1, T))
     Wh = {k: np16(v) for k, v in m.W[L - 1].items()}
-    ref, _, _ = oracle.attn_steps(y_in, Wh, K0, V0, w.n, selH)
-    for t in range(T):
-        hmid = oracle.round_fp16(y_in[t].astype(np.float64) + ref[t].delta)
-        mm = oracle.mlp_gather(hmid, Wh["fc1"], Wh["b1"], Wh["fc2T"], Wh.get("b2"), selN[t])
-        y_ref = oracle.round_fp16(hmid.astype(float) + mm)
-        assert rel_err(y_out[t], y_ref) < TOL, t
+    for b in range(B):
+        ref, _, _ = oracle.attn_steps([y[b] for y in y_in], Wh, K0[b], V0[b], w.n, selH)
+        for t in range(T):
+            hmid = oracle.round_fp16(y_in[t][b].astype(np.float64) + ref[t].delta)
+            mm = oracle.mlp_gather(hmid, Wh["fc1"], Wh["b1"], Wh["fc2T"], Wh.get("b2"), selN[t])
+            y_ref = oracle.round_fp16(hmid.astype(float) + mm)
+            assert rel_err(y_out[t][b], y_ref) < TOL, (b, t)

@@ -116,3 +116,46 @@ def test_fill_needs_the_kept_inputs_and_the_full_cache():
     with pytest.raises(dv.DvError) as e:
         dv.sparse_attn(x, D, W, None, w.h_kv, kv, 4, out, ws, flags=dv.DV_KV_FILL)
     assert e.value.code in (dv.DV_ERR_NULL, dv.DV_ERR_ALIGN)
+
+
+def test_multistep_missing_kv_batch4_union():
+    # four sequences decoded together over one (union) set of units per step;
+    # each sequence's cache gets its own recomputed rows from its own inputs
+    setup_lib()
+    w = synth.workload("opt-6.7b", d=1024, h=16, h_kv=16, dh=64, F=64)
+    B, n0, T = 4, 30, 7
+    rng = np.random.default_rng(4)
+    W = synth.layer_weights(w, 0, seed=5, full_bias=True)
+    n_max = n0 + T + 2
+    K, V = synth.kv_cache(w, 0, n_max, B=B, seed=5)
+    ys = [synth.hidden(w, B=B, seed=300 + t) for t in range(T)]
+    sels = [sorted(rng.choice(w.h_kv, 6, replace=False).tolist()) for _ in range(T)]
+    D = dv.dims(w.d, w.h, w.h_kv, w.dh, w.F, w.r, n_max)
+    ws = dv.workspace(D, B)
+    Kd, Vd = K.cuda(), V.cuda()
+    y_side = torch.zeros(B, n_max, w.d, dtype=torch.float16, device="cuda")
+    miss = torch.zeros(B, n_max, (w.h_kv + 31) // 32, dtype=torch.int32, device="cuda")
+    kv = dv.kv_cache(Kd, Vd, y_side=y_side, kv_missing=miss)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Wd = to_dev(W)
+    outs = []
+    for t in range(T):
+        out = torch.empty(B, w.d, dtype=torch.float16, device="cuda")
+        sd = torch.tensor(sels[t], dtype=torch.int32, device="cuda")
+        dv.sparse_attn(ys[t].cuda(), D, Wd, sd, len(sels[t]), kv, n0 + t, out, ws,
+                       flags=dv.DV_NO_RESIDUAL | dv.DV_KV_FILL, dev_status=st)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    Wh = host(W)
+    for b in range(B):
+        ref, Kf, _ = oracle.attn_steps([np16(y[b]) for y in ys], Wh, np16(K[b]), np16(V[b]), n0,
+                                       sels)
+        for t in range(T):
+            assert rel_err(npf(outs[t][b]), ref[t].delta) < TOL, (b, t)
+        Kg = Kd[b].cpu().numpy()
+        for u in range(w.h_kv):
+            last = max([t for t in range(T) if u in sels[t]], default=-1)
+            if last >= 0:
+                rows = list(range(n0 + last + 1))
+                assert rel_err(Kg[u, rows].astype(float), Kf[u, rows].astype(float)) < TOL, (b, u)
