@@ -732,7 +732,6 @@ def run_w4(a):
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     stream = torch.cuda.Stream(device=dev)
-    prof_n = 0
     res = {}
     for name in ("fp16", "w4"):
         def one(l):
