@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--decode-steps", type=int, default=0,
                     help="time T steps with a growing context, with and without the missing-KV "
                          "recompute")
+    ap.add_argument("--input-corr", type=float, default=0.0,
+                    help="--decode-steps: correlation of consecutive inputs (0 = independent)")
     ap.add_argument("--w4", action="store_true",
                     help="time the MLP block with fp16 and with 4-bit weight rows")
     ap.add_argument("--gate", action="store_true",
@@ -654,13 +656,21 @@ def run_multistep(a):
     """T decode steps with a growing context (n, n + 1, ..., n + T - 1), a new
     input per step, the look-ahead predictor choosing every step's sets: with
     and without the recompute of the missing K/V ("Deja Vu" 4.2)."""
+    import numpy as np
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     dvbuild.build()
     dv.lib()
     w = workload(a)
     T = a.decode_steps
-    xs = [synth.hidden(w, seed=1000 + t, device=dev) for t in range(T)]
+    # inputs x_t = rho x_{t-1} + sqrt(1 - rho^2) e_t: rho 0 gives independent
+    # tokens (the predictor's sets nearly independent from step to step), rho
+    # near 1 gives neighbouring tokens alike (overlapping sets, fewer holes)
+    rho = a.input_corr
+    xs = [synth.hidden(w, seed=1000, device=dev)]
+    for t in range(1, T):
+        e = synth.hidden(w, seed=1000 + t, device=dev).float()
+        xs.append((rho * xs[-1].float() + (1.0 - rho * rho) ** 0.5 * e).half())
     passes = max(1, a.steps // T)
     res = {}
     for fill in (False, True):
@@ -681,6 +691,14 @@ def run_multistep(a):
         torch.cuda.synchronize()
         assert m.st.item() == 0, f"device status {m.st.item()}"
         res["fill" if fill else "no_fill"] = e0.elapsed_time(e1) * 1e3 / (passes * T * w.layers)
+        if not fill:
+            # share of the units a step selects that the step before skipped
+            # (each has at least one row to recompute); without the recompute
+            # the marks keep every step's skips
+            marks = torch.stack([k[:, w.n:w.n + T] for k in m.kv_miss]).cpu().numpy()
+            bits = np.unpackbits(marks.view(np.uint8), axis=-1, bitorder="little")[..., :w.h_kv]
+            sel_now, skip_prev = bits[:, :, 1:] == 0, bits[:, :, :-1] == 1
+            res["hole_rate"] = round(float((sel_now & skip_prev).sum()) / float(sel_now.sum()), 3)
         # per-kernel times of the last step, replayed after the T - 1 before it
         prof = dv.Profiler(cap=64 * w.layers + 64)
         gp, _ = m.capture(stream, profiler=prof, x=xs[T - 1], n=w.n + T - 1, warm=False)
@@ -699,7 +717,8 @@ def run_multistep(a):
         print(f"[multistep] {'fill' if fill else 'no fill'}: "
               f"{res['fill' if fill else 'no_fill']:.2f} us/layer", file=sys.stderr, flush=True)
     out = {"metric": "decode_steps_missing_kv", "workload": workload_name(w, not a.sync),
-           "data": "synthetic", "decode_steps": T, "passes": passes,
+           "data": "synthetic", "decode_steps": T, "passes": passes, "input_corr": rho,
+           "hole_rate": res.get("hole_rate"),
            "us_per_layer": {"no_fill": round(res["no_fill"], 2), "fill": round(res["fill"], 2)},
            "fill_cost_us_per_layer": round(res["fill"] - res["no_fill"], 2),
            "kernel_us": {"no_fill": res["kernel_us_no_fill"], "fill": res["kernel_us_fill"]}}

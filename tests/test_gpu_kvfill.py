@@ -50,6 +50,7 @@ def _schedule(kind, hkv, T, rng):
     ("opt-6.7b", dict(F=64), 200, 6, "random"),                          # d 4096, 32 units
     ("opt-6.7b", dict(d=1024, h=40, h_kv=40, dh=64, F=64), 60, 10, "random"),  # two mark words
     ("tiny", {}, 0, 9, "designed"),                                      # no prefill at all
+    ("opt-175b", dict(F=64), 100, 4, "random"),       # d 12288, 96 units: three mark words
 ])
 def test_multistep_missing_kv_recompute(wl, over, n0, T, kind):
     setup_lib()
