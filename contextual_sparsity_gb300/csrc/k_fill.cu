@@ -19,12 +19,12 @@
 
 namespace dv {
 
-constexpr int kFillRows = 16;   // K/V rows of one unit per CTA (8 warps x 2 rows)
+constexpr int kFillRows = 24;   // K/V rows of one unit per CTA (12 warps x 2 rows)
 constexpr int kFillRowsW = 2;   // rows per warp
 constexpr int kFillUnroll = 4;  // 16-byte loads per row in flight per lane
 constexpr int kFillTok = 2;     // missing tokens per pass (their LN1(y) in shared memory, fp16)
 constexpr int kFillGroups = 4;  // CTAs that split a unit's passes between them
-constexpr int kFillThreads = 256;
+constexpr int kFillThreads = 384;
 
 struct FillParams {
   const uint16_t* y_side;    // [B][n_max][d]
@@ -39,10 +39,10 @@ struct FillParams {
   int* st;
 };
 
-// <= 64 registers and 2 d bytes of shared memory per token slot (48 KB at
-// d = 12288), so that a CTA fits beside a weight-streaming CTA when the
-// recompute runs on the side stream.
-__global__ void __launch_bounds__(kFillThreads, 4) k_kv_fill(const FillParams p) {
+// 12 warps and 2 d bytes of shared memory per token slot (48 KB at d = 12288):
+// on the side stream a CTA runs beside the Wo / MLP streaming CTAs where their
+// registers leave room (measured faster than 8 warps of <= 64 registers).
+__global__ void __launch_bounds__(kFillThreads, 2) k_kv_fill(const FillParams p) {
   extern __shared__ __align__(16) uint16_t zs[];  // [kFillTok][d]: LN1 of the pass's tokens
   __shared__ float red[kFillThreads / 32][kFillTok];
   __shared__ float stat[kFillTok][2];
