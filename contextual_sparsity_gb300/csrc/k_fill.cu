@@ -23,7 +23,7 @@ constexpr int kFillRows = 24;   // K/V rows of one unit per CTA (12 warps x 2 ro
 constexpr int kFillRowsW = 2;   // rows per warp
 constexpr int kFillUnroll = 4;  // 16-byte loads per row in flight per lane
 constexpr int kFillTok = 2;     // missing tokens per pass (their LN1(y) in shared memory, fp16)
-constexpr int kFillGroups = 4;  // CTAs that split a unit's passes between them
+constexpr int kFillGroups = 8;  // CTAs that split a unit's passes between them
 constexpr int kFillThreads = 384;
 
 struct FillParams {
