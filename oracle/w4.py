@@ -99,3 +99,58 @@ def mlp(x, fc1_q, fc1_s, b1, fc2T_q, fc2T_s, b2, idx, ln_g=None, ln_b=None, eps=
     if b2 is not None:
         out = out + np.asarray(b2, dtype=np.float16).astype(np.float64)
     return out
+
+
+def attn(x, W, Kc, Vc, n, sel, scale=None, eps=1e-5):
+    """Sparse MHA block output (residual excluded) of "Deja Vu" Eq. 2 with
+    dequantized projection weights. W holds the packed-row codes and scales
+    as (q, s) pairs under "Wq", "Wk", "Wv", "WoT", and fp16 biases / LN1
+    parameters under their usual names. Kc, Vc [hkv][n_max][dh] fp16 hold
+    positions 0..n-1; the new token's k, v are rounded to fp16 as the cache
+    stores them and attended as position n. Returns (delta [d], knew, vnew
+    [hkv][dh] fp16 for the selected units, zeros elsewhere)."""
+    z = layernorm(x, W.get("ln1_g"), W.get("ln1_b"), eps)
+    hkv, _, dh = Kc.shape
+    Wq = dequantize(*W["Wq"])
+    h = Wq.shape[0] // dh
+    G = h // hkv
+    scale = 1.0 / np.sqrt(dh) if scale is None else scale
+
+    def proj(name, rows, bias):
+        out = dequantize(*W[name])[rows] @ z
+        if W.get(bias) is not None:
+            out = out + np.asarray(W[bias], np.float16).astype(np.float64)[rows]
+        return out
+
+    WoT = dequantize(*W["WoT"])
+    d = WoT.shape[1]
+    delta = np.zeros(d)
+    if W.get("bo") is not None:
+        delta += np.asarray(W["bo"], np.float16).astype(np.float64)
+    knew = np.zeros((hkv, dh), np.float16)
+    vnew = np.zeros((hkv, dh), np.float16)
+    for u in sel:
+        r = np.arange(u * dh, (u + 1) * dh)
+        knew[u] = proj("Wk", r, "bk").astype(np.float16)
+        vnew[u] = proj("Wv", r, "bv").astype(np.float16)
+        Ku = np.concatenate([np.asarray(Kc[u, :n], np.float16), knew[u][None]]).astype(np.float64)
+        Vu = np.concatenate([np.asarray(Vc[u, :n], np.float16), vnew[u][None]]).astype(np.float64)
+        for g in range(G):
+            j = u * G + g
+            q = proj("Wq", np.arange(j * dh, (j + 1) * dh), "bq") * scale
+            s = Ku @ q
+            p = np.exp(s - s.max())
+            H = (p / p.sum()) @ Vu
+            delta += H @ WoT[j * dh:(j + 1) * dh]
+    return delta, knew, vnew
+
+
+def layer(x, W, Kc, Vc, n, head_sel, neuron_idx, scale=None, eps=1e-5):
+    """A decode layer with 4-bit projection and MLP weights: h = fp16(x + MHA),
+    y' = fp16(h + MLP(h)) (the fp16 points of the library)."""
+    a, _, _ = attn(x, W, Kc, Vc, n, head_sel, scale=scale, eps=eps)
+    xd = np.asarray(x, np.float16).astype(np.float64)
+    hmid = (xd + a).astype(np.float16)
+    m = mlp(hmid, *W["fc1"], W.get("b1"), *W["fc2T"], W.get("b2"), neuron_idx,
+            W.get("ln2_g"), W.get("ln2_b"), eps)
+    return (hmid.astype(np.float64) + m).astype(np.float16), hmid

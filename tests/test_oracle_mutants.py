@@ -129,6 +129,12 @@ W4_MUTANTS = {
                             "* 1.0).reshape(rows, d)"),
     "w4_mlp_no_relu": ("a = np.maximum(pre, 0.0)", "a = pre"),
     "w4_mlp_no_b1": ("pre = pre + np.asarray(b1", "pre = pre + 0 * np.asarray(b1"),
+    "w4_attn_no_scale": ('np.arange(j * dh, (j + 1) * dh), "bq") * scale',
+                         'np.arange(j * dh, (j + 1) * dh), "bq")'),
+    "w4_attn_gqa_interleaved": ("j = u * G + g", "j = g * hkv + u"),
+    "w4_attn_cache_slot_for_new_token": (
+        "Ku = np.concatenate([np.asarray(Kc[u, :n], np.float16), knew[u][None]])",
+        "Ku = np.asarray(Kc[u, :n + 1], np.float16)"),
 }
 
 

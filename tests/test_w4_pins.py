@@ -104,3 +104,42 @@ def test_mlp_equals_the_fp16_mlp_when_the_weights_are_exact():
 def test_rejects_ragged_groups():
     with pytest.raises(AssertionError):
         w4.quantize(np.zeros((1, 100), F16))
+
+
+def _exact_w4(rng, rows, d):
+    """Codes with power-of-two scales: every dequantized weight is an exact fp16."""
+    q = rng.integers(-8, 8, (rows, d)).astype(np.int8)
+    s = (2.0 ** rng.integers(-7, -4, (rows, d // 128))).astype(F16)
+    return q, s
+
+
+def test_attn_and_layer_equal_the_fp16_oracle_when_the_weights_are_exact():
+    rng = np.random.default_rng(9)
+    d, h, hkv, dh, F, n = 256, 4, 2, 64, 48, 37
+    Wq4 = {k: _exact_w4(rng, r, d) for k, r in (("Wq", h * dh), ("Wk", hkv * dh),
+                                                 ("Wv", hkv * dh), ("WoT", h * dh),
+                                                 ("fc1", F), ("fc2T", F))}
+    W16 = {k: w4.dequantize(*v).astype(F16) for k, v in Wq4.items()}
+    for k in W16:
+        assert np.array_equal(W16[k].astype(np.float64), w4.dequantize(*Wq4[k]))
+    extra = {"bq": (rng.standard_normal(h * dh) * 0.1).astype(F16),
+             "bk": (rng.standard_normal(hkv * dh) * 0.1).astype(F16),
+             "bv": (rng.standard_normal(hkv * dh) * 0.1).astype(F16),
+             "bo": (rng.standard_normal(d) * 0.1).astype(F16),
+             "b1": (rng.standard_normal(F) * 0.1).astype(F16),
+             "b2": (rng.standard_normal(d) * 0.1).astype(F16),
+             "ln1_g": (1 + 0.1 * rng.standard_normal(d)).astype(F16),
+             "ln1_b": (0.1 * rng.standard_normal(d)).astype(F16),
+             "ln2_g": (1 + 0.1 * rng.standard_normal(d)).astype(F16),
+             "ln2_b": (0.1 * rng.standard_normal(d)).astype(F16)}
+    K = rng.standard_normal((hkv, n + 3, dh)).astype(F16)
+    V = rng.standard_normal((hkv, n + 3, dh)).astype(F16)
+    x = rng.standard_normal(d).astype(F16)
+    sel, nsel = [1], np.sort(rng.choice(F, 20, replace=False))
+    delta, knew, vnew = w4.attn(x, {**Wq4, **extra}, K, V, n, sel)
+    ref = oracle.attn_gather(x, {**W16, **extra}, K, V, n, sel)
+    assert np.allclose(delta, ref.delta, rtol=0, atol=1e-10 * np.abs(ref.delta).max())
+    assert np.array_equal(knew[1], ref.knew[1]) and np.array_equal(vnew[1], ref.vnew[1])
+    y, hmid = w4.layer(x, {**Wq4, **extra}, K, V, n, sel, nsel)
+    y_ref, hmid_ref, _, _ = oracle.layer(x, {**W16, **extra}, K, V, n, sel, nsel)
+    assert np.array_equal(hmid, hmid_ref) and np.array_equal(y, y_ref)
