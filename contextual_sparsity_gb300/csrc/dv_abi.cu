@@ -197,7 +197,7 @@ static int attn_qkv(const uint16_t* x, int B, const dv_dims* D, const dv_layer_w
                     kv->kept_count, kv->b_max, kv->y_side, kv->kv_missing, fill ? 1 : 0,
                     at<int>(ws, L.cnt),
                     B * D->h_kv, P1n, D->r, (flags & DV_PRED_RELU) ? 1 : 0, u_out, st,
-                    main_ctas(), g_tune.main_ring, s, pdl);
+                    main_ctas(), g_tune.main_ring, s, pdl, (flags & DV_W4) != 0);
 }
 
 // Split-K attention with the combine fused, then the Wo^T gather-axpy and the
@@ -218,7 +218,7 @@ static int attn_rest(const uint16_t* x, int B, const dv_dims* D, const dv_layer_
   if (rc != DV_OK) return rc;
   rc = launch_wo((flags & DV_NO_RESIDUAL) ? nullptr : x, B, D->d, G, D->d_h, D->h_kv, w->WoT,
                  w->bo, sel, k, dev_count, at<float>(ws, L.hcomb), out, st, at<float>(ws, L.part),
-                 main_ctas(), g_tune.main_ring, s);
+                 main_ctas(), g_tune.main_ring, s, (flags & DV_W4) != 0);
   if (rc != DV_OK) return rc;
   if (ret && (flags & DV_KV_ADVANCE)) rc = launch_kv_advance(kv->kept_count, D->h_kv, kv->b_max, s);
   return rc;
@@ -237,6 +237,12 @@ static int run_attn(const uint16_t* x, int B, const dv_dims* D, const dv_layer_w
 static int run_mlp(const uint16_t* x, int B, const dv_dims* D, const dv_layer_weights* w,
                    const int32_t* sel, int k, const int32_t* dev_count, int flags, uint16_t* out,
                    int* st, void* ws, const WsLayout& L, cudaStream_t s, bool pdl) {
+  if (flags & DV_W4)
+    return launch_mlp_w4(x, B, D->d, D->F, w->ln2_g, w->ln2_b, D->ln_eps,
+                         reinterpret_cast<const uint8_t*>(w->fc1), w->b1,
+                         reinterpret_cast<const uint8_t*>(w->fc2T), w->b2, sel, k, dev_count,
+                         flags & (DV_SKIP_INACTIVE | DV_NO_RESIDUAL), out, st,
+                         at<float>(ws, L.part), main_ctas(), g_tune.main_ring, s, pdl);
   return launch_mlp(x, B, D->d, D->F, w->ln2_g, w->ln2_b, D->ln_eps, w->fc1, w->b1, w->fc2T, w->b2,
                     sel, k, dev_count, flags & (DV_SKIP_INACTIVE | DV_NO_RESIDUAL), out, st,
                     at<float>(ws, L.part),
@@ -290,6 +296,13 @@ static int check_weights_mlp(const dv_layer_weights* w) {
   REQ(w, DV_ERR_NULL);
   REQ_PTR(w->fc1); REQ_PTR(w->fc2T);
   OPT_PTR(w->ln2_g); OPT_PTR(w->ln2_b);
+  return DV_OK;
+}
+
+static int check_w4(const dv_dims* D, int flags) {
+  if (!(flags & DV_W4)) return DV_OK;
+  REQ(D->d % 128 == 0, DV_ERR_DIMS);
+  REQ(!(flags & DV_KV_FILL), DV_ERR_UNSUPPORTED);  // the recompute reads fp16 W^K, W^V
   return DV_OK;
 }
 
@@ -414,6 +427,7 @@ int dv_sparse_mlp(const uint16_t* x, int B, const dv_dims* dims, const dv_layer_
   if (rc != DV_OK) return rc;
   REQ_PTR(x); REQ_PTR(out); REQ(ws, DV_ERR_NULL); REQ(aligned(ws, 256), DV_ERR_ALIGN);
   if ((rc = check_weights_mlp(w)) != DV_OK) return rc;
+  if ((rc = check_w4(dims, flags)) != DV_OK) return rc;
   REQ(B >= 1 && B <= 4, DV_ERR_DIMS);
   if (!idx) k = dims->F;
   REQ(k >= 1 && k <= dims->F, DV_ERR_K);
@@ -462,6 +476,7 @@ int dv_sparse_attn(const uint16_t* x, int B, const dv_dims* dims, const dv_layer
   if (rc != DV_OK) return rc;
   REQ_PTR(x); REQ_PTR(out); REQ(ws, DV_ERR_NULL); REQ(aligned(ws, 256), DV_ERR_ALIGN);
   if ((rc = check_weights_attn(w)) != DV_OK) return rc;
+  if ((rc = check_w4(dims, flags)) != DV_OK) return rc;
   REQ(B >= 1 && B <= 4, DV_ERR_DIMS);
   if ((rc = check_kv(dims, kv, B, n, flags)) != DV_OK) return rc;
   if (!head_idx) k_heads = dims->h_kv;
@@ -545,6 +560,7 @@ static int decode_layer(const dv_dims* dims, const dv_keep* keep, int B, const d
   REQ(ws, DV_ERR_NULL); REQ(aligned(ws, 256), DV_ERR_ALIGN);
   if ((rc = check_weights_attn(w)) != DV_OK) return rc;
   if ((rc = check_weights_mlp(w)) != DV_OK) return rc;
+  if ((rc = check_w4(dims, flags)) != DV_OK) return rc;
   if ((rc = check_kv(dims, kv, B, n, flags)) != DV_OK) return rc;
   const WsLayout L = ws_layout(dims, B, 0);
   REQ(ws_bytes >= L.total, DV_ERR_WORKSPACE);
@@ -588,8 +604,9 @@ static int decode_layer(const dv_dims* dims, const dv_keep* keep, int B, const d
   // kernel right before it (a synchronous prediction on this stream).
   const bool pdl_qkv = !((flags & DV_SYNC_PREDICT) && need_pred) && (flags & DV_JOIN);
   // At batch 1 the next layer's P1 rows ride in this QKV launch; at B > 1
-  // they run on the side stream (the fused form would spill registers).
-  const bool fuse_p1 = look && B == 1;
+  // (the fused form would spill registers) and with 4-bit Q/K/V rows (P1
+  // stays fp16) they run on the side stream.
+  const bool fuse_p1 = look && B == 1 && !(flags & DV_W4);
   const bool fill_next = look && w_next && kv_next && (flags & DV_KV_FILL);
   if (fill_next) {
     if ((rc = check_kv(dims, kv_next, B, n, flags)) != DV_OK) return rc;

@@ -24,7 +24,7 @@ int launch_qkv(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const u
                const int32_t* kept_count, int b_max, uint16_t* y_side, uint32_t* kv_missing,
                int fill_clear, int* zero_cnt, int n_zero, const uint16_t* P1, int n_pred,
                int relu, float* u_out, int* st, int target_ctas, int ring_budget,
-               cudaStream_t stream, bool pdl);
+               cudaStream_t stream, bool pdl, bool w4 = false);
 
 int launch_mlp_w4(const uint16_t* x, int B, int d, int F, const uint16_t* ln_g,
                   const uint16_t* ln_b, float eps, const uint8_t* fc1q, const uint16_t* b1,
@@ -48,7 +48,7 @@ int launch_kv_fill(const uint16_t* y_side, const uint32_t* missing, int B, int d
 int launch_wo(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const uint16_t* WoT,
               const uint16_t* bo, const int32_t* idx, int k, const int32_t* dev_count,
               const float* H, uint16_t* out, int* st, float* part, int target_ctas,
-              int ring_budget, cudaStream_t stream);
+              int ring_budget, cudaStream_t stream, bool w4 = false);
 
 int launch_predict(const uint16_t* y, int B, int d, const uint16_t* P1, int r,
                    const uint16_t* P2, int N, int relu, float* scores, int ld, float* u,

@@ -61,11 +61,19 @@ __host__ __device__ inline void stream_layout(StreamGeom& g) {
 // ---------------------------------------------------------------------------
 // Kernel parameters
 // ---------------------------------------------------------------------------
-enum StreamKind { KIND_MLP = 0, KIND_QKV = 1, KIND_P1 = 2, KIND_WO = 3, KIND_MLP4 = 4 };
+enum StreamKind { KIND_MLP = 0, KIND_QKV = 1, KIND_P1 = 2, KIND_WO = 3, KIND_MLP4 = 4,
+                  KIND_QKV4 = 5, KIND_WO4 = 6 };
 // KIND_MLP4: the MLP with 4-bit weight rows ("Deja Vu" §5.2, Table 7: W4A16).
 // A packed row holds d/2 bytes of codes (column 2i in the low nibble of byte
 // i, code + 8), then the d/128 fp16 group scales, padded to 16 bytes.
 __host__ __device__ constexpr bool is_mlp(int k) { return k == KIND_MLP || k == KIND_MLP4; }
+__host__ __device__ constexpr bool is_qkv(int k) { return k == KIND_QKV || k == KIND_QKV4; }
+__host__ __device__ constexpr bool is_wo(int k) { return k == KIND_WO || k == KIND_WO4; }
+// Kinds whose rows are 4-bit packed rows (the Q/K/V and Wo kinds carry no
+// fused predictor rows: the predictor stays fp16).
+__host__ __device__ constexpr bool is_w4(int k) {
+  return k == KIND_MLP4 || k == KIND_QKV4 || k == KIND_WO4;
+}
 constexpr int kW4StageRows = 8;  // rows per ring stage for 4-bit rows
 constexpr int kW4Ilp = 4;        // 4-bit rows a consumer works on at once
 constexpr int kW4Threads = 992;  // consumer threads at B = 1 (31 warps + the producer)
@@ -155,8 +163,8 @@ DV_DEV int eff_count(const StreamParams& p) {
 // Rows streamed per selected entry (1 for neurons / predictor rows; (G+2) dh
 // for a QKV unit; G dh for a Wo unit).
 DV_DEV int rows_per_entry(const StreamParams& p, int kind) {
-  if (kind == KIND_QKV) return (p.G + 2) * p.dh;
-  if (kind == KIND_WO) return p.G * p.dh;
+  if (is_qkv(kind)) return (p.G + 2) * p.dh;
+  if (is_wo(kind)) return p.G * p.dh;
   return 1;
 }
 
@@ -185,20 +193,36 @@ DV_DEV const uint16_t* row_addr(const StreamParams& p, int kind, int phase, int 
   int u = p.idx ? p.idx[e] : e;
   bad = (u < 0 || u >= p.h_kv);
   if (bad) u = 0;
-  if (kind == KIND_WO) {  // r = g * dh + c ; query head u*G + g
-    return p.W0 + ((size_t)u * p.G * p.dh + r) * d;
+  // the matrix and row this virtual row reads
+  const uint16_t* base;
+  size_t row;
+  if (is_wo(kind)) {  // r = g * dh + c ; query head u*G + g
+    base = p.W0;
+    row = (size_t)u * p.G * p.dh + r;
+  } else {
+    const int qrows = p.G * p.dh;
+    if (r < qrows) {
+      base = p.W0;
+      row = (size_t)u * qrows + r;
+    } else if (r < qrows + p.dh) {
+      base = p.W1;
+      row = (size_t)u * p.dh + (r - qrows);
+    } else {
+      base = p.W2;
+      row = (size_t)u * p.dh + (r - qrows - p.dh);
+    }
   }
-  const int qrows = p.G * p.dh;
-  if (r < qrows) return p.W0 + ((size_t)u * qrows + r) * d;
-  if (r < qrows + p.dh) return p.W1 + ((size_t)u * p.dh + (r - qrows)) * d;
-  return p.W2 + ((size_t)u * p.dh + (r - qrows - p.dh)) * d;
+  if (is_w4(kind))
+    return reinterpret_cast<const uint16_t*>(reinterpret_cast<const uint8_t*>(base) +
+                                             row * w4_row_bytes(p.d));
+  return base + row * d;
 }
 
 // Vector v (8 columns) of a staged row: 16 bytes of fp16, or for 4-bit rows
 // {the 32-bit word of its 8 codes, its group's fp16 scale}.
 template <int KIND>
 DV_DEV uint4 stage_vec(const uint8_t* row, int v, int d) {
-  if constexpr (KIND == KIND_MLP4) {
+  if constexpr (is_w4(KIND)) {
     const uint32_t w = *reinterpret_cast<const uint32_t*>(row + v * 4);
     const uint32_t sc = *reinterpret_cast<const uint16_t*>(row + d / 2 + (v >> 4) * 2);
     return make_uint4(w, sc, 0u, 0u);
@@ -218,7 +242,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
                     const bool has_dot, const bool has_axpy, const bool skip);
 
 template <int KIND, int B, int V>
-__global__ void __launch_bounds__((KIND == KIND_MLP4 && B == 1) ? 1024 : (B == 1 ? 544 : 416), 1)
+__global__ void __launch_bounds__((is_w4(KIND) && B == 1) ? 1024 : (B == 1 ? 544 : 416), 1)
     k_stream(const StreamParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const StreamGeom& g = p.g;
@@ -239,13 +263,13 @@ __global__ void __launch_bounds__((KIND == KIND_MLP4 && B == 1) ? 1024 : (B == 1
   // This CTA's slice of the selected entries.
   const int kk = eff_count(p);
   const int per = rows_per_entry(p, KIND);
-  const int qkv_rows = (KIND == KIND_QKV) ? kk * per : 0;
+  const int qkv_rows = is_qkv(KIND) ? kk * per : 0;
   const long long tot_rows = (long long)kk * per + (KIND == KIND_QKV ? p.n_pred : 0);
   const int r0 = (int)(tot_rows * blockIdx.x / gridDim.x);
   const int r1 = (int)(tot_rows * (blockIdx.x + 1) / gridDim.x);
   const int nrows = r1 - r0;
-  const bool has_dot = (KIND != KIND_WO);
-  const bool has_axpy = (is_mlp(KIND) || KIND == KIND_WO);
+  const bool has_dot = !is_wo(KIND);
+  const bool has_axpy = (is_mlp(KIND) || is_wo(KIND));
   const bool skip = is_mlp(KIND) && (p.flags & DV_SKIP_INACTIVE);
 
   if (tid == 0) {
@@ -261,7 +285,7 @@ __global__ void __launch_bounds__((KIND == KIND_MLP4 && B == 1) ? 1024 : (B == 1
   __syncthreads();
 
   // ======================= producer warp =======================
-  if (warp == nwc && KIND == KIND_MLP4) {
+  if (warp == nwc && is_w4(KIND)) {
     // 4-bit rows are short, so one thread fetching each row's index before
     // its copy would set the pace: the warp's lanes issue a stage's rows
     // together (lane c: row c), after lane 0 has claimed the slot.
@@ -386,7 +410,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
   if (tid == 0) pdl_launch_dependents();
   // Activation columns of this thread: vectors v_m = tid + m T (8 columns each).
   float z[B][V][8];
-  __half2 zh[KIND == KIND_MLP4 ? B : 1][KIND == KIND_MLP4 ? V : 1][4];
+  __half2 zh[is_w4(KIND) ? B : 1][is_w4(KIND) ? V : 1][4];
   // The raw fp16 input, for predictor rows fused into a QKV launch (they read
   // y, not LN(y)); batch-1 launches only (at B = 4 the extra registers would
   // spill: the predictor's first layer then runs as its own launch).
@@ -480,7 +504,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
       }
     }
 
-    if constexpr (KIND == KIND_MLP4) {
+    if constexpr (is_w4(KIND)) {
       // fp16 pairs of the activations in the codes' order: {z_k, z_{k+4}}
 #pragma unroll
       for (int b = 0; b < B; ++b)
@@ -503,7 +527,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         ok = false;
       }
       ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the row sums below shuffle
-      if constexpr (KIND == KIND_MLP4) {
+      if constexpr (is_w4(KIND)) {
         // 4-bit rows: decode straight from the stage, release it afterwards
         if (ok) {
           const uint8_t* st0 = smem + (size_t)s * g.stage_bytes;
@@ -583,7 +607,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
 #pragma unroll
           for (int m = 0; m < V; ++m) {
             float w[8];
-            if constexpr (KIND == KIND_MLP4) {
+            if constexpr (is_w4(KIND)) {
               // codes times this group's scale: sum_e z_e q_e, then one FMA by s
               w4_decode(wv[c][m].x, w);
               const float sc = h2f((uint16_t)wv[c][m].y);
@@ -641,13 +665,13 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
             if (p.relu && u < 0.f) u = 0.f;
             p.u_out[(size_t)b * p.n_rows_total + v] = u;
           }
-        } else if (KIND == KIND_QKV && v >= qkv_rows) {
+        } else if (is_qkv(KIND) && v >= qkv_rows) {
           if (b < p.B) {
             float u = val;
             if (p.relu && u < 0.f) u = 0.f;
             p.u_out[(size_t)b * p.n_pred + (v - qkv_rows)] = u;
           }
-        } else if (KIND == KIND_QKV) {
+        } else if (is_qkv(KIND)) {
           const int e = v / per, r = v % per;
           const int u = p.idx ? p.idx[e] : e;
           if (u < 0 || u >= p.h_kv || b >= p.B) continue;
@@ -672,9 +696,9 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         }
       }
     }
-    if (KIND == KIND_QKV && blockIdx.x == 0)
+    if (is_qkv(KIND) && blockIdx.x == 0)
       for (int i = tid; i < p.n_zero; i += T) p.zero_cnt[i] = 0;
-    if (KIND == KIND_QKV && blockIdx.x == 0) {
+    if (is_qkv(KIND) && blockIdx.x == 0) {
       // Missing-KV bookkeeping ("Deja Vu" §4.2): keep a copy of y for the
       // units that did not get their k, v at this token.
       const int words = (p.h_kv + 31) / 32;
@@ -699,7 +723,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
           }
       }
     }
-    if (KIND == KIND_QKV && blockIdx.x == 0 && p.fill_clear && p.kv_missing) {
+    if (is_qkv(KIND) && blockIdx.x == 0 && p.fill_clear && p.kv_missing) {
       // The recompute that ran right before this launch filled every marked
       // position of the selected units ("Deja Vu" §4.2): clear those marks.
       // A unit's marks are a suffix of the positions; scan back from n - 1.
@@ -736,7 +760,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
   }
 
   if (has_axpy) {
-    if (KIND == KIND_WO) {
+    if (is_wo(KIND)) {
       // Coefficients: the combined attention output of each row's (head, dim).
       for (int i = tid; i < nrows * B; i += T) {
         const int li = i % nrows, b = i / nrows;
@@ -770,7 +794,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         ok = false;
       }
       ok = __all_sync(0xffffffffu, ok);
-      if constexpr (KIND == KIND_MLP4) {
+      if constexpr (is_w4(KIND)) {
         if (ok) {
           const uint8_t* st0 = smem + (size_t)s * g.stage_bytes;
           // The stage's rows (at most kW4StageRows) are summed in fp16 pairs,
@@ -837,7 +861,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
 #pragma unroll
           for (int m = 0; m < V; ++m) {
             float w[8];
-            if constexpr (KIND == KIND_MLP4) {
+            if constexpr (is_w4(KIND)) {
               w4_decode(wv[c][m].x, w);
               const float sc = h2f((uint16_t)wv[c][m].y);
 #pragma unroll
@@ -1070,14 +1094,16 @@ static int launch_stream(int kind, StreamParams& p, long long rows, int target_c
                          int ring_budget, cudaStream_t stream, int* grid_out, bool pdl) {
   const int Bt = p.B == 1 ? 1 : 4;
   const int CH = 256;
-  if (!make_geom(p.g, p.d, Bt, ring_budget, CH, kind == KIND_MLP4)) return DV_ERR_UNSUPPORTED;
-  const int V = pick_V(p.d / 8, (kind == KIND_MLP4 && Bt == 1) ? kW4Threads : (Bt == 1 ? 512 : 384));
+  if (!make_geom(p.g, p.d, Bt, ring_budget, CH, is_w4(kind))) return DV_ERR_UNSUPPORTED;
+  const int V = pick_V(p.d / 8, (is_w4(kind) && Bt == 1) ? kW4Threads : (Bt == 1 ? 512 : 384));
   void* fn = nullptr;
   switch (kind) {
     case KIND_MLP: fn = stream_kernel<KIND_MLP>(Bt, V); break;
     case KIND_MLP4: fn = stream_kernel<KIND_MLP4>(Bt, V); break;
     case KIND_QKV: fn = stream_kernel<KIND_QKV>(Bt, V); break;
     case KIND_WO: fn = stream_kernel<KIND_WO>(Bt, V); break;
+    case KIND_QKV4: fn = stream_kernel<KIND_QKV4>(Bt, V); break;
+    case KIND_WO4: fn = stream_kernel<KIND_WO4>(Bt, V); break;
     case KIND_P1: fn = stream_kernel<KIND_P1>(Bt, V); break;
   }
   if (!fn) return DV_ERR_UNSUPPORTED;
@@ -1088,7 +1114,8 @@ static int launch_stream(int kind, StreamParams& p, long long rows, int target_c
       cudaSuccess)
     return DV_ERR_LAUNCH;
   void* args[] = {&p};
-  static const int tags[5] = {DV_TAG_MLP, DV_TAG_QKV, DV_TAG_PRED1, DV_TAG_WO, DV_TAG_MLP};
+  static const int tags[7] = {DV_TAG_MLP, DV_TAG_QKV, DV_TAG_PRED1, DV_TAG_WO, DV_TAG_MLP,
+                              DV_TAG_QKV, DV_TAG_WO};
   note_launch(tags[kind], 0, stream);
   const cudaError_t e = launch_k(fn, dim3(grid), dim3(p.g.T + 32), p.g.total, stream, args, pdl);
   note_launch(tags[kind], 1, stream);
@@ -1148,9 +1175,10 @@ int launch_qkv(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const u
                const int32_t* kept_count, int b_max, uint16_t* y_side, uint32_t* kv_missing,
                int fill_clear, int* zero_cnt, int n_zero, const uint16_t* P1, int n_pred,
                int relu, float* u_out, int* st, int target_ctas, int ring_budget,
-               cudaStream_t stream, bool pdl) {
+               cudaStream_t stream, bool pdl, bool w4) {
   StreamParams p{};
   p.fill_clear = fill_clear;
+  if (w4) P1 = nullptr;  // 4-bit Q/K/V rows: the predictor's fp16 rows run on their own
   p.zero_cnt = zero_cnt; p.n_zero = n_zero;
   p.P1 = P1; p.n_pred = P1 ? n_pred : 0; p.relu = relu; p.u_out = u_out;
   p.d = d; p.B = B; p.x = x; p.ln_g = ln_g; p.ln_b = ln_b; p.eps = eps;
@@ -1159,20 +1187,21 @@ int launch_qkv(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const u
   p.scale = scale; p.qbuf = qbuf; p.K = K; p.V = V; p.n = n; p.n_max = n_max;
   p.Kr = Kr; p.Vr = Vr; p.kept_count = kept_count; p.b_max = b_max;
   p.y_side = y_side; p.kv_missing = kv_missing; p.st = st;
-  return launch_stream(KIND_QKV, p, (long long)k * (G + 2) * dh + p.n_pred, target_ctas,
-                       ring_budget, stream, nullptr, pdl);
+  return launch_stream(w4 ? KIND_QKV4 : KIND_QKV, p, (long long)k * (G + 2) * dh + p.n_pred,
+                       target_ctas, ring_budget, stream, nullptr, pdl);
 }
 
 int launch_wo(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const uint16_t* WoT,
               const uint16_t* bo, const int32_t* idx, int k, const int32_t* dev_count,
               const float* H, uint16_t* out, int* st, float* part, int target_ctas,
-              int ring_budget, cudaStream_t stream) {
+              int ring_budget, cudaStream_t stream, bool w4) {
   // x: residual added by the reduce (NULL: none)
   StreamParams p{};
   p.d = d; p.B = B; p.x = x; p.W0 = WoT; p.idx = idx; p.k = k; p.dev_count = dev_count;
   p.G = G; p.dh = dh; p.h_kv = h_kv; p.Hc = H; p.part = part; p.st = st;
   int grid = 0;
-  int rc = launch_stream(KIND_WO, p, (long long)k * G * dh, target_ctas, ring_budget, stream,
+  int rc = launch_stream(w4 ? KIND_WO4 : KIND_WO, p, (long long)k * G * dh, target_ctas,
+                         ring_budget, stream,
                          &grid, true);
   if (rc != DV_OK) return rc;
   return reduce_launch(part, grid, B, d, x, bo, out, stream);

@@ -31,6 +31,7 @@ DV_KV_ADVANCE = 1 << 7
 DV_JOIN = 1 << 8
 DV_NO_RESIDUAL = 1 << 9
 DV_KV_FILL = 1 << 10
+DV_W4 = 1 << 11
 
 _p = ctypes.c_void_p
 _i = ctypes.c_int

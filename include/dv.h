@@ -81,6 +81,10 @@ extern "C" {
                                       y + MHA(y) + MLP(y), sums block outputs) */
 #define DV_KV_FILL (1u << 10)      /* attention: first recompute the missing k, v of the
                                       selected units from y_side ([DV] §4.2) */
+#define DV_W4 (1u << 11)           /* the layer's Wq, Wk, Wv, WoT, fc1, fc2T point to packed
+                                      4-bit rows (dv_quantize_w4; [DV] §5.2, Table 7
+                                      W4A16); P1, P2 stay fp16; d % 128 == 0; not with
+                                      DV_KV_FILL */
 
 /* ---- shapes ------------------------------------------------------------ */
 typedef struct {

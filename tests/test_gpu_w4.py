@@ -6,8 +6,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from contextual_sparsity_gb300 import dv, synth
-from gpu_helpers import TOL, host, np16, npf, rel_err, setup_lib, to_dev
+from gpu_helpers import TOL, check_sets, host, np16, npf, rel_err, setup_lib, to_dev
 from oracle import w4 as ow4
 
 pytestmark = pytest.mark.gpu
@@ -90,3 +91,88 @@ def test_w4_mlp_residual_and_dense_index_list():
                   ln_g=Wh["ln2_g"], ln_b=Wh["ln2_b"])
     want = np16(x[0]).astype(np.float64) + ref
     assert rel_err(npf(out[0]), want) < TOL
+
+
+W4_NAMES = ("Wq", "Wk", "Wv", "WoT", "fc1", "fc2T")
+
+
+def _w4_layer(w, seed):
+    """Device weights of one layer with the six projection matrices as packed
+    4-bit rows (GPU quantizer), and the oracle's view of them."""
+    W = synth.layer_weights(w, 0, seed=seed, full_bias=True)
+    Wd = to_dev(W)
+    Wq = dict(Wd)
+    for k in W4_NAMES:
+        Wq[k] = dv.quantize_w4(Wd[k])
+    torch.cuda.synchronize()
+    Wo = host(W)
+    for k in W4_NAMES:
+        Wo[k] = ow4.unpack(Wq[k].cpu().numpy(), w.d)
+    return Wq, Wo
+
+
+@pytest.mark.parametrize("wl,over,n,sel", [
+    ("tiny", {}, 64, [1, 3]),
+    ("opt-6.7b", dict(F=64), 200, [0, 5, 31]),
+    ("compose", dict(d=512, h=8, h_kv=2, F=64), 300, [1]),        # GQA, 4 query heads per unit
+])
+def test_w4_attention_block_parity(wl, over, n, sel):
+    setup_lib()
+    w = synth.workload(wl, **over)
+    Wq, Wo = _w4_layer(w, seed=21)
+    n_max = n + 5
+    K, V = synth.kv_cache(w, 0, n_max, B=1, seed=21)
+    x = synth.hidden(w, B=1, seed=22)
+    D = dv.dims(w.d, w.h, w.h_kv, w.dh, w.F, w.r, n_max)
+    ws = dv.workspace(D, 1)
+    Kd, Vd = K.cuda(), V.cuda()
+    kv = dv.kv_cache(Kd, Vd)
+    out = torch.empty(1, w.d, dtype=torch.float16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sd = torch.tensor(sel, dtype=torch.int32, device="cuda")
+    dv.sparse_attn(x.cuda(), D, Wq, sd, len(sel), kv, n, out, ws,
+                   flags=dv.DV_NO_RESIDUAL | dv.DV_W4, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    delta, knew, vnew = ow4.attn(np16(x[0]), Wo, np16(K[0]), np16(V[0]), n, sel)
+    assert rel_err(npf(out[0]), delta) < TOL
+    for u in sel:
+        assert rel_err(npf(Kd[0, u, n]), knew[u].astype(float)) < TOL
+        assert rel_err(npf(Vd[0, u, n]), vnew[u].astype(float)) < TOL
+
+
+@pytest.mark.parametrize("wl,over,B", [("tiny", {}, 1), ("opt-6.7b", dict(F=2048), 1),
+                                       ("opt-6.7b", dict(F=2048), 4)])
+def test_w4_decode_layer_parity(wl, over, B):
+    # one layer through the driver with 4-bit projection and MLP rows (its own
+    # fp16 predictor chooses the sets); teacher-forced against the oracle layer
+    setup_lib()
+    w = synth.workload(wl, **over)
+    Wq, Wo = _w4_layer(w, seed=31)
+    n_max = w.n + 4
+    K, V = synth.kv_cache(w, 0, n_max, B=B, seed=31)
+    x = synth.hidden(w, B=B, seed=32).cuda()
+    D = dv.dims(w.d, w.h, w.h_kv, w.dh, w.F, w.r, n_max)
+    ws = dv.workspace(D, B)
+    kN = oracle.k_from_keep(w.keep_N, w.F)
+    kH = oracle.k_from_keep(w.keep_H, w.h_kv)
+    cur, cur_t = dv.sets(B, w.F, w.h_kv, kN, kH)
+    kv = dv.kv_cache(K.cuda(), V.cuda())
+    y = torch.empty_like(x)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dv.decode_layer(D, dv.Keep(w.keep_N, w.keep_H, 1.0), Wq, None, kv, w.n, cur, None, x, y, ws,
+                    dv.DV_SYNC_PREDICT | dv.DV_W4, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    if B == 1:
+        selH, selN = cur_t["idx_H"][0].cpu().numpy(), cur_t["idx_N"][0].cpu().numpy()
+    else:
+        c = cur_t["ucnt"].cpu().numpy()
+        selH, selN = cur_t["uH"][: c[1]].cpu().numpy(), cur_t["uN"][: c[0]].cpu().numpy()
+    for b in range(B):
+        ref = oracle.predict(np16(x[b]), Wo["P1"], Wo["P2"])
+        if B == 1:
+            check_sets(selN, ref[: w.F], kN)
+            check_sets(selH, ref[w.F:], kH)
+        y_ref, _ = ow4.layer(np16(x[b]), Wo, np16(K[b]), np16(V[b]), w.n, selH, selN)
+        assert rel_err(npf(y[b]), y_ref.astype(np.float64)) < TOL, b
