@@ -69,6 +69,8 @@ def parse():
                     help="--decode-steps: correlation of consecutive inputs (0 = independent)")
     ap.add_argument("--w4", action="store_true",
                     help="time the MLP block with fp16 and with 4-bit weight rows")
+    ap.add_argument("--step", action="store_true",
+                    help="with --w4: whole decode steps with 4-bit weight rows vs fp16")
     ap.add_argument("--gate", action="store_true",
                     help="calibrate the latency gate on a context sweep and validate it")
     ap.add_argument("--gate-ctx", default="2048,8192,32768,131072",
@@ -214,7 +216,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 class Model:
     def __init__(self, w, device, lookahead=True, seed=0, kv_dense=False, kept_inputs=False,
-                 fill=False, extra_slots=0):
+                 fill=False, extra_slots=0, w4=False):
         self.w = w
         self.L = w.layers
         self.n = w.n
@@ -224,6 +226,14 @@ class Model:
         self.kN = traffic.k_of(w.keep_N, w.F)
         self.kH = traffic.k_of(w.keep_H, w.h_kv)
         self.W = [synth.layer_weights(w, l, seed=seed, device=device) for l in range(self.L)]
+        if w4:
+            # "Deja Vu" 5.2, Table 7 (W4A16): the projection and MLP rows as
+            # packed 4-bit rows; the predictor stays fp16
+            for W in self.W:
+                for k in ("Wq", "Wk", "Wv", "WoT", "fc1", "fc2T"):
+                    W[k] = dv.quantize_w4(W[k])
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
         self.K, self.V = [], []
         for l in range(self.L):
             k, v = synth.kv_cache(w, l, self.n_max, seed=seed, device=device)
@@ -284,6 +294,8 @@ class Model:
         self.evj = dv.event()
         self.st = torch.zeros(1, dtype=torch.int32, device=device)
         flags = (dv.DV_LOOKAHEAD if lookahead else 0) | self.kv_flags
+        if w4:
+            flags |= dv.DV_W4
         if fill:
             assert not self.retained, "the recompute reads the full cache"
             flags |= dv.DV_KV_FILL
@@ -725,6 +737,49 @@ def run_multistep(a):
     print(json.dumps(out))
 
 
+def run_w4_step(a):
+    """Whole decode steps of the workload with fp16 weights and with 4-bit
+    projection and MLP rows (W4A16), same sets of rows, same graph replay."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dvbuild.build()
+    dv.lib()
+    w = workload(a)
+    res = {}
+    for name in ("fp16", "w4"):
+        m = Model(w, dev, lookahead=not a.sync, w4=(name == "w4"))
+        stream = torch.cuda.Stream(device=dev)
+        g, per_step = m.capture(stream)
+        for _ in range(max(3, a.warmup)):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(a.steps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        assert m.st.item() == 0, f"device status {m.st.item()}"
+        res[name] = e0.elapsed_time(e1) * 1e3 / (a.steps * w.layers)
+        print(f"[w4-step] {name}: {res[name]:.2f} us/layer, {per_step} launches/step",
+              file=sys.stderr, flush=True)
+        del m, g
+        torch.cuda.empty_cache()
+    sel, _ = traffic.layer_bytes(w)
+    G = w.h // w.h_kv
+    kN, kH = traffic.k_of(w.keep_N, w.F), traffic.k_of(w.keep_H, w.h_kv)
+    rb = dv.w4_row_bytes(w.d)
+    sel4 = (kH * (2 * G + 2) * w.dh + 2 * kN) * rb + traffic.kv_bytes(w.dh, kH, w.n + 1)
+    print(json.dumps({"metric": "decode_step_w4a16", "workload": workload_name(w, not a.sync),
+                      "data": "synthetic", "steps": a.steps,
+                      "us_per_layer": {k: round(v, 2) for k, v in res.items()},
+                      "selected_bytes": {"fp16": sel, "w4": sel4},
+                      "gbs_selected": {"fp16": round(sel / res["fp16"] / 1e3, 1),
+                                       "w4": round(sel4 / res["w4"] / 1e3, 1)},
+                      "speedup": round(res["fp16"] / res["w4"], 3)}))
+
+
 def run_w4(a):
     """The MLP block with fp16 rows and with 4-bit rows (W4A16, "Deja Vu"
     5.2, Table 7) at the workload's neuron keep, over several layers' weights
@@ -878,6 +933,8 @@ def main():
         run_gate(a)
     elif a.decode_steps:
         run_multistep(a)
+    elif a.w4 and a.step:
+        run_w4_step(a)
     elif a.w4:
         run_w4(a)
     else:

@@ -156,3 +156,31 @@ def test_opt67b_decode_steps_recompute_missing_kv(B):
             mm = oracle.mlp_gather(hmid, Wh["fc1"], Wh["b1"], Wh["fc2T"], Wh.get("b2"), selN[t])
             y_ref = oracle.round_fp16(hmid.astype(float) + mm)
             assert rel_err(y_out[t][b], y_ref) < TOL, (b, t)
+
+
+def test_opt67b_stack_w4a16():
+    # the opt-6.7b stack with 4-bit projection and MLP rows (W4A16, "Deja Vu"
+    # §5.2, Table 7), fp16 predictor, look-ahead on the side stream, replayed
+    # from its graph; the last layer checked against the oracle's W4 layer
+    from oracle import w4 as ow4
+    setup_lib()
+    dv.set_tuning()
+    w = synth.workload("opt-6.7b", layers=4)
+    m = bench.Model(w, torch.device("cuda", 0), lookahead=True, w4=True)
+    s = torch.cuda.Stream()
+    g, _ = m.capture(s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert m.st.item() == 0
+    L = m.L
+    y_prev, y_in = m.y_tmp[(L - 3) & 1], m.y_tmp[(L - 2) & 1]
+    sets_t = m.sets[(L - 1) & 1][1]
+    Wl = m.W[L - 1]
+    Wo = {k: (ow4.unpack(v.cpu().numpy(), w.d) if v.dtype == torch.uint8 else np16(v))
+          for k, v in Wl.items()}
+    ref = oracle.predict(np16(y_prev[0]), Wo["P1"], Wo["P2"])
+    check_sets(sets_t["idx_N"][0].cpu().numpy(), ref[: w.F], m.kN)
+    check_sets(sets_t["idx_H"][0].cpu().numpy(), ref[w.F:], m.kH)
+    y_ref, _ = ow4.layer(np16(y_in[0]), Wo, np16(m.K[L - 1][0]), np16(m.V[L - 1][0]), w.n,
+                         sets_t["idx_H"][0].cpu().numpy(), sets_t["idx_N"][0].cpu().numpy())
+    assert rel_err(npf(m.y_out[0]), y_ref.astype(np.float64)) < TOL
