@@ -122,6 +122,11 @@ def test_attention_and_layer_validation(L):
     kv_f = dv.KvCache(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64)
     assert a(*args(flags=dv.DV_KV_FILL | dv.DV_KV_RETAINED, kvp=kv_f)) == dv.DV_ERR_UNSUPPORTED
     assert a(*args(flags=dv.DV_KV_FILL, kvp=kv_f)) == dv.DV_ERR_WORKSPACE
+    assert a(*args(flags=dv.DV_W4 | dv.DV_KV_FILL, kvp=kv_f)) == dv.DV_ERR_UNSUPPORTED
+    assert a(*args(flags=dv.DV_W4)) == dv.DV_ERR_WORKSPACE           # d 256: a multiple of 128
+    D264 = _dims(d=264)
+    assert a(FAKE, 1, ctypes.byref(D264), ctypes.byref(w), FAKE, 2, None, ctypes.byref(kv), 10,
+             0.125, dv.DV_W4, FAKE + 4096, None, FAKE * 2, 16, None) == dv.DV_ERR_DIMS
     assert a(*args()) == dv.DV_ERR_WORKSPACE
     keep = dv.Keep(0.0, 0.5, 1.0)
     lay = L.dv_decode_layer
