@@ -69,6 +69,8 @@ def parse():
                     help="--decode-steps: correlation of consecutive inputs (0 = independent)")
     ap.add_argument("--w4", action="store_true",
                     help="time the MLP block with fp16 and with 4-bit weight rows")
+    ap.add_argument("--union-tc", action="store_true",
+                    help="the MLP block over a batch's union at B = 4..64 (tensor cores from 8)")
     ap.add_argument("--step", action="store_true",
                     help="with --w4: whole decode steps with 4-bit weight rows vs fp16")
     ap.add_argument("--gate", action="store_true",
@@ -737,6 +739,62 @@ def run_multistep(a):
     print(json.dumps(out))
 
 
+def run_union_tc(a):
+    """The MLP block of a batch over the union of its sequences' neuron sets:
+    B = 4 on the CUDA-core streaming kernel, B = 8..64 on the tensor cores
+    ("Deja Vu" 5.2, App. C.1); sets drawn independently at the workload's keep."""
+    import numpy as np
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dvbuild.build()
+    dv.lib()
+    w = workload(a)
+    kN = traffic.k_of(w.keep_N, w.F)
+    W = synth.layer_weights(w, 0, device=dev)
+    W = {k: W[k] for k in ("fc1", "fc2T", "b1", "ln2_g", "ln2_b") if k in W}
+    torch.cuda.empty_cache()
+    D = dv.dims(w.d, w.h, w.h_kv, w.dh, w.F, w.r, 8)
+    stream = torch.cuda.Stream(device=dev)
+    pk, pk_src = peaks()
+    rows = []
+    for B in (4, 8, 16, 32, 64):
+        rng = np.random.default_rng(B)
+        U = np.unique(np.concatenate([rng.choice(w.F, kN, replace=False) for _ in range(B)]))
+        Ud = torch.from_numpy(U.astype(np.int32)).to(dev)
+        x = synth.hidden(w, B=B, seed=7, device=dev)
+        out = torch.empty(B, w.d, dtype=torch.float16, device=dev)
+        if B == 4:
+            ws = dv.workspace(D, B)
+            run = lambda: dv.sparse_mlp(x, D, W, Ud, len(U), out, ws, stream=stream)
+        else:
+            ws = dv.union_mlp(x, D, W, Ud, len(U), out, stream=stream)
+            run = lambda: dv.union_mlp(x, D, W, Ud, len(U), out, ws=ws, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, a.warmup)):
+                run()
+        torch.cuda.synchronize()
+        reps = max(5, a.steps)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                run()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        by = traffic.mlp_bytes(w.d, len(U))
+        rows.append({"B": B, "union": int(len(U)), "union_frac": round(len(U) / w.F, 3),
+                     "us_per_block": round(us, 2), "us_per_sequence": round(us / B, 2),
+                     "weight_bytes": by, "gbs": round(by / us / 1e3, 1),
+                     "frac": round(by / us / 1e3 / pk, 3),
+                     "kernel": "k_stream<KIND_MLP> (CUDA cores)" if B == 4 else "mma.sync m16n8k16"})
+        print(f"[union] B {B}: |U| {len(U)} ({len(U) / w.F:.2f} F), {us:.1f} us", file=sys.stderr,
+              flush=True)
+    print(json.dumps({"metric": "union_mlp_block", "workload": workload_name(w), "data": "synthetic",
+                      "neuron_keep": w.keep_N, "peak_gbs": pk, "peak_source": pk_src,
+                      "rows": rows}))
+
+
 def run_w4_step(a):
     """Whole decode steps of the workload with fp16 weights and with 4-bit
     projection and MLP rows (W4A16), same sets of rows, same graph replay."""
@@ -933,6 +991,8 @@ def main():
         run_gate(a)
     elif a.decode_steps:
         run_multistep(a)
+    elif a.union_tc:
+        run_union_tc(a)
     elif a.w4 and a.step:
         run_w4_step(a)
     elif a.w4:

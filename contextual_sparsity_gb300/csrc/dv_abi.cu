@@ -437,6 +437,32 @@ int dv_sparse_mlp(const uint16_t* x, int B, const dv_dims* dims, const dv_layer_
   return run_mlp(x, B, dims, w, idx, k, dev_count, flags, out, dev_status, ws, L, stream, false);
 }
 
+size_t dv_union_mlp_ws_size(int B, int d, int k) {
+  if (B < 8 || B > 64 || (B & 7) || B == 24 || B == 40 || B == 48 || B == 56 || d < 16 ||
+      d % 16 || k < 1)
+    return 0;
+  return union_tc_ws_bytes(B, d, k);
+}
+
+int dv_union_mlp(const uint16_t* x, int B, const dv_dims* dims, const dv_layer_weights* w,
+                 const int32_t* union_idx, int k, const int32_t* dev_count, int flags,
+                 uint16_t* out, int* dev_status, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  int rc = check_dims(dims);
+  if (rc != DV_OK) return rc;
+  REQ_PTR(x); REQ_PTR(out); REQ(x != out, DV_ERR_DIMS);
+  if ((rc = check_weights_mlp(w)) != DV_OK) return rc;
+  REQ(union_idx, DV_ERR_NULL);
+  REQ(dims->d % 16 == 0, DV_ERR_DIMS);
+  REQ(k >= 1 && k <= dims->F, DV_ERR_K);
+  const size_t need = dv_union_mlp_ws_size(B, dims->d, k);
+  REQ(need > 0, DV_ERR_UNSUPPORTED);
+  REQ(ws, DV_ERR_NULL); REQ(aligned(ws, 256), DV_ERR_ALIGN);
+  REQ(ws_bytes >= need, DV_ERR_WORKSPACE);
+  return launch_union_mlp_tc(x, B, dims->d, dims->F, w->ln2_g, w->ln2_b, dims->ln_eps, w->fc1,
+                             w->b1, w->fc2T, w->b2, union_idx, k, dev_count,
+                             !(flags & DV_NO_RESIDUAL), out, dev_status, ws, stream);
+}
+
 size_t dv_w4_row_bytes(int d) { return (d >= 128 && d % 128 == 0) ? w4_row_bytes_host(d) : 0; }
 
 int dv_quantize_w4(const uint16_t* W, int rows, int d, uint8_t* out, cudaStream_t stream) {

@@ -125,6 +125,10 @@ def lib():
                                      ctypes.POINTER(LayerWeights), ctypes.POINTER(KvCache), _i, _f,
                                      ctypes.POINTER(Sets), _p, _p, _p, _i, _p, _p, _sz, _p, _p, _p,
                                      _p]
+        L.dv_union_mlp_ws_size.restype = _sz
+        L.dv_union_mlp_ws_size.argtypes = [_i, _i, _i]
+        L.dv_union_mlp.argtypes = [_p, _i, ctypes.POINTER(Dims), ctypes.POINTER(LayerWeights), _p,
+                                   _i, _p, _i, _p, _p, _p, _sz, _p]
         L.dv_w4_row_bytes.restype = _sz
         L.dv_w4_row_bytes.argtypes = [_i]
         L.dv_quantize_w4.argtypes = [_p, _i, _i, _p, _p]
@@ -146,7 +150,7 @@ EXPORTED = ["dv_version", "dv_status_string", "dv_workspace_size", "dv_set_tunin
             "dv_select_topk", "dv_sparse_mlp", "dv_sparse_attn", "dv_kv_select_attn",
             "dv_decode_layer", "dv_decode_step", "dv_sparse_mlp_noalloc", "dv_plan_bytes",
             "dv_cost_calibrate", "dv_plan_decode", "dv_plan_crossing", "dv_w4_row_bytes",
-            "dv_quantize_w4", "dv_sparse_mlp_w4"]
+            "dv_quantize_w4", "dv_sparse_mlp_w4", "dv_union_mlp_ws_size", "dv_union_mlp"]
 
 
 def status_string(code: int) -> str:
@@ -241,6 +245,21 @@ def sparse_mlp(x, D: Dims, W: dict, idx, k, out, ws, dev_count=None, flags=0, de
     _check(lib().dv_sparse_mlp(ptr(x), B, ctypes.byref(D), ctypes.byref(lw), ptr(idx), k,
                                ptr(dev_count), flags, ptr(out), ptr(dev_status), ptr(ws),
                                ws.numel(), _stream(stream)), "dv_sparse_mlp")
+
+
+def union_mlp(x, D: Dims, W: dict, union_idx, k, out, dev_count=None, flags=0, dev_status=None,
+              ws=None, stream=None):
+    """Batched (B = 8..64) MLP over one union of neurons on the tensor cores."""
+    import torch
+    B = x.shape[0]
+    need = lib().dv_union_mlp_ws_size(B, D.d, k)
+    if ws is None:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    lw = layer_weights(W)
+    _check(lib().dv_union_mlp(ptr(x), B, ctypes.byref(D), ctypes.byref(lw), ptr(union_idx), k,
+                              ptr(dev_count), flags, ptr(out), ptr(dev_status), ptr(ws), ws.numel(),
+                              _stream(stream)), "dv_union_mlp")
+    return ws
 
 
 def w4_row_bytes(d: int) -> int:

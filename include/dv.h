@@ -239,6 +239,20 @@ int dv_sparse_mlp_noalloc(const uint16_t* x, int B, const dv_dims* dims,
                           const int32_t* dev_count, int flags, uint16_t* out, int* dev_status,
                           cudaStream_t stream);
 
+/* ---- batched union MLP on the tensor cores ([DV] §5.2, App. C.1) ------------
+ * For a batch of B = 8, 16, 32 or 64 sequences sharing one union U of their
+ * neuron sets (union_idx[0..k-1], or *dev_count of them, distinct, in [0, F)):
+ * out[b] = x[b] + sum_{j in U} relu(LN2(x[b]) . fc1[j] + b1[j]) fc2T[j] + b2,
+ * as two dense contractions on the tensor cores (fp16 operands: LN2(x) and the
+ * activations rounded to fp16; fp32 accumulation). x, out [B][d] fp16,
+ * d % 16 == 0. ws: dv_union_mlp_ws_size(B, d, k) bytes (0 = unsupported
+ * shape). flags: DV_NO_RESIDUAL. Errors as dv_sparse_mlp, DV_ERR_UNSUPPORTED
+ * for another B. */
+size_t dv_union_mlp_ws_size(int B, int d, int k);
+int dv_union_mlp(const uint16_t* x, int B, const dv_dims* dims, const dv_layer_weights* w,
+                 const int32_t* union_idx, int k, const int32_t* dev_count, int flags,
+                 uint16_t* out, int* dev_status, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* ---- W4A16: 4-bit weight rows for the sparse MLP ([DV] §5.2, Table 7) ------
  * The pages name no format; this library's: groups of DV_W4_GROUP = 128
  * columns of a row, scale s = fp16(max |w| / 7) (fp32 division), code

@@ -176,3 +176,18 @@ def test_w4_validation(L):
     assert m(*args(B=5)) == dv.DV_ERR_DIMS
     assert m(*args(dd=_dims(d=264))) == dv.DV_ERR_DIMS      # not a multiple of 128
     assert m(*args()) == dv.DV_ERR_WORKSPACE
+
+
+def test_union_mlp_validation(L):
+    assert L.dv_union_mlp_ws_size(8, 512, 100) > 0 and L.dv_union_mlp_ws_size(24, 512, 100) == 0
+    assert L.dv_union_mlp_ws_size(4, 512, 100) == 0 and L.dv_union_mlp_ws_size(128, 512, 100) == 0
+    D = _dims()
+    w = _w()
+    u = L.dv_union_mlp
+    args = lambda B=8, idx=FAKE, k=4, ws_bytes=16: (FAKE, B, ctypes.byref(D), ctypes.byref(w), idx,
+                                                    k, None, 0, FAKE + 4096, None, FAKE * 2,
+                                                    ws_bytes, None)
+    assert u(*args(idx=None)) == dv.DV_ERR_NULL
+    assert u(*args(k=0)) == dv.DV_ERR_K
+    assert u(*args(B=12)) == dv.DV_ERR_UNSUPPORTED
+    assert u(*args()) == dv.DV_ERR_WORKSPACE
