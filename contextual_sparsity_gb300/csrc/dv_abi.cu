@@ -10,6 +10,7 @@
 #include <cstdio>
 
 #include "dv_internal.h"
+#include "k_union_tc.h"
 
 namespace dv {
 

@@ -36,14 +36,6 @@ int launch_mlp_w4(const uint16_t* x, int B, int d, int F, const uint16_t* ln_g,
 size_t w4_row_bytes_host(int d);
 int launch_quant_w4(const uint16_t* W, int rows, int d, uint8_t* out, cudaStream_t stream);
 
-// k_union_tc.cu ---------------------------------------------------------------
-size_t union_tc_ws_bytes(int B, int d, int k);
-int launch_union_mlp_tc(const uint16_t* x, int B, int d, int F, const uint16_t* ln_g,
-                        const uint16_t* ln_b, float eps, const uint16_t* fc1, const uint16_t* b1,
-                        const uint16_t* fc2T, const uint16_t* b2, const int32_t* U, int k,
-                        const int32_t* dev_count, bool resid, uint16_t* out, int* st, void* ws,
-                        cudaStream_t s);
-
 // k_fill.cu -------------------------------------------------------------------
 // Missing K/V of the selected units recomputed from the kept inputs.
 int launch_kv_fill(const uint16_t* y_side, const uint32_t* missing, int B, int d, int h_kv,

@@ -11,6 +11,7 @@
 // split over the CTA's warps; the fc2^T contraction in tiles of 16 output
 // columns x B over the union rows, K split over the warps.
 #include "dv_internal.h"
+#include "k_union_tc.h"
 
 namespace dv {
 
