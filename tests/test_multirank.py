@@ -3,6 +3,7 @@ replicas: rank setup, the barrier around the timed region, the max of the
 ranks' times and the whole-job figures — world size 2 on the gloo backend,
 CPU only (no data-path collective exists to test: the replicas share nothing).
 """
+import math
 import os
 import socket
 
@@ -70,3 +71,13 @@ def test_job_figures_weak_scaling():
     assert two["layers_per_s"] == pytest.approx(2 * one["layers_per_s"])
     assert one["gbs_selected"] == pytest.approx(sel / (410.0e-3 / 2400) / 1e9)
     assert one["gbs_all"] == pytest.approx((sel + pred) / (410.0e-3 / 2400) / 1e9)
+
+
+def test_measured_crossing_of_the_gate_sweep():
+    # bench.py's App. E interpolation of two modes' sweep times
+    ctx = [2048, 4096, 8192, 16384]
+    assert bench._measured_crossing(ctx, [10, 12, 16, 24], [13, 13.5, 14, 14.5]) == 4096 + 1.5 / 3.5 * 4096
+    # b leads first, a takes over between 4096 and 8192 (differences 6 -> -0.5)
+    assert math.isclose(bench._measured_crossing(ctx, [20, 18, 16, 14], [10, 12, 16.5, 20]),
+                        4096 + 6 / 6.5 * 4096)
+    assert bench._measured_crossing(ctx, [1, 1, 1, 1], [2, 2, 2, 2]) is None
