@@ -825,10 +825,7 @@ def run_w4_step(a):
         del m, g
         torch.cuda.empty_cache()
     sel, _ = traffic.layer_bytes(w)
-    G = w.h // w.h_kv
-    kN, kH = traffic.k_of(w.keep_N, w.F), traffic.k_of(w.keep_H, w.h_kv)
-    rb = dv.w4_row_bytes(w.d)
-    sel4 = (kH * (2 * G + 2) * w.dh + 2 * kN) * rb + traffic.kv_bytes(w.dh, kH, w.n + 1)
+    sel4 = traffic.layer_bytes_w4(w)
     print(json.dumps({"metric": "decode_step_w4a16", "workload": workload_name(w, not a.sync),
                       "data": "synthetic", "steps": a.steps,
                       "us_per_layer": {k: round(v, 2) for k, v in res.items()},

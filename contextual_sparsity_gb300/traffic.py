@@ -64,3 +64,22 @@ def layer_bytes(w, keep_N=None, keep_H=None, keys=None, union=None):
            + w.B * kv_bytes(w.dh, kH, keys))
     rows = (w.F if keep_N < 1 else 0) + (w.h_kv if keep_H < 1 else 0)
     return sel, pred_bytes(w.d, w.r, rows)
+
+
+def w4_row_bytes(d):
+    """Bytes of one packed 4-bit row: d/2 of codes, d/64 of fp16 group scales,
+    padded to a multiple of 16."""
+    return (d // 2 + d // 64 + 15) // 16 * 16
+
+
+def layer_bytes_w4(w, keep_N=None, keep_H=None, keys=None):
+    """Selected bytes of one decode layer with 4-bit projection and MLP rows
+    (the KV cache stays fp16): (2G + 2) d_h packed rows per selected unit, two
+    per selected neuron, plus the K, V rows of the attended keys."""
+    keep_N = w.keep_N if keep_N is None else keep_N
+    keep_H = w.keep_H if keep_H is None else keep_H
+    G = w.h // w.h_kv
+    kN, kH = k_of(keep_N, w.F), k_of(keep_H, w.h_kv)
+    keys = (w.n + 1) if keys is None else keys
+    return ((kH * (2 * G + 2) * w.dh + 2 * kN) * w4_row_bytes(w.d)
+            + w.B * kv_bytes(w.dh, kH, keys))

@@ -24,3 +24,14 @@ def test_opt175b_headline_bytes():
     sel, pred = traffic.layer_bytes(synth.workload("opt-175b"))
     assert round(sel / 1e6, 1) == 870.8
     assert round(pred / 1e6, 1) == 123.1
+
+
+def test_w4_layer_bytes():
+    # opt-175b: 48 units x 4 x 128 packed rows + 2 x 4915 packed rows (6336 bytes each,
+    # the oracle's packed-row size) + the fp16 K, V rows of 1025 keys
+    from oracle import w4 as ow4
+    w = synth.workload("opt-175b")
+    assert traffic.w4_row_bytes(w.d) == ow4.row_bytes(w.d) == 6336
+    want = (48 * 4 * 128 + 2 * 4915) * 6336 + 48 * 2 * 128 * 1025 * 2
+    assert traffic.layer_bytes_w4(w) == want == 243186816
+    assert traffic.layer_bytes_w4(w, keep_N=0.25) == (48 * 4 * 128 + 2 * 12288) * 6336 + 48 * 2 * 128 * 1025 * 2
