@@ -59,7 +59,8 @@ void note_launch(int tag, int phase, cudaStream_t s) {
 }
 
 static int side_ctas() { return g_tune.side_ctas > 0 ? g_tune.side_ctas : 2 * sm_count(); }
-static int main_ctas() { return g_tune.main_ctas > 0 ? g_tune.main_ctas : sm_count(); }
+int main_ctas() { return g_tune.main_ctas > 0 ? g_tune.main_ctas : sm_count(); }
+int main_ring_bytes() { return g_tune.main_ring; }
 
 static bool g_pdl = true;
 
@@ -111,7 +112,7 @@ static bool aligned(const void* p, size_t a = 16) { return ((uintptr_t)p % a) ==
     if ((p) && !aligned(p)) return DV_ERR_ALIGN; \
   } while (0)
 
-static int check_dims(const dv_dims* D) {
+int check_dims(const dv_dims* D) {
   REQ(D, DV_ERR_NULL);
   REQ(D->d >= 8 && D->d <= 16384 && D->d % 8 == 0, DV_ERR_DIMS);
   REQ(D->h >= 1 && D->h_kv >= 1 && D->h % D->h_kv == 0, DV_ERR_DIMS);
@@ -293,7 +294,7 @@ static int check_weights_attn(const dv_layer_weights* w) {
   return DV_OK;
 }
 
-static int check_weights_mlp(const dv_layer_weights* w) {
+int check_weights_mlp(const dv_layer_weights* w) {
   REQ(w, DV_ERR_NULL);
   REQ_PTR(w->fc1); REQ_PTR(w->fc2T);
   OPT_PTR(w->ln2_g); OPT_PTR(w->ln2_b);

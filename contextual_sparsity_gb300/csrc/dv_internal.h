@@ -104,6 +104,13 @@ extern int g_stage_target;  // bytes per weight-stream ring stage
 // Device properties (cached).
 int sm_count();
 
+// dv_abi.cu: launch-shape tuning in force (dv_set_tuning) and the host-side
+// argument checks the entry points share.
+int main_ctas();        // CTAs of a weight-streaming launch
+int main_ring_bytes();  // its shared-memory ring budget
+int check_dims(const dv_dims* D);
+int check_weights_mlp(const dv_layer_weights* w);
+
 // Launch with (pdl) or without a programmatic dependency on the previous
 // kernel of the stream.
 cudaError_t launch_k(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,

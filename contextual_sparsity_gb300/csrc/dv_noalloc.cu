@@ -56,30 +56,35 @@ extern "C" int dv_sparse_mlp_noalloc(const uint16_t* x, int B, const dv_dims* di
                                      const dv_layer_weights* w, const int32_t* idx, int k,
                                      const int32_t* dev_count, int flags, uint16_t* out,
                                      int* dev_status, cudaStream_t stream) {
+  // The same host-side checks as dv_sparse_mlp (dimensions including ln_eps,
+  // weight pointers and their alignment), then what is particular to this
+  // entry point: fp16 rows only, and the size limit of the built-in array.
+  int rc = check_dims(dims);
+  if (rc != DV_OK) return rc;
+  if (!x || !out) return DV_ERR_NULL;
   auto al16 = [](const void* p) { return ((uintptr_t)p % 16) == 0; };
-  if (!dims || !w || !x || !out || !w->fc1 || !w->fc2T) return DV_ERR_NULL;
-  if (!al16(x) || !al16(out) || !al16(w->fc1) || !al16(w->fc2T) || !al16(w->ln2_g) ||
-      !al16(w->ln2_b))
-    return DV_ERR_ALIGN;
-  if (dims->d < 8 || dims->d > 16384 || dims->d % 8 != 0 || dims->F < 1 || B < 1 || B > 4 ||
-      x == out)
-    return DV_ERR_DIMS;
+  if (!al16(x) || !al16(out)) return DV_ERR_ALIGN;
+  if ((rc = check_weights_mlp(w)) != DV_OK) return rc;
+  // Packed 4-bit rows (DV_W4) are not served here: their rows have another
+  // size, and reading them as fp16 rows would run past the caller's buffers.
+  if (flags & DV_W4) return DV_ERR_UNSUPPORTED;
+  if (B < 1 || B > 4 || x == out) return DV_ERR_DIMS;
   if (!idx) k = dims->F;
   if (k < 1 || k > dims->F) return DV_ERR_K;
 
-  // One CTA per SM, as dv_sparse_mlp, when the partial sums fit; fewer CTAs
-  // (each streaming more rows, at most 256) when they would not; otherwise the
-  // problem is too large for the built-in array.
+  // As many CTAs as dv_sparse_mlp launches (one per SM, or the dv_set_tuning
+  // count) when their partial sums fit the array; fewer CTAs, each streaming
+  // more rows (at most 256), when they would not; otherwise the problem is
+  // too large for the built-in array.
   const size_t per_cta = (size_t)B * dims->d * sizeof(float);
   const long long max_ctas = (long long)(kNoAllocScratchBytes / per_cta);
   const long long need = ((long long)k + 255) / 256;
   if (max_ctas < need || max_ctas < 1) return DV_ERR_WORKSPACE;
-  const int target = (int)std::min<long long>(sm_count(), max_ctas);
+  const int target = (int)std::min<long long>(main_ctas(), max_ctas);
 
-  int rc = DV_OK;
   float* scratch = noalloc_scratch_ptr(&rc);
   if (rc != DV_OK) return rc;
   return launch_mlp(x, B, dims->d, dims->F, w->ln2_g, w->ln2_b, dims->ln_eps, w->fc1, w->b1,
                     w->fc2T, w->b2, idx, k, dev_count, flags & (DV_SKIP_INACTIVE | DV_NO_RESIDUAL),
-                    out, dev_status, scratch, target, 160 * 1024, stream, false);
+                    out, dev_status, scratch, target, main_ring_bytes(), stream, false);
 }

@@ -93,11 +93,14 @@ __global__ void __launch_bounds__(kTcWarps * 32) k_union_fc1(
   if (j0 >= kk) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   // the two union rows this thread reads (rows beyond the union: row 0, zero weight)
+  // (an entry inside the union that is negative or >= F is reported and skipped)
   int ra = j0 + g < kk ? U[j0 + g] : -1, rb = j0 + g + 8 < kk ? U[j0 + g + 8] : -1;
-  if ((ra >= F) || (rb >= F)) {
+  const bool bad_a = j0 + g < kk && (ra < 0 || ra >= F);
+  const bool bad_b = j0 + g + 8 < kk && (rb < 0 || rb >= F);
+  if (bad_a || bad_b) {
     flag(st, DV_DEV_BAD_INDEX);
-    if (ra >= F) ra = -1;
-    if (rb >= F) rb = -1;
+    if (bad_a) ra = -1;
+    if (bad_b) rb = -1;
   }
   const uint16_t* wa = fc1 + (size_t)(ra < 0 ? 0 : ra) * d;
   const uint16_t* wb = fc1 + (size_t)(rb < 0 ? 0 : rb) * d;
@@ -170,7 +173,7 @@ __global__ void __launch_bounds__(kTcWarps * 32) k_union_fc2(
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       int u = jj[q] < kk ? U[jj[q]] : -1;
-      if (u >= F) {
+      if (jj[q] < kk && (u < 0 || u >= F)) {  // reported and skipped
         bad = true;
         u = -1;
       }

@@ -226,14 +226,16 @@ int dv_sparse_mlp(const uint16_t* x, int B, const dv_dims* dims, const dv_layer_
  * memory (a plugin inside a serving engine that owns all device memory, code
  * that must not allocate after start-up, a latency path that cannot take
  * cudaMalloc's synchronisation). The pages have no counterpart: this is a
- * deployment convenience. Same arguments and result as dv_sparse_mlp, minus
- * ws / ws_bytes: the per-CTA partial sums live in a fixed 8 MiB array inside
- * the library, held on every device that loads it until the process exits.
- * The call allocates nothing. Its first call on a device looks the array's
- * device address up; make that first call before any stream capture. Calls
- * that overlap on the GPU share the array and race. Returns DV_ERR_WORKSPACE
- * when B * d fp32 partial sums per CTA cannot fit the array at a launch that
- * keeps at most 256 selected rows per CTA. */
+ * deployment convenience. Same arguments, checks and result as dv_sparse_mlp
+ * with fp16 rows, minus ws / ws_bytes (launch tuning from dv_set_tuning
+ * applies the same way): the per-CTA partial sums live in a fixed 8 MiB array
+ * inside the library, held on every device that loads it until the process
+ * exits. The call allocates nothing. Its first call on a device looks the
+ * array's device address up; make that first call before any stream capture.
+ * Calls that overlap on the GPU share the array and race. Returns
+ * DV_ERR_UNSUPPORTED for DV_W4 (packed 4-bit rows are not served here) and
+ * DV_ERR_WORKSPACE when B * d fp32 partial sums per CTA cannot fit the array
+ * at a launch that keeps at most 256 selected rows per CTA. */
 int dv_sparse_mlp_noalloc(const uint16_t* x, int B, const dv_dims* dims,
                           const dv_layer_weights* w, const int32_t* idx, int k,
                           const int32_t* dev_count, int flags, uint16_t* out, int* dev_status,

@@ -191,3 +191,66 @@ def test_union_mlp_validation(L):
     assert u(*args(k=0)) == dv.DV_ERR_K
     assert u(*args(B=12)) == dv.DV_ERR_UNSUPPORTED
     assert u(*args()) == dv.DV_ERR_WORKSPACE
+
+
+_NOALLOC_CHECKS = r'''
+import ctypes, sys
+sys.path.insert(0, sys.argv[1])
+from contextual_sparsity_gb300 import dv
+L = dv.lib()
+f = L.dv_sparse_mlp_noalloc
+f.restype = ctypes.c_int
+f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(dv.Dims),
+              ctypes.POINTER(dv.LayerWeights), ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+              ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+FAKE = 0x100000
+D = dv.Dims(d=256, h=4, h_kv=4, d_h=64, F=1024, r=32, n_max=80, ln_eps=1e-5)
+w = dv.LayerWeights(*[FAKE if n in ("fc1", "fc2T") else None for n in dv._W_FIELDS])
+call = lambda D=D, w=w, B=1, idx=FAKE, k=4, flags=0, x=FAKE, out=FAKE + 4096: f(
+    x, B, ctypes.byref(D), ctypes.byref(w), idx, k, None, flags, out, None, None)
+res = {
+    "w4": call(flags=dv.DV_W4),
+    "w4_all": call(flags=dv.DV_W4 | dv.DV_SKIP_INACTIVE, idx=None),
+    "eps": call(D=dv.Dims(d=256, h=4, h_kv=4, d_h=64, F=1024, r=32, n_max=80, ln_eps=-1.0)),
+    "heads": call(D=dv.Dims(d=256, h=6, h_kv=4, d_h=64, F=1024, r=32, n_max=80, ln_eps=1e-5)),
+    "ln2_misaligned": call(w=dv.LayerWeights(*[FAKE if n in ("fc1", "fc2T") else
+                                             (FAKE + 2 if n == "ln2_g" else None)
+                                             for n in dv._W_FIELDS])),
+    "null_out": call(out=None),
+    "alias": call(out=FAKE),
+    "k": call(k=0),
+    "B": call(B=5),
+    # 4 rows of 16384 fp32 partial sums need 256 KiB per CTA, and 262144 rows
+    # need at least 1024 CTAs of 256 rows: beyond the 8 MiB array
+    "too_big": call(D=dv.Dims(d=16384, h=128, h_kv=128, d_h=128, F=262144, r=8, n_max=8,
+                              ln_eps=1e-5), B=4, idx=None, k=0),
+}
+print(repr(res))
+'''
+
+
+def test_noalloc_validation_without_a_gpu():
+    """dv_sparse_mlp_noalloc rejects what it cannot serve before it launches
+    anything: packed 4-bit rows, the dimension and weight checks of
+    dv_sparse_mlp, and problems beyond its built-in array. Run in a child
+    process that sees no CUDA device, so a call that got past its checks would
+    fail on the host (a launch error), never reach a GPU."""
+    import ast
+    import sys
+
+    build.build()
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", _NOALLOC_CHECKS, ROOT], env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    res = ast.literal_eval(r.stdout.strip().splitlines()[-1])
+    assert res["w4"] == dv.DV_ERR_UNSUPPORTED
+    assert res["w4_all"] == dv.DV_ERR_UNSUPPORTED
+    assert res["eps"] == dv.DV_ERR_DIMS
+    assert res["heads"] == dv.DV_ERR_DIMS
+    assert res["ln2_misaligned"] == dv.DV_ERR_ALIGN
+    assert res["null_out"] == dv.DV_ERR_NULL
+    assert res["alias"] == dv.DV_ERR_DIMS
+    assert res["k"] == dv.DV_ERR_K
+    assert res["B"] == dv.DV_ERR_DIMS
+    assert res["too_big"] == dv.DV_ERR_WORKSPACE
