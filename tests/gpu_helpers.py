@@ -49,3 +49,24 @@ def check_sets(gpu_idx, ref_scores, k, rtol=1e-6):
     for i in gpu ^ ref:
         assert abs(ref_scores[i] - sk) <= rtol * abs(sk), (i, ref_scores[i], sk)
     return len(gpu ^ ref)
+
+
+def check_kv_kept(gpu_kept, ref_kept, ref_scores, gpu_scores, forced):
+    """KV-selection parity for one KV head: the GPU keeps as many positions as
+    the oracle, every forced position (sinks and window) is kept, and a
+    position kept by one side only must score, on the oracle's smoothed
+    scores, within 2 eps of the oracle's cut score (the lowest score it keeps
+    beyond the forced set), eps the largest GPU-vs-oracle difference of the
+    smoothed scores of this head: a swap is only accepted between positions
+    that the GPU's own rounding could have ordered either way."""
+    gpu, ref = set(int(p) for p in gpu_kept), set(int(p) for p in ref_kept)
+    assert len(gpu) == len(ref)
+    assert set(forced) <= gpu and set(forced) <= ref
+    diff = gpu ^ ref
+    if not diff:
+        return 0
+    eps = float(np.max(np.abs(np.asarray(gpu_scores, float) - np.asarray(ref_scores, float))))
+    cut = min(ref_scores[p] for p in ref - set(forced))
+    for p in diff:
+        assert abs(ref_scores[p] - cut) <= 2 * eps + 1e-6 * abs(cut), (p, ref_scores[p], cut, eps)
+    return len(diff)

@@ -13,7 +13,8 @@ import torch
 
 import oracle
 from contextual_sparsity_gb300 import dv, synth
-from gpu_helpers import TOL, check_sets, host, np16, npf, rel_err, setup_lib, to_dev
+from gpu_helpers import (TOL, check_kv_kept, check_sets, host, np16, npf, rel_err,
+                         setup_lib, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -351,7 +352,8 @@ def test_kv_select_parity(over, n, keep, plant):
         if plant is not None:
             assert plant in kept
         ref_kept = oracle.kv_choose(ref_sm[u], 4, W, b)
-        assert len(set(kept) ^ set(ref_kept)) <= 2
+        forced = [p for p in range(n) if p < 4 or p >= n - W]
+        check_kv_kept(kept, ref_kept, ref_sm[u], gs[u], forced)
         # attention of every query head of u over kept + the new token (slot n)
         G = w.h // w.h_kv
         for g in range(G):

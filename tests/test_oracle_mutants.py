@@ -31,6 +31,8 @@ MUTANTS = {
     "window_off_by_one": ("if (p < n_sinks || p >= n - W) {", "if (p < n_sinks || p > n - W) {"),
     "round_half_away": ("double r = nearbyint(a / q);", "double r = round(a / q);"),
     "v_new_unrounded": ("vd[c] = or_h2d(vnew16[(size_t)u * dh + c]);", ""),
+    "kvsel_table_stride_is_count": ("kept + (size_t)u * kept_ld, cnt[u]", "kept + (size_t)u * cnt[u], cnt[u]"),
+    "kvsel_count_of_first_head": ("kept + (size_t)u * kept_ld, cnt[u], u,", "kept + (size_t)u * kept_ld, cnt[0], u,"),
     "predictor_transposed_p2": ("const uint16_t* row = P2 + (size_t)n * r;\n    for (int j = 0; j < r; ++j) acc += H(row, j) * u[j];",
                                 "for (int j = 0; j < r; ++j) acc += H(P2, (size_t)j * N + n) * u[j];"),
 }
@@ -153,4 +155,33 @@ def test_w4_pins_catch_mutant(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         "tests/test_w4_pins.py"], cwd=tmp_path, env=env,
                        capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
+
+
+LAYER_MUTANTS = {
+    "layer_mlp_reads_x": ("m = mlp_gather(hmid, W[\"fc1\"]", "m = mlp_gather(x, W[\"fc1\"]"),
+    "layer_output_adds_unrounded_h": ("y = round_fp16(h2d(_h(hmid)) + m)",
+                                      "y = round_fp16(xd + a.delta + m)"),
+    "layer_output_unrounded": ("y = round_fp16(h2d(_h(hmid)) + m)", "y = h2d(_h(hmid)) + m"),
+    "layer_attention_residual_dropped": ("hmid = round_fp16(xd + a.delta)",
+                                         "hmid = round_fp16(a.delta)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(LAYER_MUTANTS))
+def test_layer_pins_catch_mutant(name, tmp_path):
+    old, new = LAYER_MUTANTS[name]
+    src = open(os.path.join(ROOT, "oracle", "__init__.py")).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    shutil.copytree(os.path.join(ROOT, "oracle"), tmp_path / "oracle",
+                    ignore=shutil.ignore_patterns("*.so", "__pycache__"))
+    (tmp_path / "oracle" / "__init__.py").write_text(src.replace(old, new))
+    os.makedirs(tmp_path / "tests")
+    for f in ("conftest.py", "test_oracle_pins.py"):
+        shutil.copy(os.path.join(ROOT, "tests", f), tmp_path / "tests" / f)
+    shutil.copytree(os.path.join(ROOT, "tests", "golden"), tmp_path / "tests" / "golden")
+    env = dict(os.environ, PYTHONPATH=str(tmp_path))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        "tests/test_oracle_pins.py", "-k", "test_layer_"],
+                       cwd=tmp_path, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"

@@ -536,3 +536,227 @@ def test_attn_steps_cache_rows_come_from_their_own_token():
     dense = oracle.attn_steps(ys, W, K, V, n0, [[0, 1, 2, 3]] * T)[0]
     assert _close(outs[3].H[3], dense[3].H[3], atol=TIGHT)
     assert not np.allclose(outs[3].H[3], 0.0)
+
+
+# --------------------------------------------------------------------------
+# One decode layer ("Deja Vu" App. C.3: y~ = y + MHA(y), y^ = y~ + MLP(y~)),
+# with the fp16 points where the library hands values on: h = fp16(y + MHA)
+# and y' = fp16(h + MLP(h))
+# --------------------------------------------------------------------------
+def _layer_example():
+    """d 4, one head of d_h 2, F 2, no cached token, eps 0. Worked by hand:
+
+    * LN1(x), x = (4, 2, 4, 2): mean 3, biased variance 1, so z = (1, -1, 1, -1).
+    * W^Q = W^K = 0 and no bias: q = k_new = 0; W^V = 0, b_v = (1, -1): v_new =
+      (1, -1), exact in fp16. With n = 0 the only key is the new token, whose
+      softmax weight is 1: H = (1, -1).
+    * MHA = 1 WoT[0] - 1 WoT[1] + b_o = (1, 0, 0, 2) - (0, -1, 1, -1)
+      + (2^-10, 0, 0, 0) = (1 + 2^-10, 1, -1, 3).
+    * x + MHA = (5 + 2^-10, 3, 3, 5). fp16 values in [4, 8) are 2^-8 apart, so
+      5 + 2^-10 rounds to 5: h = (5, 3, 3, 5).
+    * LN2(h): mean 4, biased variance 1, z' = (1, -1, -1, 1). Neuron 0 reads
+      z'[3] = 1 (bias 0): a_0 = 1. Neuron 1 reads z'[2] + 0.5 = -0.5: a_1 = 0.
+    * MLP = a_0 fc2T[0] + b_2 = (0.25 + 3 2^-11, 0, 0, 0).
+    * h + MLP = (5.25 + 3 2^-11, 3, 3, 5); 3 2^-11 is below half the spacing
+      (2^-9), so y' = (5.25, 3, 3, 5).
+
+    Had the MLP read x instead of h, LN2 would give (1, -1, 1, -1): a_0 = 0,
+    a_1 = 1.5 and y' = (5.0, 3, 3.75, 5). Had y' added the unrounded h, its
+    first entry 5.25 + 5 2^-11 would pass the midpoint 5.25 + 2^-9 and round to
+    5.25 + 2^-8. Unrounded, it would be 5.25 + 3 2^-11.
+    """
+    x = f16([4.0, 2.0, 4.0, 2.0])
+    W = {"Wq": f16(np.zeros((2, 4))), "Wk": f16(np.zeros((2, 4))), "Wv": f16(np.zeros((2, 4))),
+         "bv": f16([1.0, -1.0]),
+         "WoT": f16([[1, 0, 0, 2], [0, -1, 1, -1]]), "bo": f16([2.0 ** -10, 0, 0, 0]),
+         "fc1": f16([[0, 0, 0, 1], [0, 0, 1, 0]]), "b1": f16([0.0, 0.5]),
+         "fc2T": f16([[0.25, 0, 0, 0], [0, 0, 0.5, 0]]), "b2": f16([3 * 2.0 ** -11, 0, 0, 0])}
+    K = np.zeros((1, 2, 2), F16)
+    return x, W, K
+
+
+def test_layer_worked_example():
+    x, W, K = _layer_example()
+    y, hmid, a, m = oracle.layer(x, W, K, K.copy(), 0, [0], [0, 1], eps=0.0)
+    assert _close(a.H, [[1.0, -1.0]], atol=TIGHT)
+    assert _close(a.delta, [1 + 2.0 ** -10, 1, -1, 3], atol=TIGHT)
+    assert hmid.dtype == F16 and np.array_equal(hmid.astype(float), [5, 3, 3, 5])
+    assert _close(m, [0.25 + 3 * 2.0 ** -11, 0, 0, 0], atol=TIGHT)
+    assert y.dtype == F16 and np.array_equal(y.astype(float), [5.25, 3, 3, 5])
+    # neuron 1 is inactive: selecting neuron 0 alone gives the same layer
+    y0, *_ = oracle.layer(x, W, K, K.copy(), 0, [0], [0], eps=0.0)
+    assert np.array_equal(y0, y)
+    # neuron 1 alone: the MLP output is b_2, y' = fp16(h + b_2) = h
+    y1, _, _, m1 = oracle.layer(x, W, K, K.copy(), 0, [0], [1], eps=0.0)
+    assert _close(m1, [3 * 2.0 ** -11, 0, 0, 0], atol=TIGHT)
+    assert np.array_equal(y1.astype(float), [5, 3, 3, 5])
+
+
+def _np_dense_layer(x, W, K, V, n, scale, eps):
+    """The dense OPT layer with numpy's matmul (every head, every neuron): the
+    keep = 1 case of Eq. 1-2, with the new k, v and h, y' rounded to fp16."""
+    def ln(v, g, b):
+        v = np.asarray(v, float)
+        mu = v.mean()
+        out = (v - mu) / np.sqrt(((v - mu) ** 2).mean() + eps)
+        return out * (1.0 if g is None else g.astype(float)) + (0.0 if b is None else b.astype(float))
+
+    get = lambda k: None if W.get(k) is None else W[k].astype(float)
+    bias = lambda k, n_: np.zeros(n_) if W.get(k) is None else W[k].astype(float)
+    hkv, _, dh = K.shape
+    h = W["Wq"].shape[0] // dh
+    G = h // hkv
+    z = ln(x.astype(float), W.get("ln1_g"), W.get("ln1_b"))
+    q = (get("Wq") @ z + bias("bq", h * dh)).reshape(h, dh)
+    k = (get("Wk") @ z + bias("bk", hkv * dh)).astype(F16).astype(float).reshape(hkv, dh)
+    v = (get("Wv") @ z + bias("bv", hkv * dh)).astype(F16).astype(float).reshape(hkv, dh)
+    Hs = np.zeros((h, dh))
+    for j in range(h):
+        u = j // G
+        keys = np.vstack([K[u, :n].astype(float), k[u]])
+        vals = np.vstack([V[u, :n].astype(float), v[u]])
+        s = keys @ q[j] * scale
+        p = np.exp(s - s.max())
+        Hs[j] = (p / p.sum()) @ vals
+    mha = Hs.reshape(-1) @ get("WoT") + bias("bo", x.size)
+    hmid = (x.astype(float) + mha).astype(F16)
+    z2 = ln(hmid.astype(float), W.get("ln2_g"), W.get("ln2_b"))
+    act = np.maximum(get("fc1") @ z2 + bias("b1", W["fc1"].shape[0]), 0.0)
+    mlp = act @ get("fc2T") + bias("b2", x.size)
+    return (hmid.astype(float) + mlp).astype(F16), hmid, mha, mlp
+
+
+def _rand_layer(rng, d=32, h=4, hkv=2, dh=8, F=64, n=6):
+    W = _attn_weights(d, h, hkv, dh, rng, 0.25)
+    W.update({"bq": f16(rng.standard_normal(h * dh) * 0.1),
+              "bk": f16(rng.standard_normal(hkv * dh) * 0.1),
+              "bv": f16(rng.standard_normal(hkv * dh) * 0.1),
+              "bo": f16(rng.standard_normal(d) * 0.1),
+              "ln1_g": f16(rng.normal(1, 0.1, d)), "ln1_b": f16(rng.normal(0, 0.1, d)),
+              "ln2_g": f16(rng.normal(1, 0.1, d)), "ln2_b": f16(rng.normal(0, 0.1, d)),
+              "fc1": f16(rng.standard_normal((F, d)) * 0.25), "b1": f16(rng.normal(-0.2, 0.1, F)),
+              "fc2T": f16(rng.standard_normal((F, d)) * 0.25),
+              "b2": f16(rng.standard_normal(d) * 0.1)})
+    x = f16(rng.standard_normal(d) * 1.5)
+    K = f16(rng.standard_normal((hkv, n + 2, dh)))
+    V = f16(rng.standard_normal((hkv, n + 2, dh)))
+    return x, W, K, V
+
+
+def _ulps_apart(a, b):
+    """fp16 codes apart, for finite values of one sign."""
+    ia = np.asarray(a, F16).view(np.int16).astype(int)
+    ib = np.asarray(b, F16).view(np.int16).astype(int)
+    return np.abs(ia - ib)
+
+
+def test_layer_keep_all_equals_dense_layer():
+    # keep = 1 (every unit and every neuron) is the dense layer: against the
+    # oracle's masked-dense blocks (no index lists) and against numpy's matmul
+    for seed in range(3):
+        x, W, K, V = _rand_layer(np.random.default_rng(100 + seed))
+        hkv, n = K.shape[0], K.shape[1] - 2
+        F = W["fc1"].shape[0]
+        y, hmid, a, m = oracle.layer(x, W, K, V, n, np.arange(hkv), np.arange(F))
+        ad = oracle.attn_masked(x, W, K, V, n, None)
+        assert _close(a.delta, ad.delta, rtol=1e-13, atol=1e-13)
+        md = oracle.mlp_masked(hmid, W["fc1"], W["b1"], W["fc2T"], W["b2"], None,
+                               ln_g=W["ln2_g"], ln_b=W["ln2_b"])
+        assert _close(m, md, rtol=1e-13, atol=1e-13)
+        yn, hn, mha, mlp = _np_dense_layer(x, W, K, V, n, 1.0 / math.sqrt(K.shape[2]), 1e-5)
+        assert _close(a.delta, mha, rtol=1e-12, atol=1e-12)
+        # h rounds the same way on both sides (no value of these draws sits on
+        # a rounding boundary); y' may differ by one fp16 code at a boundary
+        assert np.array_equal(hmid, hn)
+        assert _close(m, mlp, rtol=1e-9, atol=1e-9 * np.abs(mlp).max())
+        assert (_ulps_apart(y, yn) <= 1).all()
+
+
+def test_layer_mlp_reads_the_attention_output():
+    # the MLP block reads h = fp16(x + MHA), not x: equal to the MLP oracle on h
+    x, W, K, V = _rand_layer(np.random.default_rng(7))
+    hkv, n = K.shape[0], K.shape[1] - 2
+    sel_u, sel_n = np.array([0], np.int32), np.arange(0, 64, 3).astype(np.int32)
+    y, hmid, a, m = oracle.layer(x, W, K, V, n, sel_u, sel_n)
+    expect_h = (x.astype(float) + a.delta).astype(F16)
+    assert np.array_equal(hmid, expect_h)
+    m_h = oracle.mlp_gather(expect_h, W["fc1"], W["b1"], W["fc2T"], W["b2"], sel_n,
+                            ln_g=W["ln2_g"], ln_b=W["ln2_b"])
+    m_x = oracle.mlp_gather(x, W["fc1"], W["b1"], W["fc2T"], W["b2"], sel_n,
+                            ln_g=W["ln2_g"], ln_b=W["ln2_b"])
+    assert _close(m, m_h, atol=TIGHT) and not _close(m, m_x, atol=1e-3)
+    assert np.array_equal(y, (expect_h.astype(float) + m_h).astype(F16))
+
+
+# --------------------------------------------------------------------------
+# Attention over the retained KV positions (ByteCross §3.2, §4.1, App. A)
+# --------------------------------------------------------------------------
+def _rand_attn(rng, d=24, h=4, hkv=2, dh=8, n=40):
+    W = _attn_weights(d, h, hkv, dh, rng, 0.3)
+    for k_, n_ in (("bq", h * dh), ("bk", hkv * dh), ("bv", hkv * dh)):
+        W[k_] = f16(rng.standard_normal(n_) * 0.1)
+    W["bo"] = f16(rng.standard_normal(d) * 0.1)
+    W["ln1_g"] = f16(rng.normal(1, 0.1, d))
+    W["ln1_b"] = f16(rng.normal(0, 0.1, d))
+    x = f16(rng.standard_normal(d))
+    K = f16(rng.standard_normal((hkv, n + 3, dh)))
+    V = f16(rng.standard_normal((hkv, n + 3, dh)))
+    return x, W, K, V
+
+
+def test_attn_kvsel_budget_covering_the_cache_is_dense():
+    # b >= n: the selection keeps every position, and attention over the
+    # retained positions is dense attention over the cache
+    rng = np.random.default_rng(31)
+    x, W, K, V = _rand_attn(rng)
+    hkv, n, dh = K.shape[0], 40, K.shape[2]
+    q_obs = f16(rng.standard_normal((4, 8, dh)))
+    kept, _ = oracle.kv_select(q_obs, K, n, 1.0)
+    for u in range(hkv):
+        assert np.array_equal(kept[u], np.arange(n))
+    ld = n + 5
+    table = np.zeros((hkv, ld), np.int32)
+    for u in range(hkv):
+        table[u, :n] = kept[u]
+    r = oracle.attn_kvsel(x, W, K, V, n, table, np.full(hkv, n, np.int32))
+    dn = oracle.attn_masked(x, W, K, V, n, None)
+    assert _close(r.H, dn.H, rtol=1e-13, atol=1e-13)
+    assert _close(r.delta, dn.delta, rtol=1e-13, atol=1e-13)
+    assert np.array_equal(r.knew, dn.knew) and np.array_equal(r.vnew, dn.vnew)
+
+
+def test_attn_kvsel_subset_is_attention_over_those_rows():
+    # per KV head u, its query heads attend over kept[u][:cnt[u]] plus the new
+    # token: (1) the same as attending over a cache that holds only those rows,
+    # (2) the same as the single-query routine given those positions. The
+    # table is wider than the counts and the counts differ per head, so a
+    # wrong row stride or count in the table lookup fails.
+    rng = np.random.default_rng(32)
+    x, W, K, V = _rand_attn(rng)
+    hkv, n, dh = K.shape[0], 40, K.shape[2]
+    h = W["Wq"].shape[0] // dh
+    G = h // hkv
+    scale = 1.0 / math.sqrt(dh)
+    cnt = np.array([5, 11], np.int32)
+    ld = 16
+    table = np.zeros((hkv, ld), np.int32)          # padding: position 0 (valid, wrong)
+    for u in range(hkv):
+        table[u, :cnt[u]] = np.sort(rng.choice(np.arange(1, n), cnt[u], replace=False))
+    r = oracle.attn_kvsel(x, W, K, V, n, table, cnt)
+    z = _np_layernorm(x.astype(float))
+    z = z * W["ln1_g"].astype(float) + W["ln1_b"].astype(float)
+    q = (W["Wq"].astype(float) @ z + W["bq"].astype(float)).reshape(h, dh)
+    for u in range(hkv):
+        pos = table[u, :cnt[u]]
+        Ks = np.zeros((hkv, cnt[u] + 1, dh), F16)
+        Vs = np.zeros_like(Ks)
+        Ks[u, :cnt[u]], Vs[u, :cnt[u]] = K[u, pos], V[u, pos]
+        g = oracle.attn_gather(x, W, Ks, Vs, int(cnt[u]), [u])
+        for j in range(u * G, (u + 1) * G):
+            assert _close(r.H[j], g.H[j], rtol=1e-13, atol=1e-13)
+            Hj = oracle.attend(q[j], K[u], V[u], r.knew[u].astype(float),
+                               r.vnew[u].astype(float), scale, pos=pos)
+            assert _close(r.H[j], Hj, rtol=1e-12, atol=1e-12)
+    # the output projection sums every head's output: delta - b_o = H WoT
+    assert _close(r.delta, r.H.reshape(-1) @ W["WoT"].astype(float) + W["bo"].astype(float),
+                  rtol=1e-12, atol=1e-12)
