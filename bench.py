@@ -37,6 +37,7 @@ from contextual_sparsity_gb300 import dv, synth, traffic  # noqa: E402
 METRIC = "decode µs/layer at batch 1 and HBM GB/s over selected bytes vs 8 TB/s peak"
 UNIT = "µs/layer"
 NOMINAL_HBM = 8000.0
+REPEATS = 5  # timed groups of steps; the headline is their median
 
 
 def parse():
@@ -358,35 +359,66 @@ def oracle_layer_seconds(w, budget_s, W=None, K=None, V=None, x=None, seed=0):
 
 
 def run_reference(a):
+    """The reference arm of this workload: the fp64 C oracle on the host, one
+    layer of the stack per step (the metric is per layer). It runs exactly
+    --warmup untimed and --steps timed single-layer steps, and reports the
+    same config dict as the GPU arm."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    import numpy as np
+
+    import oracle
+
+    oracle.build()
     w = workload(a)
     W = synth.layer_weights(w, 0)
     K, V = synth.kv_cache(w, 0, w.n + 1)
     x = synth.hidden(w)
-    if a.warmup:
-        oracle_layer_seconds(w, 0.0, W, K, V, x)
-    steps = max(1, min(a.steps, 3))
-    tot, reps = 0.0, 0
-    for _ in range(steps):
-        s, r = oracle_layer_seconds(w, a.cpu_seconds / steps, W, K, V, x)
-        tot += s
-        reps += r
-    val = tot / steps * 1e6
-    sample = (f"{reps} single-layer samples of {w.name} (predictor, top-k, sparse attention and "
-              f"MLP in gather form), fp64 C oracle, one thread")
+    h = lambda t: t.detach().cpu().contiguous().numpy()
+    Wh = {k: h(v) for k, v in W.items()}
+    Kh, Vh, xh = h(K[0]), h(V[0]), h(x[0])
+    kN, kH = traffic.k_of(w.keep_N, w.F), traffic.k_of(w.keep_H, w.h_kv)
+
+    def one_layer():
+        s = oracle.predict(xh, Wh["P1"], Wh["P2"])
+        selN = oracle.topk(s[: w.F], kN) if kN < w.F else np.arange(w.F)
+        selH = oracle.topk(s[w.F:], kH) if kH < w.h_kv else np.arange(w.h_kv)
+        oracle.layer(xh, Wh, Kh, Vh, w.n, selH, selN)
+
+    for _ in range(a.warmup):
+        one_layer()
+    t0 = time.perf_counter()
+    for _ in range(a.steps):
+        one_layer()
+    el = time.perf_counter() - t0
+    val = el / a.steps * 1e6
+    sample = (f"{a.steps} timed single-layer steps of {w.name} (predictor, top-k, sparse "
+              f"attention and MLP in gather form), fp64 C oracle, one thread")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(val, 2), "unit": UNIT,
-        "n_gpus": a.gpus, "steps": steps, "warmup": a.warmup,
-        "ms_per_step": round(val * w.layers / 1e3, 3), "higher_is_better": False,
+        "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": round(val / 1e3, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_name(w), "batch": w.B},
+        "step": "one layer of the stack on the host (the metric is per layer)",
+        "timed_region_s": round(el, 3),
+        "config": config_dict(w, not a.sync, a.gpus),
         "cpu_baseline": {"value": round(val, 2), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample, "host_cpus": os.cpu_count()},
         "e2e": {"value": round(val, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }))
+
+
+def config_dict(w, lookahead, wsz):
+    """The workload as both arms report it."""
+    step_gb = sum(traffic.layer_bytes(w)) * w.layers / 1e9
+    return {"workload": workload_name(w, lookahead), "layers": w.layers, "batch": w.B,
+            "n_cached": w.n, "keep_neuron": w.keep_N, "keep_head": w.keep_H,
+            "parallelism": "replicas" if wsz > 1 else "single GPU",
+            "l2": (f"inputs larger than L2 (every step streams "
+                   f"~{step_gb:.1f} GB)" if step_gb > 0.129 else
+                   f"inputs fit in L2 (every step streams ~{step_gb * 1e3:.1f} MB)")}
 
 
 # ---------------------------------------------------------------------------
@@ -453,19 +485,27 @@ def run_ours(a):
     for _ in range(max(3, a.warmup)):
         g.replay()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # Exactly a.steps replays in one timed region; events at the boundaries of
+    # REPEATS equal groups of steps inside it give the median over repeats.
+    reps = max(1, min(REPEATS, a.steps))
+    bounds = [a.steps * i // reps for i in range(reps + 1)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
     with ClockSampler(local) as clk:
         barrier(wsz)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(a.steps):
-                g.replay()
-            e1.record(stream)
+            ev[0].record(stream)
+            for i in range(reps):
+                for _ in range(bounds[i + 1] - bounds[i]):
+                    g.replay()
+                ev[i + 1].record(stream)
         torch.cuda.synchronize()
         barrier(wsz)
-    ms_total = max_over_ranks(e0.elapsed_time(e1), wsz)
+    ms_total = max_over_ranks(ev[0].elapsed_time(ev[-1]), wsz)
     ms_step = ms_total / a.steps
+    group_ms_step = [max_over_ranks(ev[i].elapsed_time(ev[i + 1]), wsz) / (bounds[i + 1] - bounds[i])
+                     for i in range(reps)]
+    median_ms_step = statistics.median(group_ms_step)
     assert m.st.item() == 0, f"device status {m.st.item()}"
 
     union = None
@@ -477,7 +517,9 @@ def run_ours(a):
         uH = sum(x[1] for x in c) / 2 if w.keep_H < 1 else w.h_kv
         union = (uN, uH)
     sel, pred = traffic.layer_bytes(w, keys=m.keys, union=union)
-    job = job_figures(ms_total, a.steps, w.layers, wsz, sel, pred)
+    # the headline: the median over the repeats (each of steps/REPEATS steps)
+    job = job_figures(median_ms_step * a.steps, a.steps, w.layers, wsz, sel, pred)
+    mean_us_layer = ms_total * 1e3 / a.steps / w.layers / wsz
     us_layer = job["us_layer_replica"]
     gbs_sel, gbs_all = job["gbs_selected"], job["gbs_all"]
     print(f"[bench] {us_layer:.2f} us/layer, {gbs_sel:.0f} GB/s selected, {gbs_all:.0f} GB/s all, "
@@ -590,13 +632,16 @@ def run_ours(a):
     out = {
         "metric": METRIC, "value": round(job["us_layer_job"], 2), "unit": UNIT, "n_gpus": wsz,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_step, 4),
+        "timing": {"repeats": reps, "steps_per_repeat": [bounds[i + 1] - bounds[i]
+                                                         for i in range(reps)],
+                   "value_is": "median over the repeats of their mean step time, per layer",
+                   "us_layer_per_repeat": [round(t * 1e3 / w.layers / wsz, 2)
+                                           for t in group_ms_step],
+                   "us_layer_mean_all_steps": round(mean_us_layer, 2),
+                   "timed_region_ms": round(ms_total, 3)},
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "accumulate": "f32", "data": "synthetic (seeded random weights of the workload's shapes)",
-        "config": {"workload": workload_name(w, lookahead), "layers": w.layers, "batch": w.B,
-                   "n_cached": w.n, "keep_neuron": w.keep_N, "keep_head": w.keep_H,
-                   "parallelism": "replicas" if wsz > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (every step streams ~"
-                         f"{(sel + pred) * w.layers / 1e9:.1f} GB)"},
+        "config": config_dict(w, lookahead, wsz),
         "selected_bytes_per_layer": round(sel), "predictor_bytes_per_layer": pred,
         "union_sizes": ({"neurons": union[0], "units": union[1]} if union else None),
         "kv": ({"mode": "retained", "keep": w.keep_KV, "budget": m.b, "keys_read": m.keys,

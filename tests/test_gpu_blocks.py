@@ -313,13 +313,18 @@ def _kvsel_case(over, n, keep, seed=0, plant=None):
     return w, n_max, K, V, q_obs, q
 
 
-@pytest.mark.parametrize("over,n,keep,plant", [
-    (dict(h=8, h_kv=2, obs_window=16), 300, 0.125, 150),
-    (dict(obs_window=64), 2048, 0.125, None),              # composition shape (32q/8kv x 128)
-    (dict(h=8, h_kv=2, obs_window=16), 100, 1.0, None),    # budget covers everything
-    (dict(h=8, h_kv=2, obs_window=16), 300, 0.05, None),   # budget below sinks + window
+@pytest.mark.parametrize("over,n,keep,plant,heads", [
+    (dict(h=8, h_kv=2, obs_window=16), 300, 0.125, 150, None),
+    (dict(obs_window=64), 2048, 0.125, None, None),        # composition shape (32q/8kv x 128)
+    (dict(h=8, h_kv=2, obs_window=16), 100, 1.0, None, None),   # budget covers everything
+    (dict(h=8, h_kv=2, obs_window=16), 300, 0.05, None, None),  # budget below sinks + window
+    # the composition's long contexts: the kernels run on every KV head, the
+    # fp64 oracle's pooled scores are computed for all 8 heads at 32K and for
+    # two of them at 128K (the scoring pass is 34 G multiply-adds per layer)
+    (dict(obs_window=64), 32768, 0.125, 20000, None),
+    (dict(obs_window=64), 131072, 0.125, None, [0, 5]),
 ])
-def test_kv_select_parity(over, n, keep, plant):
+def test_kv_select_parity(over, n, keep, plant, heads):
     w, n_max, K, V, q_obs, q = _kvsel_case(over, n, keep, plant=plant)
     W = w.obs_window
     b = oracle.kv_budget(n, keep)
@@ -338,12 +343,17 @@ def test_kv_select_parity(over, n, keep, plant):
     dv.kv_select_attn(qd, D, kv, n, H, ws, q_obs=q_obs.cuda(), obs_window=W, kv_keep=keep,
                       flags=dv.DV_KV_RESELECT, sel_scores=sel)
     torch.cuda.synchronize()
-    ref_sm = oracle.kv_smooth(oracle.kv_pool(np16(q_obs), np16(K), n))
-    assert rel_err(npf(sel), ref_sm) < 1e-4
+    G = w.h // w.h_kv
+    heads = list(range(w.h_kv)) if heads is None else heads
+    qo, Kh = np16(q_obs), np16(K)
+    ref_sm = np.zeros((w.h_kv, n))
+    for u in heads:
+        ref_sm[u] = oracle.kv_smooth(oracle.kv_pool(qo[u * G:(u + 1) * G], Kh[u:u + 1], n))[0]
     gs = npf(sel)
+    assert rel_err(gs[heads], ref_sm[heads]) < 1e-4
     counts = kc.cpu().numpy()
     scale = w.dh ** -0.5
-    for u in range(w.h_kv):
+    for u in heads:
         kept = oracle.kv_choose(gs[u], 4, W, b)           # same decision on the GPU's scores
         assert counts[u] == len(kept)
         assert np.array_equal(kp[u, : len(kept)].cpu().numpy(), kept)
@@ -355,7 +365,6 @@ def test_kv_select_parity(over, n, keep, plant):
         forced = [p for p in range(n) if p < 4 or p >= n - W]
         check_kv_kept(kept, ref_kept, ref_sm[u], gs[u], forced)
         # attention of every query head of u over kept + the new token (slot n)
-        G = w.h // w.h_kv
         for g in range(G):
             j = u * G + g
             Hr = oracle.attend(npf(q[j]) / scale, np16(K[u]), np16(V[u]),

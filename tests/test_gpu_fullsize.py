@@ -30,12 +30,14 @@ def _step(w, kv_dense=False):
     return m
 
 
-def _check_last_layer(m, kv_sel=None):
-    w, L = m.w, m.L
-    y_prev = m.y_tmp[(L - 3) & 1] if L >= 3 else m.x          # y_{L-2}
-    y_in = m.y_tmp[(L - 2) & 1] if L >= 2 else m.x            # y_{L-1}
-    sets_t = m.sets[(L - 1) & 1][1]
-    Wh = {k: np16(v) for k, v in m.W[L - 1].items()}
+def _check_layer(m, l, y_prev, y_in, y_out, sets_t, kv_sel=None):
+    """Layer l of a replayed step, teacher-forced: its input y_in and its sets
+    come from the GPU. The sets are checked against the oracle's predictor of
+    layer l on y_prev (the look-ahead input y_{l-1}; for layer 0, which
+    predicts synchronously, its own input), and the output y_out against the
+    oracle layer on y_in with those sets."""
+    w = m.w
+    Wh = {k: np16(v) for k, v in m.W[l].items()}
     for b in range(w.B):
         ref = oracle.predict(np16(y_prev[b]), Wh["P1"], Wh["P2"])
         if w.keep_N < 1:
@@ -50,7 +52,7 @@ def _check_last_layer(m, kv_sel=None):
         selN = sets_t["uN"][: c[0]].cpu().numpy() if w.keep_N < 1 else np.arange(w.F)
         selH = sets_t["uH"][: c[1]].cpu().numpy() if w.keep_H < 1 else np.arange(w.h_kv)
         assert np.array_equal(selN, oracle.union(sets_t["idx_N"].cpu().numpy(), w.F))
-    K, V = np16(m.K[L - 1]), np16(m.V[L - 1])
+    K, V = np16(m.K[l]), np16(m.V[l])
     for b in range(w.B):
         if kv_sel is None:
             y_ref, *_ = oracle.layer(np16(y_in[b]), Wh, K[b], V[b], w.n, selH, selN)
@@ -60,18 +62,66 @@ def _check_last_layer(m, kv_sel=None):
             hmid = oracle.round_fp16(npf(y_in[b]) + a.delta)
             mm = oracle.mlp_gather(hmid, Wh["fc1"], Wh["b1"], Wh["fc2T"], Wh.get("b2"), selN)
             y_ref = oracle.round_fp16(hmid.astype(float) + mm)
-        assert rel_err(npf(m.y_out[b]), y_ref) < TOL, b
+        assert rel_err(npf(y_out[b]), y_ref) < TOL, (l, b)
+
+
+def _check_last_layer(m, kv_sel=None):
+    L = m.L
+    y_prev = m.y_tmp[(L - 3) & 1] if L >= 3 else m.x          # y_{L-2}
+    y_in = m.y_tmp[(L - 2) & 1] if L >= 2 else m.x            # y_{L-1}
+    _check_layer(m, L - 1, y_prev, y_in, m.y_out, m.sets[(L - 1) & 1][1], kv_sel)
+
+
+def _check_first_layers(m):
+    """Layers 0 and 1 of the same stack, from a step over its first two layers
+    in the same launch configuration: layer 0 predicts its sets synchronously
+    from its input, layer 1 reads the sets layer 0 looked ahead for it."""
+    w = m.w
+    step2 = dv.Step(m.D, m.keep, m.W[:2], m.kvs[:2], [s for s, _ in m.sets], m.ws, m.step.flags,
+                    m.side, m.evf, m.evj, dev_status=m.st)
+    y_tmp = torch.empty(2, w.B, w.d, dtype=torch.float16, device="cuda")
+    y_out = torch.empty(w.B, w.d, dtype=torch.float16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step2(m.x, y_tmp, y_out, m.n, stream=s)
+    torch.cuda.synchronize()
+    assert m.st.item() == 0, m.st.item()
+    _check_layer(m, 0, m.x, m.x, y_tmp[0], m.sets[0][1])
+    _check_layer(m, 1, m.x, y_tmp[0], y_out, m.sets[1][1])
 
 
 def test_opt175b_stack_as_benchmarked():
     # 24 layers, d 12288, 96 heads, FFN 49152, neuron keep 10 %, head keep 50 %
     m = _step(synth.workload("opt-175b"))
     _check_last_layer(m)
+    _check_first_layers(m)
 
 
 def test_opt67b_stack():
     m = _step(synth.workload("opt-6.7b"))
     _check_last_layer(m)
+    _check_first_layers(m)
+
+
+@pytest.mark.parametrize("kn,kh", [(0.1, 0.25), (0.5, 1.0)])
+def test_opt175b_keep_sweep_corners(kn, kh):
+    # the corners of the benchmarked opt-175b keep sweep, 24 layers
+    m = _step(synth.workload("opt-175b", keep_N=kn, keep_H=kh))
+    _check_last_layer(m)
+
+
+@pytest.mark.parametrize("kn,kh", [(0.1, 1.0), (0.5, 0.5)])
+def test_opt67b_keep_sweep_full_stack(kn, kh):
+    m = _step(synth.workload("opt-6.7b", keep_N=kn, keep_H=kh))
+    _check_last_layer(m)
+
+
+def test_opt66b_batch1_stack():
+    # 16 layers, d 9216, 72 heads, FFN 36864, neuron keep 10 %, head keep 50 %
+    m = _step(synth.workload("opt-66b"))
+    _check_last_layer(m)
+    _check_first_layers(m)
 
 
 @pytest.mark.parametrize("kn,kh", [(0.25, 1.0), (1.0, 0.5), (1.0, 1.0)])
@@ -85,7 +135,7 @@ def test_opt66b_batch4_union():
     _check_last_layer(m)
 
 
-@pytest.mark.parametrize("n", [2048, 8192])
+@pytest.mark.parametrize("n", [2048, 8192, 32768, 131072])
 def test_composition_retained_kv(n):
     # d 4096, 32 query / 8 KV heads x 128, neuron keep 1/2, KV keep 1/8;
     # the full 32 layers, decode through the retained KV buffers
