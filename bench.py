@@ -487,15 +487,15 @@ def run_ours(a):
     torch.cuda.synchronize()
     # Exactly a.steps replays in one timed region; events at the boundaries of
     # REPEATS equal groups of steps inside it give the median over repeats.
-    reps = max(1, min(REPEATS, a.steps))
-    bounds = [a.steps * i // reps for i in range(reps + 1)]
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    n_rep = max(1, min(REPEATS, a.steps))
+    bounds = [a.steps * i // n_rep for i in range(n_rep + 1)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
     with ClockSampler(local) as clk:
         barrier(wsz)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             ev[0].record(stream)
-            for i in range(reps):
+            for i in range(n_rep):
                 for _ in range(bounds[i + 1] - bounds[i]):
                     g.replay()
                 ev[i + 1].record(stream)
@@ -504,7 +504,7 @@ def run_ours(a):
     ms_total = max_over_ranks(ev[0].elapsed_time(ev[-1]), wsz)
     ms_step = ms_total / a.steps
     group_ms_step = [max_over_ranks(ev[i].elapsed_time(ev[i + 1]), wsz) / (bounds[i + 1] - bounds[i])
-                     for i in range(reps)]
+                     for i in range(n_rep)]
     median_ms_step = statistics.median(group_ms_step)
     assert m.st.item() == 0, f"device status {m.st.item()}"
 
@@ -632,8 +632,8 @@ def run_ours(a):
     out = {
         "metric": METRIC, "value": round(job["us_layer_job"], 2), "unit": UNIT, "n_gpus": wsz,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms_step, 4),
-        "timing": {"repeats": reps, "steps_per_repeat": [bounds[i + 1] - bounds[i]
-                                                         for i in range(reps)],
+        "timing": {"repeats": n_rep, "steps_per_repeat": [bounds[i + 1] - bounds[i]
+                                                          for i in range(n_rep)],
                    "value_is": "median over the repeats of their mean step time, per layer",
                    "us_layer_per_repeat": [round(t * 1e3 / w.layers / wsz, 2)
                                            for t in group_ms_step],

@@ -86,6 +86,12 @@ int launch_kv_select(const uint16_t* q_obs, int h, int h_kv, int dh, int W, cons
 
 size_t kv_select_ws_floats(int h, int h_kv, int W, int n);
 
+// k_kvscore_tc.cu: the scoring pass of the KV selection on the tensor cores
+// (pooled [h_kv][n]); DV_ERR_UNSUPPORTED for shapes it does not take.
+int launch_kv_scores_tc(const uint16_t* q_obs, const uint16_t* K, int h, int h_kv, int dh, int W,
+                        int n, int n_max, float scale2, float* stats, size_t stats_floats,
+                        float* pooled, int* st, cudaStream_t stream);
+
 int launch_kv_append(const uint16_t* K, const uint16_t* V, int h_kv, int dh, int n, int n_max,
                      uint16_t* Kr, uint16_t* Vr, const int32_t* kept_count, int b_max,
                      cudaStream_t stream);

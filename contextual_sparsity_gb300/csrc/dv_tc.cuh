@@ -1,0 +1,117 @@
+// dv_tc.cuh -- fifth-generation tensor-core helpers (sm_103a): TMEM
+// allocation, tcgen05.mma issue and completion, TMEM loads, tiled TMA loads
+// through a tensor map, and the shared-memory matrix descriptors they use.
+//
+// Operand tiles live in shared memory in the K-major, 128-byte-swizzled
+// layout a tiled TMA load with CU_TENSOR_MAP_SWIZZLE_128B produces: a box of
+// 64 fp16 columns (128 bytes) x R rows lands as R rows of 128 bytes, 8-row
+// groups 1024 bytes apart, each row's 16-byte chunks permuted by (row % 8).
+// A tile base must be 1024-byte aligned; the k-th 16-column slice of a box
+// starts k * 32 bytes after it (the hardware applies the swizzle to the
+// computed address, so the slice descriptors only move the start address).
+// Accumulators are fp32 in TMEM: lane = row of D (M), column = N index.
+#pragma once
+
+#include <cuda.h>
+
+#include "dv_common.cuh"
+
+namespace dv {
+
+// ---- shared-memory matrix descriptor (tcgen05 form) ----------------------
+// bits 0-13 start address >> 4, 16-29 leading-dimension byte offset >> 4
+// (unused by swizzled K-major layouts; 1 by convention), 32-45 stride byte
+// offset >> 4 (1024 B between 8-row groups), 46-47 descriptor version (1 on
+// this architecture), 61-63 layout (2 = 128-byte swizzle).
+DV_DEV uint64_t sdesc_k128(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+
+// ---- instruction descriptor, kind::f16 ------------------------------------
+// fp16 A and B (format 0), fp32 D (bits 4-5 = 1), both operands K-major
+// (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ---- TMEM allocation (one warp, converged) ---------------------------------
+DV_DEV void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_addr(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+DV_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+DV_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+DV_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one instruction of shape (M, N, 16).
+DV_DEV void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                       bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// The mbarrier receives one arrival once every tcgen05 operation this thread
+// issued before has completed.
+DV_DEV void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (the warp reads its
+// 32-lane quadrant; taddr carries lane << 16 | column).
+DV_DEV void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---- tiled TMA load (no multicast), completion on an mbarrier ---------------
+// x is the innermost coordinate (elements), y the row; x * 2 bytes must be a
+// multiple of 16.
+DV_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+DV_DEV void tma_prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---- host: tensor maps ---------------------------------------------------------
+// A 2-D fp16 tensor of `rows` rows of `cols` elements (row pitch `pitch_elems`),
+// read in boxes of box_rows x 64 columns with the 128-byte swizzle; rows and
+// columns outside the tensor read as zero. Returns false if the driver
+// rejects the description.
+bool make_tmap_f16_sw128(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                         uint64_t pitch_elems, uint32_t box_rows);
+
+}  // namespace dv

@@ -627,22 +627,29 @@ int launch_kv_select(const uint16_t* q_obs, int h, int h_kv, int dh, int W, cons
   float* pooled = mz + (size_t)h * W * 2;
   float* keys = pooled + (size_t)h_kv * n;
   int32_t* kept = reinterpret_cast<int32_t*>(keys + (size_t)h_kv * n);
+  // The scoring contraction on the tensor cores where its shape allows
+  // (d_h 64 or 128, G W a multiple of 64 up to 256); CUDA cores otherwise.
+  int rc_tc = launch_kv_scores_tc(q_obs, K, h, h_kv, dh, W, n, n_max, scale * kLog2e, stats,
+                                  (size_t)h * W * nchunks * 2, pooled, st, stream);
+  if (rc_tc != DV_OK && rc_tc != DV_ERR_UNSUPPORTED) return rc_tc;
   KvSelParams p{q_obs, K, h, h_kv, dh, W, n, n_max, nchunks, scale * kLog2e, stats, mz, pooled};
   const int NQ = G * W;
   const size_t smem0 = (size_t)(dh * NQ + dh * KP) * 4 + (size_t)NQ * (KP / 4) * 2 * 4;
   const size_t smem1 = (size_t)(dh * NQ + dh * KP) * 4 + (size_t)(NQ / 4) * KP * 4;
   if (smem0 > 227 * 1024 || smem1 > 227 * 1024) return DV_ERR_UNSUPPORTED;
-  cudaFuncSetAttribute(k_kv_score<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem0);
-  cudaFuncSetAttribute(k_kv_score<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
-  note_launch(DV_TAG_KVSEL, 0, stream);
-  k_kv_score<0><<<dim3(nchunks, h_kv), 256, smem0, stream>>>(p);
-  note_launch(DV_TAG_KVSEL, 1, stream);
-  note_launch(DV_TAG_KVSEL, 0, stream);
-  k_kv_mz<<<(h * W + 127) / 128, 128, 0, stream>>>(stats, h * W, nchunks, mz);
-  note_launch(DV_TAG_KVSEL, 1, stream);
-  note_launch(DV_TAG_KVSEL, 0, stream);
-  k_kv_score<1><<<dim3(nchunks, h_kv), 256, smem1, stream>>>(p);
-  note_launch(DV_TAG_KVSEL, 1, stream);
+  if (rc_tc == DV_ERR_UNSUPPORTED) {
+    cudaFuncSetAttribute(k_kv_score<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem0);
+    cudaFuncSetAttribute(k_kv_score<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
+    note_launch(DV_TAG_KVSEL, 0, stream);
+    k_kv_score<0><<<dim3(nchunks, h_kv), 256, smem0, stream>>>(p);
+    note_launch(DV_TAG_KVSEL, 1, stream);
+    note_launch(DV_TAG_KVSEL, 0, stream);
+    k_kv_mz<<<(h * W + 127) / 128, 128, 0, stream>>>(stats, h * W, nchunks, mz);
+    note_launch(DV_TAG_KVSEL, 1, stream);
+    note_launch(DV_TAG_KVSEL, 0, stream);
+    k_kv_score<1><<<dim3(nchunks, h_kv), 256, smem1, stream>>>(p);
+    note_launch(DV_TAG_KVSEL, 1, stream);
+  }
   note_launch(DV_TAG_KVSEL, 0, stream);
   k_kv_smooth<<<dim3((n + 255) / 256, h_kv), 256, 0, stream>>>(pooled, n, smooth, n_sinks, W, keys,
                                                                sel_scores);

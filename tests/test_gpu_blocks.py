@@ -318,6 +318,9 @@ def _kvsel_case(over, n, keep, seed=0, plant=None):
     (dict(obs_window=64), 2048, 0.125, None, None),        # composition shape (32q/8kv x 128)
     (dict(h=8, h_kv=2, obs_window=16), 100, 1.0, None, None),   # budget covers everything
     (dict(h=8, h_kv=2, obs_window=16), 300, 0.05, None, None),  # budget below sinks + window
+    # 4 x 24 window queries per KV head: not a multiple of 64, so the scoring
+    # runs on the CUDA-core kernels instead of the tensor cores
+    (dict(h=8, h_kv=2, obs_window=24), 300, 0.125, 150, None),
     # the composition's long contexts: the kernels run on every KV head, the
     # fp64 oracle's pooled scores are computed for all 8 heads at 32K and for
     # two of them at 128K (the scoring pass is 34 G multiply-adds per layer)

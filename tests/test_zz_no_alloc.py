@@ -6,7 +6,7 @@ array inside the library instead of a caller workspace.
 Called through the C ABI, it must give the same block output as dv_sparse_mlp
 (which uses a caller workspace) and as the CPU oracle's gathered MLP, on two
 calls in a row, since every call reuses the same array. The cases include one
-where the array holds fewer partial sums than one per SM (d 16384, batch 4),
+where the array holds fewer partial sums than one per SM (d 12288, batch 4),
 so the launch uses fewer CTAs that each stream more rows. The host-side
 rejections (packed 4-bit rows, sizes beyond the array) are checked without a
 GPU in tests/test_abi.py. This file is collected last on purpose.
@@ -38,9 +38,9 @@ def _fn():
     ("tiny", {}, 1, 0.25),
     ("opt-6.7b", {}, 1, 0.1),
     ("tiny", dict(d=512, F=2048), 4, 0.1),
-    # 4 x 16384 fp32 partial sums per CTA: the 8 MiB array holds 32 of them,
-    # so 6000 rows run on 32 CTAs of up to 188 rows instead of one per SM
-    ("tiny", dict(d=16384, F=6400), 4, 0.9375),
+    # 4 x 12288 fp32 partial sums per CTA: the 8 MiB array holds 42 of them,
+    # so 6000 rows run on 42 CTAs of up to 143 rows instead of one per SM
+    ("tiny", dict(d=12288, F=6400), 4, 0.9375),
 ])
 def test_noalloc_matches_workspace_entry_point_and_oracle(wl, over, B, keep):
     f = _fn()
