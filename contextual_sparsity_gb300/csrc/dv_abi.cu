@@ -440,8 +440,8 @@ int dv_sparse_mlp(const uint16_t* x, int B, const dv_dims* dims, const dv_layer_
 }
 
 size_t dv_union_mlp_ws_size(int B, int d, int k) {
-  if (B < 8 || B > 64 || (B & 7) || B == 24 || B == 40 || B == 48 || B == 56 || d < 16 ||
-      d % 16 || k < 1)
+  if (B < 8 || B > 64 || (B & 7) || B == 24 || B == 40 || B == 48 || B == 56 || d < 64 ||
+      d % 64 || k < 1)
     return 0;
   return union_tc_ws_bytes(B, d, k);
 }
@@ -454,7 +454,7 @@ int dv_union_mlp(const uint16_t* x, int B, const dv_dims* dims, const dv_layer_w
   REQ_PTR(x); REQ_PTR(out); REQ(x != out, DV_ERR_DIMS);
   if ((rc = check_weights_mlp(w)) != DV_OK) return rc;
   REQ(union_idx, DV_ERR_NULL);
-  REQ(dims->d % 16 == 0, DV_ERR_DIMS);
+  REQ(dims->d % 64 == 0, DV_ERR_DIMS);
   REQ(k >= 1 && k <= dims->F, DV_ERR_K);
   const size_t need = dv_union_mlp_ws_size(B, dims->d, k);
   REQ(need > 0, DV_ERR_UNSUPPORTED);

@@ -64,6 +64,11 @@ int launch_pred2(const float* u, int B, int r, const uint16_t* P2, int N, float*
 
 size_t stream_part_bytes(int d, int B, long long max_rows, int target_ctas);
 
+// out[b] = fp16(x[b] + bias + sum_g part[g][b]) in a fixed order of g (x, bias
+// nullable); programmatic dependent launch on the previous kernel.
+int reduce_launch(const float* part, int G, int B, int d, const uint16_t* x, const uint16_t* bias,
+                  uint16_t* out, cudaStream_t stream);
+
 // k_attn.cu ------------------------------------------------------------------
 struct SplitPlan {
   int C;  // keys per split

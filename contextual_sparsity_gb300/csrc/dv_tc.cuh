@@ -28,11 +28,23 @@ DV_DEV uint64_t sdesc_k128(uint32_t saddr) {
          (1ull << 46) | (2ull << 61);
 }
 
+// The same 128-byte-swizzled form with explicit offsets. For an MN-major
+// operand (its M or N index contiguous in memory: 64 fp16 of M per 128-byte
+// row, one row per K index, 8 K rows per 1024-byte atom) the leading offset
+// is the distance between consecutive 64-wide M blocks and the stride offset
+// the distance between consecutive 8-row K groups.
+DV_DEV uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
 // ---- instruction descriptor, kind::f16 ------------------------------------
-// fp16 A and B (format 0), fp32 D (bits 4-5 = 1), both operands K-major
-// (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
-  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// fp16 A and B (format 0), fp32 D (bits 4-5 = 1), A K-major (bit 15 = 0) or
+// MN-major (1), B K-major (bit 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits
+// 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_major = false) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
 }
 
 // ---- TMEM allocation (one warp, converged) ---------------------------------
@@ -91,6 +103,22 @@ DV_DEV void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+DV_DEV void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // ---- tiled TMA load (no multicast), completion on an mbarrier ---------------
 // x is the innermost coordinate (elements), y the row; x * 2 bytes must be a
 // multiple of 16.
@@ -99,6 +127,20 @@ DV_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Four rows r0..r3 (any order, out-of-range rows read as zero) of a 2-D
+// tensor whose map has a box one row high and 64 columns wide, columns
+// x..x+63: 4 x 128 bytes land as four consecutive rows at dst with the
+// map's swizzle.
+DV_DEV void tma_gather4(void* dst, const CUtensorMap* map, int x, int r0, int r1, int r2, int r3,
+                        uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(smem_addr(bar))
       : "memory");
 }
 

@@ -1,37 +1,333 @@
 // k_union_tc.cu -- the sparse MLP of a batch of 8..64 sequences over the union
-// of their neuron sets, on the tensor cores (sm_103a, mma.sync m16n8k16).
+// of their neuron sets, on the fifth-generation tensor cores (sm_103a).
 //
 // "Deja Vu: Contextual Sparsity for Efficient LLMs at Inference Time", §5.2
 // and App. C.1: a batch computes every row over the union U of its sequences'
 // sets, which turns the per-sequence gathers into one dense contraction:
 //   H = relu(Z W1_U^T + b1_U)   (B x |U|),  Z = LN2(x) in fp16
 //   out = x + H W2_U + b2       (B x d)
-// fp16 operands (the 16-bit activations), fp32 accumulation. Three launches:
-// LN2 of the B inputs; the fc1 contraction in tiles of 16 union rows x B, K
-// split over the CTA's warps; the fc2^T contraction in tiles of 16 output
-// columns x B over the union rows, K split over the warps.
+// fp16 operands (the 16-bit activations), fp32 accumulation in TMEM.
+//
+// Launches: LN2 of the B inputs (fp16 Z); the fc1 contraction; the fc2^T
+// contraction; a fixed-order reduce of the fc2 partial sums (+ b2, + x).
+//   fc1: D[128 union rows][Bp] += fc1[U rows][64-column slice] * Z[Bp][slice]^T.
+//        The union rows are gathered by TMA (tile::gather4, four rows per
+//        instruction, 128-byte swizzle), Z slices by tiled TMA loads. Work
+//        units are (row tile, K range); the CTA that completes a row tile's
+//        last K range sums the ranges' fp32 partials in range order, adds b1,
+//        applies ReLU and writes H (fp16) -- deterministic.
+//   fc2: D[128 output columns][Bp] += fc2T[U rows][128 columns]^T * H[Bp][rows]^T.
+//        A is MN-major here (an fc2T row is contiguous along the output
+//        columns): each gathered union row lands as a 128-byte row of two
+//        64-column blocks. Work units are (column tile, union-row range);
+//        each writes an fp32 partial [range][B][d], summed in range order.
+// Bp = max(B, 16) (the instruction shape with M = 128 takes N in steps of
+// 16; rows B..Bp-1 of Z and H feed only columns of D that are never read).
+// One producer warp issues the copies (one gather4 per lane), one thread
+// issues tcgen05.mma, four warps read the accumulators back (tcgen05.ld).
 #include "dv_internal.h"
+#include "dv_tc.cuh"
 #include "k_union_tc.h"
 
 namespace dv {
 
-constexpr int kTcWarps = 4;
+namespace {
 
-// D (16 x 8, fp32) += A (16 x 16, fp16, row-major) * B (16 x 8, fp16, column-major).
-// Fragments (g = lane / 4, c = lane % 4): a[0] = A[g][2c..2c+1],
-// a[1] = A[g+8][2c..], a[2] = A[g][2c+8..], a[3] = A[g+8][2c+8..];
-// b[0] = B[2c..2c+1][g], b[1] = B[2c+8..2c+9][g]; d[0..1] = D[g][2c..2c+1],
-// d[2..3] = D[g+8][2c..2c+1].
-DV_DEV void mma16816(float* d, const uint32_t* a, const uint32_t* b) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+constexpr int kUStages = 6;
+constexpr int kUThreads = 192;       // 4 epilogue warps + producer warp + MMA warp
+constexpr int kUIdxMax = 4096;       // union indices one fc2 unit stages in shared memory
+constexpr uint32_t kUTmemCols = 128; // two accumulators of Bp <= 64 columns
+constexpr int kABytes = 128 * 128;   // A stage: 128 rows (or 2 x 64 columns) x 128 bytes
+
+struct UnionTcParams {
+  int B, Bp, d, F, k, kpad, ksplit1, ksplit2;
+  const int32_t* U;
+  const int32_t* dev_count;
+  const uint16_t* b1;
+  uint16_t* H;    // [Bp][kpad]
+  float* part1;   // [ceil(k/128)][ksplit1][Bp][128]
+  int* cnt1;      // [ceil(k/128)]
+  float* part2;   // [ksplit2][B][d]
+  int* st;
+};
+
+struct USmem {
+  uint32_t a, b, idx, bars, misc, total;
+};
+
+__host__ __device__ inline USmem u_layout(int Bp) {
+  USmem L{};
+  L.a = 0;
+  L.b = L.a + kUStages * kABytes;
+  L.idx = L.b + kUStages * Bp * 128;
+  L.bars = L.idx + kUIdxMax * 4;
+  L.misc = L.bars + 256;
+  L.total = L.misc + 64;
+  return L;
 }
 
-DV_DEV uint32_t ld32(const uint16_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
-DV_DEV uint32_t pack2(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
+DV_DEV int union_count(const UnionTcParams& p) {
+  int kk = p.k;
+  if (p.dev_count) {
+    const int c = *p.dev_count;
+    kk = c < kk ? (c < 0 ? 0 : c) : kk;
+  }
+  return kk;
+}
+
+// A union index as a row coordinate. Positions past the union's end and
+// entries that are not rows of the matrix (reported) read row 0 instead: the
+// fc1 epilogue writes H = 0 for them, so they add nothing in either phase,
+// and no copy addresses a row outside the matrix.
+DV_DEV int row_of(const UnionTcParams& p, int j, int kk, bool& bad) {
+  if (j >= kk) return 0;
+  const int r = p.U[j];
+  if (r < 0 || r >= p.F) {
+    bad = true;
+    return 0;
+  }
+  return r;
+}
+
+// TMEM -> registers: Bp (16, 32 or 64) columns of this thread's lane.
+DV_DEV void tmem_ld_row(uint32_t taddr, int Bp, float* v) {
+  if (Bp == 16) {
+    tmem_ld16(taddr, v);
+  } else {
+    tmem_ld32(taddr, v);
+    if (Bp == 64) tmem_ld32(taddr + 32, v + 32);
+  }
+}
+
+template <int PHASE>
+__global__ void __launch_bounds__(kUThreads, 1)
+    k_union_mlp_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const UnionTcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~uintptr_t(1023));
+  const USmem L = u_layout(p.Bp);
+  uint8_t* sA = sm + L.a;
+  uint8_t* sB = sm + L.b;
+  int* sidx = reinterpret_cast<int*>(sm + L.idx);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L.bars);
+  uint64_t* empty = full + kUStages;
+  uint64_t* accf = empty + kUStages;
+  uint64_t* acce = accf + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L.misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L.misc + 4);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(sm + L.misc + 8);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t bBytes = p.Bp * 128;
+
+  if (tid == 0) {
+    for (int s = 0; s < kUStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&accf[a], 1);
+      mbar_init(&acce[a], 4);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, kUTmemCols);
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // The index list and Z / H come from the kernels before this one.
+  pdl_wait();
+  if (tid == 0) pdl_launch_dependents();
+
+  const int kk = union_count(p);
+  // units: fc1 (row tile, K range); fc2 (column tile, union-row range)
+  const int KB = (p.d + 63) / 64;  // 64-column slices of d
+  const int ntile = PHASE == 1 ? (kk + 127) / 128 : (p.d + 127) / 128;
+  const int ksplit = PHASE == 1 ? p.ksplit1 : p.ksplit2;
+  const int JS = (kk + 63) / 64;   // 64-row stages of the union (fc2)
+  const int nunits = ntile * ksplit;
+  auto stage_range = [&](int part, int& s0, int& s1) {
+    const int tot = PHASE == 1 ? KB : JS;
+    s0 = (int)((long long)tot * part / ksplit);
+    s1 = (int)((long long)tot * (part + 1) / ksplit);
+  };
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    flag(p.st, DV_DEV_TIMEOUT);
+  };
+
+  if (warp == 4) {
+    // ---------------- producer ----------------------------------------------
+    bool bad = false;
+    int it = 0;
+    if (lane == 0) {
+      tma_prefetch_map(&tmW);
+      tma_prefetch_map(&tmX);
+    }
+    for (int u = blockIdx.x; u < nunits && !*abort_flag; u += gridDim.x) {
+      const int tile = u / ksplit, part = u % ksplit;
+      int s0, s1;
+      stage_range(part, s0, s1);
+      // stage the unit's union rows (as row coordinates) in shared memory;
+      // the previous unit's copies that read them have all been issued
+      const int j0 = PHASE == 1 ? tile * 128 : s0 * 64;
+      const int nj = PHASE == 1 ? 128 : (s1 - s0) * 64;
+      __syncwarp();
+      for (int i = lane; i < nj; i += 32) sidx[i] = row_of(p, j0 + i, kk, bad);
+      __syncwarp();
+      for (int sI = s0; sI < s1; ++sI, ++it) {
+        const int s = it % kUStages;
+        int go = 1;
+        if (lane == 0) {
+          if (*abort_flag) {
+            go = 0;
+          } else if (it >= kUStages && !mbar_wait(&empty[s], ((it / kUStages) & 1) ^ 1)) {
+            give_up();
+            go = 0;
+          }
+          if (go) mbar_arrive_expect_tx(&full[s], kABytes + bBytes);
+        }
+        if (!__shfl_sync(0xffffffffu, go, 0)) break;
+        uint8_t* a = sA + s * kABytes;
+        if (PHASE == 1) {
+          // rows 4 lane .. 4 lane + 3 of the tile, columns sI*64 .. +63
+          const int* r = sidx + 4 * lane;
+          tma_gather4(a + lane * 512, &tmW, sI * 64, r[0], r[1], r[2], r[3], &full[s]);
+          if (lane == 0) tma_load_2d(sB + s * bBytes, &tmX, sI * 64, 0, &full[s]);
+        } else {
+          // union rows (sI - s0)*64 + 4 (lane % 16) .. +3, output-column block lane / 16
+          const int mb = lane >> 4, r4 = (lane & 15) * 4;
+          const int* r = sidx + (sI - s0) * 64 + r4;
+          tma_gather4(a + mb * 8192 + r4 * 128, &tmW, tile * 128 + mb * 64, r[0], r[1], r[2], r[3],
+                      &full[s]);
+          if (lane == 0) tma_load_2d(sB + s * bBytes, &tmX, sI * 64, 0, &full[s]);
+        }
+      }
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) flag(p.st, DV_DEV_BAD_INDEX);
+    if (lane == 0)  // every issued copy lands before the CTA exits
+      for (int j = (it > kUStages ? it - kUStages : 0); j < it; ++j)
+        if (!mbar_wait(&full[j % kUStages], (j / kUStages) & 1)) flag(p.st, DV_DEV_TIMEOUT);
+    __syncwarp();
+  } else if (warp == 5) {
+    // ---------------- MMA issuer (one thread) ---------------------------------
+    if (lane == 0) {
+      const uint32_t a0 = smem_addr(sA), b0 = smem_addr(sB);
+      const uint32_t idesc = idesc_f16_f32(128, p.Bp, PHASE == 2);
+      int it = 0, nu = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < nunits && ok && !*abort_flag; u += gridDim.x) {
+        int s0, s1;
+        stage_range(u % ksplit, s0, s1);
+        if (s1 == s0) continue;
+        const int a = nu & 1;
+        if (nu >= 2 && !mbar_wait(&acce[a], ((nu >> 1) & 1) ^ 1)) {
+          give_up();
+          break;
+        }
+        for (int sI = s0; sI < s1; ++sI, ++it) {
+          const int s = it % kUStages;
+          if (*abort_flag || !mbar_wait(&full[s], (it / kUStages) & 1)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            // fc1: A K-major (16 columns = 32 bytes per step); fc2: A MN-major
+            // (16 union rows = 2048 bytes per step, column blocks 8 KB apart)
+            const uint64_t ad = PHASE == 1 ? sdesc_k128(a0 + s * kABytes + ks * 32)
+                                           : sdesc_sw128(a0 + s * kABytes + ks * 2048, 8192, 1024);
+            tc_mma_f16(tmem + a * p.Bp, ad, sdesc_k128(b0 + s * bBytes + ks * 32), idesc,
+                       sI > s0 || ks > 0);
+          }
+          tc_commit(&empty[s]);
+        }
+        if (!ok) break;
+        tc_commit(&accf[a]);
+        ++nu;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: 4 warps, thread = TMEM lane = row / column ----
+    const int row = warp * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+    int nu = 0;
+    bool dead = false;
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
+      const int tile = u / ksplit, part = u % ksplit;
+      int s0, s1;
+      stage_range(part, s0, s1);
+      float v[64];
+#pragma unroll
+      for (int b = 0; b < 64; ++b) v[b] = 0.f;
+      if (s1 > s0) {
+        const int a = nu & 1;
+        if (!dead && (*abort_flag || !mbar_wait(&accf[a], (nu >> 1) & 1))) {
+          give_up();
+          dead = true;
+        }
+        if (!dead) {
+          tc_fence_after();
+          tmem_ld_row(tl + a * p.Bp, p.Bp, v);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acce[a]);
+        }
+        ++nu;
+      }
+      if (PHASE == 2) {
+        // partial sums of this union-row range for 128 output columns
+        const int c = tile * 128 + row;
+        if (c < p.d && !dead)
+          for (int b = 0; b < p.B; ++b)
+            p.part2[((size_t)part * p.B + b) * p.d + c] = v[b];
+        continue;
+      }
+      // fc1: partial sums of this K range, or the whole dot product
+      const int j = tile * 128 + row;
+      bool last = true;
+      if (ksplit > 1) {
+        float* my = p.part1 + ((size_t)(tile * ksplit + part) * p.Bp) * 128 + row;
+        if (!dead)
+          for (int b = 0; b < p.Bp; ++b) my[b * 128] = v[b];
+        __threadfence();
+        consumer_sync(128);
+        if (row == 0) *last_flag = (atomicAdd(&p.cnt1[tile], 1) == ksplit - 1);
+        consumer_sync(128);
+        last = *last_flag;
+        if (last) {
+          __threadfence();
+          for (int b = 0; b < p.Bp; ++b) v[b] = 0.f;
+          for (int q = 0; q < ksplit; ++q) {
+            const float* src = p.part1 + ((size_t)(tile * ksplit + q) * p.Bp) * 128 + row;
+            for (int b = 0; b < p.Bp; ++b) v[b] += __ldcg(src + b * 128);
+          }
+          if (row == 0) p.cnt1[tile] = 0;  // ready for the next call
+        }
+      }
+      if (last && !dead) {
+        float bias = 0.f;
+        const bool on = j < kk && p.U[j] >= 0 && p.U[j] < p.F;
+        if (on && p.b1) bias = h2f(p.b1[p.U[j]]);
+        for (int b = 0; b < p.Bp; ++b)
+          p.H[(size_t)b * p.kpad + j] = on ? f2h(fmaxf(v[b] + bias, 0.f)) : (uint16_t)0;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kUTmemCols);
+  }
+}
 
 // Z[b] = fp16(LN2(x[b])): one CTA per sequence, two passes in fp32.
 __global__ void __launch_bounds__(256) k_union_ln(const uint16_t* __restrict__ x, int d,
@@ -78,193 +374,106 @@ __global__ void __launch_bounds__(256) k_union_ln(const uint16_t* __restrict__ x
   }
 }
 
-// H[b][j] = fp16(relu(Z[b] . fc1[U[j]] + b1[U[j]])) for a tile of 16 union rows.
-template <int NT>
-__global__ void __launch_bounds__(kTcWarps * 32) k_union_fc1(
-    const uint16_t* __restrict__ Z, int B, int d, const uint16_t* __restrict__ fc1,
-    const uint16_t* __restrict__ b1, int F, const int32_t* __restrict__ U, int k,
-    const int32_t* __restrict__ dev_count, uint16_t* __restrict__ H, int ldh, int* st) {
-  __shared__ float red[kTcWarps][16][NT * 8];
-  pdl_wait();
-  if (threadIdx.x == 0) pdl_launch_dependents();
-  int kk = k;
-  if (dev_count) kk = min(kk, *dev_count);
-  const int j0 = blockIdx.x * 16;
-  if (j0 >= kk) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-  // the two union rows this thread reads (rows beyond the union: row 0, zero weight)
-  // (an entry inside the union that is negative or >= F is reported and skipped)
-  int ra = j0 + g < kk ? U[j0 + g] : -1, rb = j0 + g + 8 < kk ? U[j0 + g + 8] : -1;
-  const bool bad_a = j0 + g < kk && (ra < 0 || ra >= F);
-  const bool bad_b = j0 + g + 8 < kk && (rb < 0 || rb >= F);
-  if (bad_a || bad_b) {
-    flag(st, DV_DEV_BAD_INDEX);
-    if (bad_a) ra = -1;
-    if (bad_b) rb = -1;
-  }
-  const uint16_t* wa = fc1 + (size_t)(ra < 0 ? 0 : ra) * d;
-  const uint16_t* wb = fc1 + (size_t)(rb < 0 ? 0 : rb) * d;
-  const uint32_t ma = ra < 0 ? 0u : 0xffffffffu, mb = rb < 0 ? 0u : 0xffffffffu;
-  float acc[NT][4];
-#pragma unroll
-  for (int t = 0; t < NT; ++t)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[t][i] = 0.f;
-  const int ksteps = d / 16;
-  for (int s = warp; s < ksteps; s += kTcWarps) {
-    const int k0 = s * 16 + 2 * c;
-    uint32_t a[4] = {ld32(wa + k0) & ma, ld32(wb + k0) & mb, ld32(wa + k0 + 8) & ma,
-                     ld32(wb + k0 + 8) & mb};
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const uint16_t* zr = Z + (size_t)(t * 8 + g) * d;
-      const uint32_t bf[2] = {ld32(zr + k0), ld32(zr + k0 + 8)};
-      mma16816(acc[t], a, bf);
-    }
-  }
-  // the warps' K slices, summed in warp order
-#pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    red[warp][g][t * 8 + 2 * c] = acc[t][0];
-    red[warp][g][t * 8 + 2 * c + 1] = acc[t][1];
-    red[warp][g + 8][t * 8 + 2 * c] = acc[t][2];
-    red[warp][g + 8][t * 8 + 2 * c + 1] = acc[t][3];
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 16 * B; i += blockDim.x) {
-    const int r = i / B, b = i % B, j = j0 + r;
-    if (j >= kk) continue;
-    float v = 0.f;
-#pragma unroll
-    for (int w = 0; w < kTcWarps; ++w) v += red[w][r][b];
-    const int u = U[j];
-    const bool ok = u >= 0 && u < F;
-    v += (b1 && ok) ? h2f(b1[u]) : 0.f;
-    H[(size_t)b * ldh + j] = f2h(ok && v > 0.f ? v : 0.f);
-  }
+// Host-side plan of one call (shared by the workspace size and the launch).
+struct UnionPlan {
+  int Bp, kpad, ntile1, ksplit1, ksplit2;
+  size_t off_z, off_h, off_p1, off_cnt, off_p2, total;
+};
+
+size_t al256(size_t x) { return (x + 255) / 256 * 256; }
+
+UnionPlan union_plan(int B, int d, int k) {
+  UnionPlan P{};
+  const int sms = sm_count();
+  P.Bp = B < 16 ? 16 : B;
+  P.ntile1 = (k + 127) / 128;
+  P.kpad = P.ntile1 * 128;
+  const int KB = (d + 63) / 64;
+  // about eight units per SM in each phase (balance), at least four K slices
+  // per fc1 unit, and a union-row range per fc2 unit that fits its index stage
+  P.ksplit1 = std::max(1, std::min((8 * sms + P.ntile1 - 1) / P.ntile1, std::max(1, KB / 4)));
+  const int nct = (d + 127) / 128, JS = (k + 63) / 64;
+  const int need = (JS * 64 + kUIdxMax - 1) / kUIdxMax;
+  P.ksplit2 = std::max(need, std::min((8 * sms + nct - 1) / nct, JS));
+  P.ksplit2 = std::max(1, P.ksplit2);
+  size_t off = 0;
+  P.off_z = off;
+  off += al256((size_t)P.Bp * d * 2);
+  P.off_h = off;
+  off += al256((size_t)P.Bp * P.kpad * 2);
+  P.off_p1 = off;
+  off += al256((size_t)P.ntile1 * P.ksplit1 * P.Bp * 128 * 4);
+  P.off_cnt = off;
+  off += al256((size_t)P.ntile1 * 4);
+  P.off_p2 = off;
+  off += al256((size_t)P.ksplit2 * B * d * 4);
+  P.total = off;
+  return P;
 }
 
-// out[b][col] = x[b][col] + b2[col] + sum_j H[b][j] fc2T[U[j]][col], a tile of
-// 16 output columns.
-template <int NT>
-__global__ void __launch_bounds__(kTcWarps * 32) k_union_fc2(
-    const uint16_t* __restrict__ H, int ldh, int B, int d, const uint16_t* __restrict__ fc2T,
-    int F, const uint16_t* __restrict__ b2, const int32_t* __restrict__ U, int k,
-    const int32_t* __restrict__ dev_count, const uint16_t* __restrict__ x,
-    uint16_t* __restrict__ out, int* st) {
-  __shared__ float red[kTcWarps][16][NT * 8];
-  pdl_wait();
-  if (threadIdx.x == 0) pdl_launch_dependents();
-  int kk = k;
-  if (dev_count) kk = min(kk, *dev_count);
-  const int c0 = blockIdx.x * 16;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-  float acc[NT][4];
-#pragma unroll
-  for (int t = 0; t < NT; ++t)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[t][i] = 0.f;
-  const int ksteps = (kk + 15) / 16;
-  bool bad = false;
-  for (int s = warp; s < ksteps; s += kTcWarps) {
-    const int j = s * 16 + 2 * c;  // this thread's union rows: j, j+1, j+8, j+9
-    uint16_t v[8];
-    int jj[4] = {j, j + 1, j + 8, j + 9};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      int u = jj[q] < kk ? U[jj[q]] : -1;
-      if (jj[q] < kk && (u < 0 || u >= F)) {  // reported and skipped
-        bad = true;
-        u = -1;
-      }
-      const uint16_t* row = fc2T + (size_t)(u < 0 ? 0 : u) * d + c0;
-      v[2 * q] = u < 0 ? 0 : row[g];           // A[g][row jj[q]]
-      v[2 * q + 1] = u < 0 ? 0 : row[g + 8];   // A[g+8][row jj[q]]
-    }
-    const uint32_t a[4] = {pack2(v[0], v[2]), pack2(v[1], v[3]), pack2(v[4], v[6]),
-                           pack2(v[5], v[7])};
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const uint16_t* hr = H + (size_t)(t * 8 + g) * ldh;
-      // H beyond the union's count is never written: those rows carry zero A
-      const uint32_t bf[2] = {j + 1 < kk ? ld32(hr + j) : (j < kk ? (uint32_t)hr[j] : 0u),
-                              j + 9 < kk ? ld32(hr + j + 8) : (j + 8 < kk ? (uint32_t)hr[j + 8] : 0u)};
-      mma16816(acc[t], a, bf);
-    }
-  }
-  if (bad) flag(st, DV_DEV_BAD_INDEX);
-#pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    red[warp][g][t * 8 + 2 * c] = acc[t][0];
-    red[warp][g][t * 8 + 2 * c + 1] = acc[t][1];
-    red[warp][g + 8][t * 8 + 2 * c] = acc[t][2];
-    red[warp][g + 8][t * 8 + 2 * c + 1] = acc[t][3];
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 16 * B; i += blockDim.x) {
-    const int r = i / B, b = i % B, col = c0 + r;
-    if (col >= d) continue;
-    float v = 0.f;
-#pragma unroll
-    for (int w = 0; w < kTcWarps; ++w) v += red[w][r][b];
-    v += b2 ? h2f(b2[col]) : 0.f;
-    v += x ? h2f(x[(size_t)b * d + col]) : 0.f;
-    out[(size_t)b * d + col] = f2h(v);
-  }
-}
+}  // namespace
 
-template <int NT>
-static int union_launch(const uint16_t* x, int B, int d, int F, const uint16_t* ln_g,
-                        const uint16_t* ln_b, float eps, const uint16_t* fc1, const uint16_t* b1,
-                        const uint16_t* fc2T, const uint16_t* b2, const int32_t* U, int k,
-                        const int32_t* dev_count, bool resid, uint16_t* out, int* st,
-                        uint16_t* Z, uint16_t* H, int ldh, cudaStream_t s) {
-  note_launch(DV_TAG_MLP, 0, s);
-  k_union_ln<<<B, 256, 0, s>>>(x, d, ln_g, ln_b, eps, Z);
-  note_launch(DV_TAG_MLP, 1, s);
-  if (cudaGetLastError() != cudaSuccess) return DV_ERR_LAUNCH;
-  {
-    void* args[] = {&Z, &B, &d, &fc1, &b1, &F, &U, &k, &dev_count, &H, &ldh, &st};
-    note_launch(DV_TAG_MLP, 0, s);
-    const cudaError_t e = launch_k((const void*)k_union_fc1<NT>, dim3((k + 15) / 16),
-                                   dim3(kTcWarps * 32), 0, s, args, true);
-    note_launch(DV_TAG_MLP, 1, s);
-    if (e != cudaSuccess) return DV_ERR_LAUNCH;
-  }
-  const uint16_t* xr = resid ? x : nullptr;
-  void* args[] = {&H, &ldh, &B, &d, &fc2T, &F, &b2, &U, &k, &dev_count, &xr, &out, &st};
-  note_launch(DV_TAG_MLP, 0, s);
-  const cudaError_t e = launch_k((const void*)k_union_fc2<NT>, dim3((d + 15) / 16),
-                                 dim3(kTcWarps * 32), 0, s, args, true);
-  note_launch(DV_TAG_MLP, 1, s);
-  return e == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
-}
-
-int union_tc_ldh(int k);
-
-size_t union_tc_ws_bytes(int B, int d, int k) {
-  const size_t z = ((size_t)B * d * 2 + 255) / 256 * 256;
-  return z + (size_t)B * union_tc_ldh(k) * 2;
-}
-
-int union_tc_ldh(int k) { return (k + 15) / 16 * 16; }
+size_t union_tc_ws_bytes(int B, int d, int k) { return union_plan(B, d, k).total; }
 
 int launch_union_mlp_tc(const uint16_t* x, int B, int d, int F, const uint16_t* ln_g,
                         const uint16_t* ln_b, float eps, const uint16_t* fc1, const uint16_t* b1,
                         const uint16_t* fc2T, const uint16_t* b2, const int32_t* U, int k,
                         const int32_t* dev_count, bool resid, uint16_t* out, int* st, void* ws,
                         cudaStream_t s) {
-  uint16_t* Z = static_cast<uint16_t*>(ws);
-  uint16_t* H = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) +
-                                            ((size_t)B * d * 2 + 255) / 256 * 256);
-  const int ldh = union_tc_ldh(k);
-  switch (B / 8) {
-    case 1: return union_launch<1>(x, B, d, F, ln_g, ln_b, eps, fc1, b1, fc2T, b2, U, k, dev_count, resid, out, st, Z, H, ldh, s);
-    case 2: return union_launch<2>(x, B, d, F, ln_g, ln_b, eps, fc1, b1, fc2T, b2, U, k, dev_count, resid, out, st, Z, H, ldh, s);
-    case 4: return union_launch<4>(x, B, d, F, ln_g, ln_b, eps, fc1, b1, fc2T, b2, U, k, dev_count, resid, out, st, Z, H, ldh, s);
-    case 8: return union_launch<8>(x, B, d, F, ln_g, ln_b, eps, fc1, b1, fc2T, b2, U, k, dev_count, resid, out, st, Z, H, ldh, s);
-    default: return DV_ERR_UNSUPPORTED;
+  const UnionPlan P = union_plan(B, d, k);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint16_t* Z = reinterpret_cast<uint16_t*>(w + P.off_z);
+  UnionTcParams p{};
+  p.B = B;
+  p.Bp = P.Bp;
+  p.d = d;
+  p.F = F;
+  p.k = k;
+  p.kpad = P.kpad;
+  p.ksplit1 = P.ksplit1;
+  p.ksplit2 = P.ksplit2;
+  p.U = U;
+  p.dev_count = dev_count;
+  p.b1 = b1;
+  p.H = reinterpret_cast<uint16_t*>(w + P.off_h);
+  p.part1 = reinterpret_cast<float*>(w + P.off_p1);
+  p.cnt1 = reinterpret_cast<int*>(w + P.off_cnt);
+  p.part2 = reinterpret_cast<float*>(w + P.off_p2);
+  p.st = st;
+  CUtensorMap tW1, tZ, tW2, tH;
+  if (!make_tmap_f16_sw128(&tW1, fc1, d, F, d, 1) || !make_tmap_f16_sw128(&tZ, Z, d, P.Bp, d, P.Bp) ||
+      !make_tmap_f16_sw128(&tW2, fc2T, d, F, d, 1) ||
+      !make_tmap_f16_sw128(&tH, p.H, P.kpad, P.Bp, P.kpad, P.Bp))
+    return DV_ERR_UNSUPPORTED;
+  const size_t smem = u_layout(P.Bp).total + 1024;
+  if (cudaFuncSetAttribute(k_union_mlp_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess ||
+      cudaFuncSetAttribute(k_union_mlp_tc<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return DV_ERR_LAUNCH;
+  if (cudaMemsetAsync(p.cnt1, 0, (size_t)P.ntile1 * 4, s) != cudaSuccess) return DV_ERR_LAUNCH;
+  note_launch(DV_TAG_MLP, 0, s);
+  k_union_ln<<<B, 256, 0, s>>>(x, d, ln_g, ln_b, eps, Z);
+  note_launch(DV_TAG_MLP, 1, s);
+  if (cudaGetLastError() != cudaSuccess) return DV_ERR_LAUNCH;
+  const int grid = sm_count();
+  {
+    void* args[] = {&tW1, &tZ, &p};
+    note_launch(DV_TAG_MLP, 0, s);
+    const cudaError_t e = launch_k((const void*)k_union_mlp_tc<1>, dim3(grid), dim3(kUThreads),
+                                   smem, s, args, true);
+    note_launch(DV_TAG_MLP, 1, s);
+    if (e != cudaSuccess) return DV_ERR_LAUNCH;
   }
+  {
+    void* args[] = {&tW2, &tH, &p};
+    note_launch(DV_TAG_MLP, 0, s);
+    const cudaError_t e = launch_k((const void*)k_union_mlp_tc<2>, dim3(grid), dim3(kUThreads),
+                                   smem, s, args, true);
+    note_launch(DV_TAG_MLP, 1, s);
+    if (e != cudaSuccess) return DV_ERR_LAUNCH;
+  }
+  return reduce_launch(p.part2, P.ksplit2, B, d, resid ? x : nullptr, b2, out, s);
 }
 
 }  // namespace dv

@@ -245,11 +245,15 @@ int dv_sparse_mlp_noalloc(const uint16_t* x, int B, const dv_dims* dims,
  * For a batch of B = 8, 16, 32 or 64 sequences sharing one union U of their
  * neuron sets (union_idx[0..k-1], or *dev_count of them, distinct, in [0, F)):
  * out[b] = x[b] + sum_{j in U} relu(LN2(x[b]) . fc1[j] + b1[j]) fc2T[j] + b2,
- * as two dense contractions on the tensor cores (fp16 operands: LN2(x) and the
- * activations rounded to fp16; fp32 accumulation). x, out [B][d] fp16,
- * d % 16 == 0. ws: dv_union_mlp_ws_size(B, d, k) bytes (0 = unsupported
- * shape). flags: DV_NO_RESIDUAL. Errors as dv_sparse_mlp, DV_ERR_UNSUPPORTED
- * for another B. */
+ * as two dense contractions on the fifth-generation tensor cores (tcgen05,
+ * accumulators in TMEM; the union rows gathered into shared memory by TMA;
+ * fp16 operands: LN2(x) and the activations rounded to fp16; fp32
+ * accumulation, partial sums added in a fixed order). x, out [B][d] fp16,
+ * d % 64 == 0, d >= 64. An entry of the union outside [0, F) sets
+ * DV_DEV_BAD_INDEX and adds nothing. ws: dv_union_mlp_ws_size(B, d, k) bytes
+ * (0 = unsupported shape); it holds LN2(x), the activations and partial sums.
+ * flags: DV_NO_RESIDUAL. Errors as dv_sparse_mlp, DV_ERR_UNSUPPORTED for
+ * another B. */
 size_t dv_union_mlp_ws_size(int B, int d, int k);
 int dv_union_mlp(const uint16_t* x, int B, const dv_dims* dims, const dv_layer_weights* w,
                  const int32_t* union_idx, int k, const int32_t* dev_count, int flags,

@@ -22,6 +22,7 @@ def _union(F, k, B, rng):
     ("opt-6.7b", dict(d=1024, F=2048), 32, 0.02),
     ("opt-6.7b", dict(d=512, F=4096), 64, 0.01),
     ("opt-175b", dict(F=8192), 8, 0.1),                  # d 12288
+    ("opt-66b", {}, 8, 0.1),                              # d 9216, F 36864: ~21000 union rows
 ])
 def test_union_mlp_parity(wl, over, B, keep):
     setup_lib()
@@ -63,4 +64,4 @@ def test_union_mlp_device_count_and_shapes():
                                 U[: len(U) - 17], ln_g=Wh["ln2_g"], ln_b=Wh["ln2_b"])
         assert rel_err(npf(out[b]), ref) < TOL, b
     assert dv.lib().dv_union_mlp_ws_size(12, 512, 10) == 0          # B not 8, 16, 32 or 64
-    assert dv.lib().dv_union_mlp_ws_size(8, 500, 10) == 0           # d not a multiple of 16
+    assert dv.lib().dv_union_mlp_ws_size(8, 496, 10) == 0           # d not a multiple of 64
