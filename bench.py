@@ -832,7 +832,8 @@ def run_union_tc(a):
                      "us_per_block": round(us, 2), "us_per_sequence": round(us / B, 2),
                      "weight_bytes": by, "gbs": round(by / us / 1e3, 1),
                      "frac": round(by / us / 1e3 / pk, 3),
-                     "kernel": "k_stream<KIND_MLP> (CUDA cores)" if B == 4 else "mma.sync m16n8k16"})
+                     "kernel": "k_stream<KIND_MLP> (CUDA cores)" if B == 4 else
+                     "tcgen05 (TMEM accumulators, rows gathered by TMA gather4)"})
         print(f"[union] B {B}: |U| {len(U)} ({len(U) / w.F:.2f} F), {us:.1f} us", file=sys.stderr,
               flush=True)
     print(json.dumps({"metric": "union_mlp_block", "workload": workload_name(w), "data": "synthetic",
