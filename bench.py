@@ -827,11 +827,19 @@ def run_union_tc(a):
             e1.record(stream)
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / reps
+        # per-launch durations of one more call, each launch between events
+        prof = dv.Profiler(cap=16)
+        prof.start()
+        with torch.cuda.stream(stream):
+            run()
+        prof.stop()
+        torch.cuda.synchronize()
+        launch_us = [round(ms * 1e3, 2) for _, ms in prof.durations_ms()]
         by = traffic.mlp_bytes(w.d, len(U))
         rows.append({"B": B, "union": int(len(U)), "union_frac": round(len(U) / w.F, 3),
                      "us_per_block": round(us, 2), "us_per_sequence": round(us / B, 2),
                      "weight_bytes": by, "gbs": round(by / us / 1e3, 1),
-                     "frac": round(by / us / 1e3 / pk, 3),
+                     "frac": round(by / us / 1e3 / pk, 3), "launch_us": launch_us,
                      "kernel": "k_stream<KIND_MLP> (CUDA cores)" if B == 4 else
                      "tcgen05 (TMEM accumulators, rows gathered by TMA gather4)"})
         print(f"[union] B {B}: |U| {len(U)} ({len(U) / w.F:.2f} F), {us:.1f} us", file=sys.stderr,

@@ -33,14 +33,26 @@ namespace dv {
 
 namespace {
 
-constexpr int kUStages = 6;
-constexpr int kUThreads = 192;       // 4 epilogue warps + producer warp + MMA warp
+constexpr int kUStages = 8;
+// Warps: 0-3 epilogue, 4..4+kUProd-1 producers (each issues a quarter of a
+// stage's copies: one warp issuing all of them sets the pace), then the MMA
+// issuer and the index warp.
+constexpr int kUProd = 8;
+constexpr int kUMmaWarp = 4 + kUProd;
+constexpr int kUIdxWarp = kUMmaWarp + 1;
+constexpr int kUThreads = (kUIdxWarp + 1) * 32;
+constexpr int kUOpsPerProd = 32 / kUProd;  // gather4 copies per producer warp and stage
 constexpr int kUIdxMax = 4096;       // union indices one fc2 unit stages in shared memory
-constexpr uint32_t kUTmemCols = 128; // two accumulators of Bp <= 64 columns
+// Each K step of a stage accumulates into its own TMEM accumulator (kUChains
+// independent chains, summed by the epilogue): with N = Bp as small as 16 one
+// instruction's latency, not its work, would otherwise set the pace.
+constexpr int kUChains = 2;
+constexpr uint32_t kUTmemCols = 512; // 2 buffers x kUChains x Bp (<= 64) columns
 constexpr int kABytes = 128 * 128;   // A stage: 128 rows (or 2 x 64 columns) x 128 bytes
 
 struct UnionTcParams {
   int B, Bp, d, F, k, kpad, ksplit1, ksplit2;
+  const uint16_t* W;  // the phase's weight rows (fc1 or fc2T), [F][d]
   const int32_t* U;
   const int32_t* dev_count;
   const uint16_t* b1;
@@ -60,7 +72,7 @@ __host__ __device__ inline USmem u_layout(int Bp) {
   L.a = 0;
   L.b = L.a + kUStages * kABytes;
   L.idx = L.b + kUStages * Bp * 128;
-  L.bars = L.idx + kUIdxMax * 4;
+  L.bars = L.idx + 2 * kUIdxMax * 4;  // two index buffers: the next unit's fill ahead
   L.misc = L.bars + 256;
   L.total = L.misc + 64;
   return L;
@@ -99,14 +111,14 @@ DV_DEV void tmem_ld_row(uint32_t taddr, int Bp, float* v) {
   }
 }
 
-template <int PHASE>
+template <int PHASE, int BP>
 __global__ void __launch_bounds__(kUThreads, 1)
     k_union_mlp_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    const UnionTcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
-  const USmem L = u_layout(p.Bp);
+  const USmem L = u_layout(BP);
   uint8_t* sA = sm + L.a;
   uint8_t* sB = sm + L.b;
   int* sidx = reinterpret_cast<int*>(sm + L.idx);
@@ -114,26 +126,30 @@ __global__ void __launch_bounds__(kUThreads, 1)
   uint64_t* empty = full + kUStages;
   uint64_t* accf = empty + kUStages;
   uint64_t* acce = accf + 2;
+  uint64_t* ifull = acce + 2;   // index buffer b holds the next unit's rows
+  uint64_t* iempty = ifull + 2; // the producer is done with index buffer b
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L.misc + 4);
   volatile int* last_flag = reinterpret_cast<volatile int*>(sm + L.misc + 8);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t bBytes = p.Bp * 128;
+  constexpr uint32_t bBytes = BP * 128;
 
   if (tid == 0) {
     for (int s = 0; s < kUStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], kUProd);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&accf[a], 1);
       mbar_init(&acce[a], 4);
+      mbar_init(&ifull[a], 1);
+      mbar_init(&iempty[a], kUProd);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kUMmaWarp) {
     tmem_alloc(tmem_slot, kUTmemCols);
     tc_fence_before();
   }
@@ -161,25 +177,65 @@ __global__ void __launch_bounds__(kUThreads, 1)
     flag(p.st, DV_DEV_TIMEOUT);
   };
 
-  if (warp == 4) {
-    // ---------------- producer ----------------------------------------------
+  if (warp == kUIdxWarp) {
+    // ---------------- index warp: each unit's union rows, one unit ahead -------
     bool bad = false;
-    int it = 0;
-    if (lane == 0) {
+    int n = 0;
+    for (int u = blockIdx.x; u < nunits && !*abort_flag; u += gridDim.x, ++n) {
+      const int buf = n & 1;
+      int go = 1;
+      if (lane == 0 && n >= 2 && !mbar_wait(&iempty[buf], ((n >> 1) & 1) ^ 1)) {
+        give_up();
+        go = 0;
+      }
+      if (!__shfl_sync(0xffffffffu, go, 0)) break;
+      __syncwarp();  // lane 0's wait orders the producer's reads before these writes
+      int s0, s1;
+      stage_range(u % ksplit, s0, s1);
+      const int j0 = PHASE == 1 ? (u / ksplit) * 128 : s0 * 64;
+      const int nj = PHASE == 1 ? 128 : (s1 - s0) * 64;
+      int* dst = sidx + buf * kUIdxMax;
+      for (int i0 = 0; i0 < nj; i0 += 32 * 16) {
+        int v[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          const int i = i0 + r * 32 + lane;
+          v[r] = i < nj ? row_of(p, j0 + i, kk, bad) : 0;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          const int i = i0 + r * 32 + lane;
+          if (i < nj) dst[i] = v[r];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ifull[buf]);
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) flag(p.st, DV_DEV_BAD_INDEX);
+    __syncwarp();
+  } else if (warp >= 4 && warp < 4 + kUProd) {
+    // ---------------- producers: copies o = pw*8 .. pw*8+7 of every stage ------
+    const int pw = warp - 4;
+    const int o = pw * kUOpsPerProd + lane;  // this lane's gather4 (lanes < 8)
+    const uint32_t my_tx = kUOpsPerProd * 512 + (pw == 0 ? bBytes : 0);
+    int it = 0, n = 0;
+    if (lane == 0 && pw == 0) {
       tma_prefetch_map(&tmW);
       tma_prefetch_map(&tmX);
     }
-    for (int u = blockIdx.x; u < nunits && !*abort_flag; u += gridDim.x) {
+    for (int u = blockIdx.x; u < nunits && !*abort_flag; u += gridDim.x, ++n) {
       const int tile = u / ksplit, part = u % ksplit;
       int s0, s1;
       stage_range(part, s0, s1);
-      // stage the unit's union rows (as row coordinates) in shared memory;
-      // the previous unit's copies that read them have all been issued
-      const int j0 = PHASE == 1 ? tile * 128 : s0 * 64;
-      const int nj = PHASE == 1 ? 128 : (s1 - s0) * 64;
-      __syncwarp();
-      for (int i = lane; i < nj; i += 32) sidx[i] = row_of(p, j0 + i, kk, bad);
-      __syncwarp();
+      const int buf = n & 1;
+      int ready = 1;
+      if (lane == 0 && !mbar_wait(&ifull[buf], (n >> 1) & 1)) {
+        give_up();
+        ready = 0;
+      }
+      if (!__shfl_sync(0xffffffffu, ready, 0)) break;
+      __syncwarp();  // lane 0's wait orders the index warp's writes before these reads
+      const int* sidx_u = sidx + buf * kUIdxMax;
       for (int sI = s0; sI < s1; ++sI, ++it) {
         const int s = it % kUStages;
         int go = 1;
@@ -190,35 +246,38 @@ __global__ void __launch_bounds__(kUThreads, 1)
             give_up();
             go = 0;
           }
-          if (go) mbar_arrive_expect_tx(&full[s], kABytes + bBytes);
+          if (go) mbar_arrive_expect_tx(&full[s], my_tx);
         }
         if (!__shfl_sync(0xffffffffu, go, 0)) break;
         uint8_t* a = sA + s * kABytes;
-        if (PHASE == 1) {
-          // rows 4 lane .. 4 lane + 3 of the tile, columns sI*64 .. +63
-          const int* r = sidx + 4 * lane;
-          tma_gather4(a + lane * 512, &tmW, sI * 64, r[0], r[1], r[2], r[3], &full[s]);
-          if (lane == 0) tma_load_2d(sB + s * bBytes, &tmX, sI * 64, 0, &full[s]);
-        } else {
-          // union rows (sI - s0)*64 + 4 (lane % 16) .. +3, output-column block lane / 16
-          const int mb = lane >> 4, r4 = (lane & 15) * 4;
-          const int* r = sidx + (sI - s0) * 64 + r4;
-          tma_gather4(a + mb * 8192 + r4 * 128, &tmW, tile * 128 + mb * 64, r[0], r[1], r[2], r[3],
-                      &full[s]);
-          if (lane == 0) tma_load_2d(sB + s * bBytes, &tmX, sI * 64, 0, &full[s]);
+        if (lane < kUOpsPerProd) {
+          if (PHASE == 1) {
+            // rows 4 o .. 4 o + 3 of the tile, columns sI*64 .. +63
+            const int* r = sidx_u + 4 * o;
+            tma_gather4(a + o * 512, &tmW, sI * 64, r[0], r[1], r[2], r[3], &full[s]);
+          } else {
+            // union rows (sI - s0)*64 + 4 (o % 16) .. +3, output-column block o / 16
+            const int mb = o >> 4, r4 = (o & 15) * 4;
+            const int* r = sidx_u + (sI - s0) * 64 + r4;
+            tma_gather4(a + mb * 8192 + r4 * 128, &tmW, tile * 128 + mb * 64, r[0], r[1], r[2],
+                        r[3], &full[s]);
+          }
         }
+        if (lane == 0 && pw == 0) tma_load_2d(sB + s * bBytes, &tmX, sI * 64, 0, &full[s]);
+        __syncwarp();
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&iempty[buf]);  // this warp's copies of the unit are issued
     }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) flag(p.st, DV_DEV_BAD_INDEX);
     if (lane == 0)  // every issued copy lands before the CTA exits
       for (int j = (it > kUStages ? it - kUStages : 0); j < it; ++j)
         if (!mbar_wait(&full[j % kUStages], (j / kUStages) & 1)) flag(p.st, DV_DEV_TIMEOUT);
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kUMmaWarp) {
     // ---------------- MMA issuer (one thread) ---------------------------------
     if (lane == 0) {
       const uint32_t a0 = smem_addr(sA), b0 = smem_addr(sB);
-      const uint32_t idesc = idesc_f16_f32(128, p.Bp, PHASE == 2);
+      const uint32_t idesc = idesc_f16_f32(128, BP, PHASE == 2);
       int it = 0, nu = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < nunits && ok && !*abort_flag; u += gridDim.x) {
@@ -244,8 +303,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
             // (16 union rows = 2048 bytes per step, column blocks 8 KB apart)
             const uint64_t ad = PHASE == 1 ? sdesc_k128(a0 + s * kABytes + ks * 32)
                                            : sdesc_sw128(a0 + s * kABytes + ks * 2048, 8192, 1024);
-            tc_mma_f16(tmem + a * p.Bp, ad, sdesc_k128(b0 + s * bBytes + ks * 32), idesc,
-                       sI > s0 || ks > 0);
+            tc_mma_f16(tmem + (a * kUChains + ks % kUChains) * BP, ad,
+                       sdesc_k128(b0 + s * bBytes + ks * 32), idesc, sI > s0 || ks >= kUChains);
           }
           tc_commit(&empty[s]);
         }
@@ -265,9 +324,9 @@ __global__ void __launch_bounds__(kUThreads, 1)
       const int tile = u / ksplit, part = u % ksplit;
       int s0, s1;
       stage_range(part, s0, s1);
-      float v[64];
+      float v[BP];
 #pragma unroll
-      for (int b = 0; b < 64; ++b) v[b] = 0.f;
+      for (int b = 0; b < BP; ++b) v[b] = 0.f;
       if (s1 > s0) {
         const int a = nu & 1;
         if (!dead && (*abort_flag || !mbar_wait(&accf[a], (nu >> 1) & 1))) {
@@ -276,7 +335,14 @@ __global__ void __launch_bounds__(kUThreads, 1)
         }
         if (!dead) {
           tc_fence_after();
-          tmem_ld_row(tl + a * p.Bp, p.Bp, v);
+          tmem_ld_row(tl + a * kUChains * BP, BP, v);
+#pragma unroll
+          for (int c = 1; c < kUChains; ++c) {
+            float w[BP];
+            tmem_ld_row(tl + (a * kUChains + c) * BP, BP, w);
+#pragma unroll
+            for (int b = 0; b < BP; ++b) v[b] += w[b];
+          }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acce[a]);
@@ -287,17 +353,19 @@ __global__ void __launch_bounds__(kUThreads, 1)
         // partial sums of this union-row range for 128 output columns
         const int c = tile * 128 + row;
         if (c < p.d && !dead)
-          for (int b = 0; b < p.B; ++b)
-            p.part2[((size_t)part * p.B + b) * p.d + c] = v[b];
+#pragma unroll
+          for (int b = 0; b < BP; ++b)
+            if (b < p.B) p.part2[((size_t)part * p.B + b) * p.d + c] = v[b];
         continue;
       }
       // fc1: partial sums of this K range, or the whole dot product
       const int j = tile * 128 + row;
       bool last = true;
       if (ksplit > 1) {
-        float* my = p.part1 + ((size_t)(tile * ksplit + part) * p.Bp) * 128 + row;
+        float* my = p.part1 + ((size_t)(tile * ksplit + part) * BP) * 128 + row;
         if (!dead)
-          for (int b = 0; b < p.Bp; ++b) my[b * 128] = v[b];
+#pragma unroll
+          for (int b = 0; b < BP; ++b) my[b * 128] = v[b];
         __threadfence();
         consumer_sync(128);
         if (row == 0) *last_flag = (atomicAdd(&p.cnt1[tile], 1) == ksplit - 1);
@@ -305,10 +373,12 @@ __global__ void __launch_bounds__(kUThreads, 1)
         last = *last_flag;
         if (last) {
           __threadfence();
-          for (int b = 0; b < p.Bp; ++b) v[b] = 0.f;
+#pragma unroll
+          for (int b = 0; b < BP; ++b) v[b] = 0.f;
           for (int q = 0; q < ksplit; ++q) {
-            const float* src = p.part1 + ((size_t)(tile * ksplit + q) * p.Bp) * 128 + row;
-            for (int b = 0; b < p.Bp; ++b) v[b] += __ldcg(src + b * 128);
+            const float* src = p.part1 + ((size_t)(tile * ksplit + q) * BP) * 128 + row;
+#pragma unroll
+            for (int b = 0; b < BP; ++b) v[b] += __ldcg(src + b * 128);
           }
           if (row == 0) p.cnt1[tile] = 0;  // ready for the next call
         }
@@ -317,13 +387,14 @@ __global__ void __launch_bounds__(kUThreads, 1)
         float bias = 0.f;
         const bool on = j < kk && p.U[j] >= 0 && p.U[j] < p.F;
         if (on && p.b1) bias = h2f(p.b1[p.U[j]]);
-        for (int b = 0; b < p.Bp; ++b)
+#pragma unroll
+        for (int b = 0; b < BP; ++b)
           p.H[(size_t)b * p.kpad + j] = on ? f2h(fmaxf(v[b] + bias, 0.f)) : (uint16_t)0;
       }
     }
   }
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kUMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kUTmemCols);
   }
@@ -389,12 +460,14 @@ UnionPlan union_plan(int B, int d, int k) {
   P.ntile1 = (k + 127) / 128;
   P.kpad = P.ntile1 * 128;
   const int KB = (d + 63) / 64;
-  // about eight units per SM in each phase (balance), at least four K slices
-  // per fc1 unit, and a union-row range per fc2 unit that fits its index stage
+  // about eight fc1 and sixteen fc2 units per SM (balance: the units of a
+  // phase are equal, so a CTA's share differs by at most one), at least four
+  // K slices per fc1 unit, and a union-row range per fc2 unit that fits its
+  // index stage
   P.ksplit1 = std::max(1, std::min((8 * sms + P.ntile1 - 1) / P.ntile1, std::max(1, KB / 4)));
   const int nct = (d + 127) / 128, JS = (k + 63) / 64;
   const int need = (JS * 64 + kUIdxMax - 1) / kUIdxMax;
-  P.ksplit2 = std::max(need, std::min((8 * sms + nct - 1) / nct, JS));
+  P.ksplit2 = std::max(need, std::min((16 * sms + nct - 1) / nct, JS));
   P.ksplit2 = std::max(1, P.ksplit2);
   size_t off = 0;
   P.off_z = off;
@@ -446,10 +519,14 @@ int launch_union_mlp_tc(const uint16_t* x, int B, int d, int F, const uint16_t* 
       !make_tmap_f16_sw128(&tH, p.H, P.kpad, P.Bp, P.kpad, P.Bp))
     return DV_ERR_UNSUPPORTED;
   const size_t smem = u_layout(P.Bp).total + 1024;
-  if (cudaFuncSetAttribute(k_union_mlp_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess ||
-      cudaFuncSetAttribute(k_union_mlp_tc<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+  const void* k1 = P.Bp == 16 ? (const void*)k_union_mlp_tc<1, 16>
+                 : P.Bp == 32 ? (const void*)k_union_mlp_tc<1, 32> : (const void*)k_union_mlp_tc<1, 64>;
+  const void* k2 = P.Bp == 16 ? (const void*)k_union_mlp_tc<2, 16>
+                 : P.Bp == 32 ? (const void*)k_union_mlp_tc<2, 32> : (const void*)k_union_mlp_tc<2, 64>;
+  if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess)
     return DV_ERR_LAUNCH;
   if (cudaMemsetAsync(p.cnt1, 0, (size_t)P.ntile1 * 4, s) != cudaSuccess) return DV_ERR_LAUNCH;
   note_launch(DV_TAG_MLP, 0, s);
@@ -458,18 +535,18 @@ int launch_union_mlp_tc(const uint16_t* x, int B, int d, int F, const uint16_t* 
   if (cudaGetLastError() != cudaSuccess) return DV_ERR_LAUNCH;
   const int grid = sm_count();
   {
+    p.W = fc1;
     void* args[] = {&tW1, &tZ, &p};
     note_launch(DV_TAG_MLP, 0, s);
-    const cudaError_t e = launch_k((const void*)k_union_mlp_tc<1>, dim3(grid), dim3(kUThreads),
-                                   smem, s, args, true);
+    const cudaError_t e = launch_k(k1, dim3(grid), dim3(kUThreads), smem, s, args, true);
     note_launch(DV_TAG_MLP, 1, s);
     if (e != cudaSuccess) return DV_ERR_LAUNCH;
   }
   {
+    p.W = fc2T;
     void* args[] = {&tW2, &tH, &p};
     note_launch(DV_TAG_MLP, 0, s);
-    const cudaError_t e = launch_k((const void*)k_union_mlp_tc<2>, dim3(grid), dim3(kUThreads),
-                                   smem, s, args, true);
+    const cudaError_t e = launch_k(k2, dim3(grid), dim3(kUThreads), smem, s, args, true);
     note_launch(DV_TAG_MLP, 1, s);
     if (e != cudaSuccess) return DV_ERR_LAUNCH;
   }
