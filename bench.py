@@ -59,8 +59,6 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--prefetch", default=None,
-                    help="wo_rows,mlp_rows: L2 prefetch rows per CTA (dv_set_prefetch)")
     ap.add_argument("--tuning", default=None,
                     help="main,side,main_ring_kb,side_ring_kb,attn,pdl,stage_kb (see dv_set_tuning)")
     ap.add_argument("--timeline", type=int, default=0,
@@ -477,8 +475,6 @@ def run_ours(a):
     dv.lib()
     if a.tuning:
         dv.set_tuning(*[int(x) for x in a.tuning.split(",")])
-    if a.prefetch:
-        dv.set_prefetch(*[int(x) for x in a.prefetch.split(",")])
     w = workload(a)
     lookahead = not a.sync
     m = Model(w, dev, lookahead=lookahead, kv_dense=a.kv_dense)

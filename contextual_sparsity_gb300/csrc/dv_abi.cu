@@ -22,7 +22,6 @@ struct Tuning {
   int attn_ctas = 0;        // split-K CTA target; 0: 4 per SM
 };
 static Tuning g_tune;
-int g_pf_wo_rows = 0, g_pf_mlp_rows = 0;
 
 int sm_count() {
   static int cached = 0;
@@ -205,34 +204,23 @@ static int attn_qkv(const uint16_t* x, int B, const dv_dims* D, const dv_layer_w
 
 // Split-K attention with the combine fused, then the Wo^T gather-axpy and the
 // residual.
-// (mlp_*: the MLP launch that follows, whose first fc1 rows the Wo launch
-// prefetches into L2; mlp_fc1 == NULL: no MLP follows.)
 static int attn_rest(const uint16_t* x, int B, const dv_dims* D, const dv_layer_weights* w,
                      const int32_t* sel, int k, const int32_t* dev_count, dv_kv_cache* kv, int n,
                      int flags, uint16_t* out, int* st, void* ws, const WsLayout& L,
-                     cudaStream_t s, const uint16_t* mlp_fc1 = nullptr,
-                     const int32_t* mlp_idx = nullptr, int mlp_k = 0,
-                     const int32_t* mlp_cnt = nullptr) {
+                     cudaStream_t s) {
   const int G = D->h / D->h_kv;
   const bool ret = (flags & DV_KV_RETAINED) != 0;
-  const bool w4 = (flags & DV_W4) != 0;
   const int max_keys = ret ? kv->b_max : n + 1;
   SplitPlan plan = split_plan(max_keys, k, B, attn_ctas());
   if (plan.S > L.S_max) return DV_ERR_WORKSPACE;
-  // The W^O rows the Wo launch streams first are requested into L2 by the
-  // split-K launch, which leaves most of the HBM bandwidth unused.
-  const int wo_grid = stream_ctas_max(256, (long long)k * G * D->d_h, main_ctas());
   int rc = launch_splitk(at<float>(ws, L.qbuf), B, D->d_h, G, D->h_kv, sel, k, dev_count, kv->K,
                          kv->V, n, D->n_max, kv->Kr, kv->Vr, kv->kept_count, kv->b_max,
                          ret ? 1 : 0, plan, at<float>(ws, L.sk), at<float>(ws, L.hcomb),
-                         at<int>(ws, L.cnt), st, s, true, w4 ? nullptr : w->WoT, wo_grid,
-                         g_pf_wo_rows, D->d);
+                         at<int>(ws, L.cnt), st, s, true);
   if (rc != DV_OK) return rc;
-  const int mlp_grid = mlp_fc1 ? stream_ctas_max(256, mlp_k, main_ctas()) : 0;
   rc = launch_wo((flags & DV_NO_RESIDUAL) ? nullptr : x, B, D->d, G, D->d_h, D->h_kv, w->WoT,
                  w->bo, sel, k, dev_count, at<float>(ws, L.hcomb), out, st, at<float>(ws, L.part),
-                 main_ctas(), g_tune.main_ring, s, w4, mlp_fc1, mlp_idx, mlp_k, mlp_cnt, mlp_grid,
-                 g_pf_mlp_rows);
+                 main_ctas(), g_tune.main_ring, s, (flags & DV_W4) != 0);
   if (rc != DV_OK) return rc;
   if (ret && (flags & DV_KV_ADVANCE)) rc = launch_kv_advance(kv->kept_count, D->h_kv, kv->b_max, s);
   return rc;
@@ -388,13 +376,6 @@ int dv_profile(cudaEvent_t* events, int* tags, int cap) {
 }
 
 long long dv_launch_count(void) { return g_launches; }
-
-int dv_set_prefetch(int wo_rows, int mlp_rows) {
-  if (wo_rows < 0 || wo_rows > 4096 || mlp_rows < 0 || mlp_rows > 4096) return DV_ERR_DIMS;
-  g_pf_wo_rows = wo_rows;
-  g_pf_mlp_rows = mlp_rows;
-  return DV_OK;
-}
 
 // Tuning knobs for launch shapes (aux; defaults need no call).
 int dv_set_tuning(int main_ctas, int side_ctas, int main_ring_kb, int side_ring_kb,
@@ -692,8 +673,7 @@ static int decode_layer(const dv_dims* dims, const dv_keep* keep, int B, const d
   const int32_t* selN = nd ? nullptr : (B == 1 ? cur->idx_N : cur->uN);
   const int32_t* cntN = (nd || B == 1) ? nullptr : cur->ucnt;
   const int kNe = (nd || B == 1) ? kN : std::min(dims->F, B * kN);
-  rc = attn_rest(y_in, B, dims, w, selH, kHe, cntH, kv, n, flags, hmid, dev_status, ws, L, main,
-                 w->fc1, selN, kNe, cntN);
+  rc = attn_rest(y_in, B, dims, w, selH, kHe, cntH, kv, n, flags, hmid, dev_status, ws, L, main);
   if (rc != DV_OK) return rc;
   // MLP block: y' = h + MLP_{S_M}(h).
   rc = run_mlp(hmid, B, dims, w, selN, kNe, cntN, flags, y_out, dev_status, ws, L, main, true);

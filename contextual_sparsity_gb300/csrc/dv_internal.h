@@ -45,21 +45,10 @@ int launch_kv_fill(const uint16_t* y_side, const uint32_t* missing, int B, int d
                    uint16_t* K, uint16_t* V, int n, int n_max, int* st, cudaStream_t stream,
                    bool pdl);
 
-// pf_*: L2 prefetch, by each CTA's producer once its own rows are issued, of
-// the first pf_rows fc1 rows the MLP launch that follows streams (its CTA c of
-// pf_grid starts at row pf_k c / pf_grid of pf_idx; pf_cnt: device count).
 int launch_wo(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const uint16_t* WoT,
               const uint16_t* bo, const int32_t* idx, int k, const int32_t* dev_count,
               const float* H, uint16_t* out, int* st, float* part, int target_ctas,
-              int ring_budget, cudaStream_t stream, bool w4 = false,
-              const uint16_t* pf_W = nullptr, const int32_t* pf_idx = nullptr, int pf_k = 0,
-              const int32_t* pf_cnt = nullptr, int pf_grid = 0, int pf_rows = 0);
-
-// Rows per CTA that the latency-bound launches prefetch into L2 for the next
-// weight-streaming launch (dv_set_prefetch).
-extern int g_pf_wo_rows, g_pf_mlp_rows;
-
-int stream_ctas_max(int CH_rows, long long rows, int target);
+              int ring_budget, cudaStream_t stream, bool w4 = false);
 
 int launch_predict(const uint16_t* y, int B, int d, const uint16_t* P1, int r,
                    const uint16_t* P2, int N, int relu, float* scores, int ld, float* u,
@@ -92,8 +81,7 @@ int launch_splitk(const float* q, int B, int dh, int G, int h_kv, const int32_t*
                   const int32_t* dev_count, const uint16_t* K, const uint16_t* V, int n, int n_max,
                   const uint16_t* Kr, const uint16_t* Vr, const int32_t* kept_count, int b_max,
                   int retained, SplitPlan plan, float* part, float* H, int* cnt, int* st,
-                  cudaStream_t stream, bool pdl, const uint16_t* pf_W = nullptr,
-                  int pf_grid = 0, int pf_rows = 0, int d = 0);
+                  cudaStream_t stream, bool pdl);
 
 int launch_kv_select(const uint16_t* q_obs, int h, int h_kv, int dh, int W, const uint16_t* K,
                      const uint16_t* V, int n, int n_max, float scale, int n_sinks, int smooth,

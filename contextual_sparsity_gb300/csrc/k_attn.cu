@@ -38,32 +38,7 @@ struct SplitParams {
   float* H;     // [B][k][G][DH] combined head outputs
   int* cnt;     // [B][k] splits finished per unit (zero between launches)
   int* st;
-  // L2 prefetch of the W^O rows the next launch streams first: its CTA c
-  // (of pf_grid) starts at row kk G dh c / pf_grid; the first pf_rows rows of
-  // every such range are requested while this latency-bound launch leaves
-  // HBM bandwidth unused (pf_W == NULL: none).
-  const uint16_t* pf_W;
-  int pf_grid, pf_rows, d;
 };
-
-// The W^O rows v of the Wo launch (v < kk G dh, in its order: selected unit
-// idx[v / (G dh)], row v % (G dh) of that unit) into L2, a share per CTA.
-template <int DH, int G>
-DV_DEV void prefetch_wo(const SplitParams& p, int kk, int lin, int ncta, int lane) {
-  const long long per = (long long)G * DH, tot = kk * per;
-  const long long T = (long long)p.pf_grid * p.pf_rows;
-  const long long i0 = T * lin / ncta, i1 = T * (lin + 1) / ncta;
-  for (long long i = i0 + lane; i < i1; i += 32) {
-    const int c = (int)(i / p.pf_rows), j = (int)(i % p.pf_rows);
-    const long long v = tot * c / p.pf_grid + j;
-    if (v >= tot * (c + 1) / p.pf_grid) continue;
-    const int e = (int)(v / per), r = (int)(v % per);
-    const int u = p.idx ? p.idx[e] : e;
-    if (u < 0 || u >= p.h_kv) continue;
-    const uint16_t* row = p.pf_W + ((size_t)u * per + r) * p.d;
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row), "r"(p.d * 2) : "memory");
-  }
-}
 
 // Online-softmax merge of (m2, l2, o2) into (m, l, o) (base 2).
 template <int N>
@@ -116,8 +91,6 @@ __global__ void __launch_bounds__(128) k_splitk(const SplitParams p) {
 
   int kk = p.k;
   if (p.dev_count) kk = min(kk, *p.dev_count);
-  if (p.pf_W && b == 0 && warp == 1)
-    prefetch_wo<DH, G>(p, kk, e * gridDim.x + s, gridDim.x * gridDim.y, lane);
   if (e >= kk) return;  // uniform over a unit's splits (one cluster)
   int u = p.idx ? p.idx[e] : e;
   if (u < 0 || u >= p.h_kv) {
@@ -432,8 +405,7 @@ int launch_splitk(const float* q, int B, int dh, int G, int h_kv, const int32_t*
                   const int32_t* dev_count, const uint16_t* K, const uint16_t* V, int n, int n_max,
                   const uint16_t* Kr, const uint16_t* Vr, const int32_t* kept_count, int b_max,
                   int retained, SplitPlan plan, float* part, float* H, int* cnt, int* st,
-                  cudaStream_t stream, bool pdl, const uint16_t* pf_W, int pf_grid, int pf_rows,
-                  int d) {
+                  cudaStream_t stream, bool pdl) {
   const bool cl = plan.S <= kClusterSplits;
   const int nst = (!cl && (plan.C + kChunk - 1) / kChunk > kLongRangeChunks) ? 3 : 2;
   void* fn = nullptr;
@@ -441,8 +413,7 @@ int launch_splitk(const float* q, int B, int dh, int G, int h_kv, const int32_t*
   if (dh == 64) fn = splitk_pick<64>(G, cl, nst);
   if (!fn) return DV_ERR_UNSUPPORTED;
   SplitParams p{q, K, V, Kr, Vr, kept_count, idx, dev_count, k, h_kv, n, n_max, b_max,
-                retained, plan.C, plan.S, part, H, cnt, st,
-                (pf_rows > 0 && pf_grid > 0) ? pf_W : nullptr, pf_grid, pf_rows, d};
+                retained, plan.C, plan.S, part, H, cnt, st};
   void* args[] = {&p};
   const size_t smem = (size_t)nst * 2 * kChunk * dh * 2;  // nst stages of K and V
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)

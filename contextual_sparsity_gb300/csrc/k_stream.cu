@@ -148,13 +148,6 @@ struct StreamParams {
   // partial outputs
   float* part;            // [gridDim][B][d]
   int* st;
-  // Wo: L2 prefetch of the first pf_rows fc1 rows of MLP CTA blockIdx.x (of
-  // pf_grid; its rows start at pf_k blockIdx.x / pf_grid in pf_idx), issued
-  // once this CTA's own rows are all requested (pf_W == NULL: none)
-  const uint16_t* pf_W;
-  const int32_t* pf_idx;
-  const int32_t* pf_cnt;
-  int pf_k, pf_grid, pf_rows;
 };
 
 // Number of selected entries this launch processes.
@@ -386,21 +379,6 @@ __global__ void __launch_bounds__((is_w4(KIND) && B == 1) ? 1024 : (B == 1 ? 544
         }
       }
       if (bad_any) flag(p.st, DV_DEV_BAD_INDEX);
-      if (is_wo(KIND) && p.pf_W && (int)blockIdx.x < p.pf_grid && !*abort_flag) {
-        // the MLP launch's first rows for the CTA that will stand here next
-        int k2 = p.pf_k;
-        if (p.pf_cnt) k2 = min(k2, max(0, *p.pf_cnt));
-        const long long r0 = (long long)k2 * blockIdx.x / p.pf_grid;
-        const long long r1 = (long long)k2 * (blockIdx.x + 1) / p.pf_grid;
-        for (long long v = r0; v < min(r1, r0 + p.pf_rows); ++v) {
-          const int j = p.pf_idx ? p.pf_idx[v] : (int)v;
-          if (j < 0) continue;
-          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                           p.pf_W + (size_t)j * p.d),
-                       "r"(p.d * 2)
-                       : "memory");
-        }
-      }
       // Drain: every issued copy must land before the CTA exits.
       for (int j = (it > g.NS ? it - g.NS : 0); j < it; ++j)
         if (!mbar_wait(&full[j % g.NS], (j / g.NS) & 1)) flag(p.st, DV_DEV_TIMEOUT);
@@ -1216,16 +1194,11 @@ int launch_qkv(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const u
 int launch_wo(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const uint16_t* WoT,
               const uint16_t* bo, const int32_t* idx, int k, const int32_t* dev_count,
               const float* H, uint16_t* out, int* st, float* part, int target_ctas,
-              int ring_budget, cudaStream_t stream, bool w4, const uint16_t* pf_W,
-              const int32_t* pf_idx, int pf_k, const int32_t* pf_cnt, int pf_grid, int pf_rows) {
+              int ring_budget, cudaStream_t stream, bool w4) {
   // x: residual added by the reduce (NULL: none)
   StreamParams p{};
   p.d = d; p.B = B; p.x = x; p.W0 = WoT; p.idx = idx; p.k = k; p.dev_count = dev_count;
   p.G = G; p.dh = dh; p.h_kv = h_kv; p.Hc = H; p.part = part; p.st = st;
-  if (pf_W && pf_rows > 0 && pf_grid > 0 && !w4) {
-    p.pf_W = pf_W; p.pf_idx = pf_idx; p.pf_cnt = pf_cnt; p.pf_k = pf_k; p.pf_grid = pf_grid;
-    p.pf_rows = pf_rows;
-  }
   int grid = 0;
   int rc = launch_stream(w4 ? KIND_WO4 : KIND_WO, p, (long long)k * G * dh, target_ctas,
                          ring_budget, stream,

@@ -150,8 +150,7 @@ EXPORTED = ["dv_version", "dv_status_string", "dv_workspace_size", "dv_set_tunin
             "dv_select_topk", "dv_sparse_mlp", "dv_sparse_attn", "dv_kv_select_attn",
             "dv_decode_layer", "dv_decode_step", "dv_sparse_mlp_noalloc", "dv_plan_bytes",
             "dv_cost_calibrate", "dv_plan_decode", "dv_plan_crossing", "dv_w4_row_bytes",
-            "dv_quantize_w4", "dv_sparse_mlp_w4", "dv_union_mlp_ws_size", "dv_union_mlp",
-            "dv_set_prefetch"]
+            "dv_quantize_w4", "dv_sparse_mlp_w4", "dv_union_mlp_ws_size", "dv_union_mlp"]
 
 
 def status_string(code: int) -> str:
@@ -217,11 +216,6 @@ def set_tuning(main_ctas=0, side_ctas=0, main_ring_kb=160, side_ring_kb=32, attn
                stage_kb=48):
     _check(lib().dv_set_tuning(main_ctas, side_ctas, main_ring_kb, side_ring_kb, attn_ctas, pdl,
                                stage_kb), "dv_set_tuning")
-
-
-def set_prefetch(wo_rows=0, mlp_rows=0):
-    """Rows per CTA prefetched into L2 for the Wo and MLP launches (dv_set_prefetch)."""
-    _check(lib().dv_set_prefetch(wo_rows, mlp_rows), "dv_set_prefetch")
 
 
 # ---------------------------------------------------------------------------

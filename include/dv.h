@@ -192,15 +192,6 @@ int dv_set_tuning(int main_ctas, int side_ctas, int main_ring_kb, int side_ring_
 int dv_profile(cudaEvent_t* events, int* tags, int cap);
 long long dv_launch_count(void);
 
-/* L2 prefetch between launches (aux, process-wide; default 0 = off). In
- * dv_sparse_attn and the decode driver, the split-K launch (latency-bound:
- * it reads a few MB of K/V) requests into L2 the first wo_rows W^O rows of
- * every CTA of the Wo launch that follows; in the decode driver each Wo CTA,
- * once its own rows are requested, does the same for the first mlp_rows fc1
- * rows of the MLP launch's CTA of the same index. Results are unchanged.
- * DV_OK or DV_ERR_DIMS (a count outside 0..4096). */
-int dv_set_prefetch(int wo_rows, int mlp_rows);
-
 /* ---- a2: predictor ([DV] §4.1 "Design", §4.2 "Approach") ------------------
  * scores[b][i] = sum_j act(sum_c y[b][c] P1[j][c]) * P2[i][j] for i < N,
  * act = identity, or ReLU with DV_PRED_RELU. y [B][d] fp16 is the layer input

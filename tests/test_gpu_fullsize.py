@@ -234,23 +234,3 @@ def test_opt67b_stack_w4a16():
     y_ref, _ = ow4.layer(np16(y_in[0]), Wo, np16(m.K[L - 1][0]), np16(m.V[L - 1][0]), w.n,
                          sets_t["idx_H"][0].cpu().numpy(), sets_t["idx_N"][0].cpu().numpy())
     assert rel_err(npf(m.y_out[0]), y_ref.astype(np.float64)) < TOL
-
-
-def test_l2_prefetch_changes_nothing():
-    # the L2 prefetch between launches (dv_set_prefetch) moves no result: the
-    # decode step gives the same bits with and without it
-    setup_lib()
-    dv.set_tuning()
-    w = synth.workload("opt-6.7b", layers=4)
-    m = bench.Model(w, torch.device("cuda", 0), lookahead=True)
-    s = torch.cuda.Stream()
-    outs = []
-    for pf in ((0, 0), (24, 16)):
-        dv.set_prefetch(*pf)
-        g, _ = m.capture(s)
-        g.replay()
-        torch.cuda.synchronize()
-        assert m.st.item() == 0
-        outs.append(m.y_out.clone())
-    dv.set_prefetch(0, 0)
-    assert torch.equal(outs[0], outs[1])
