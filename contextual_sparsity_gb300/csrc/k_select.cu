@@ -266,17 +266,29 @@ __global__ void __cluster_dims__(kClusterTopk, 1, 1) __launch_bounds__(kTopkThre
   bool nan_seen = false;
   float fmn = INFINITY, fmx = -INFINITY;
   uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;
-  for (int i = tid; i < cn; i += NT) {
-    const float f = s[c0 + i];
-    nan_seen |= isnan(f);
-    if (!isnan(f)) {
-      fmn = fminf(fmn, f);
-      fmx = fmaxf(fmx, f);
+  // eight loads in flight per thread (one round trip per 8 NT scores, not per NT)
+  for (int i0 = 0; i0 < cn; i0 += 8 * NT) {
+    float fv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + j * NT + tid;
+      fv[j] = i < cn ? s[c0 + i] : 0.f;
     }
-    const uint32_t key = key_of(f);
-    kmn = min(kmn, key);
-    kmx = max(kmx, key);
-    keys[i] = key;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + j * NT + tid;
+      if (i >= cn) continue;
+      const float f = fv[j];
+      nan_seen |= isnan(f);
+      if (!isnan(f)) {
+        fmn = fminf(fmn, f);
+        fmx = fmaxf(fmx, f);
+      }
+      const uint32_t key = key_of(f);
+      kmn = min(kmn, key);
+      kmx = max(kmx, key);
+      keys[i] = key;
+    }
   }
   for (int i = tid; i < kRangeBins; i += NT) hist[i] = 0;
   if (tid == 0) lcount = 0;
@@ -311,13 +323,26 @@ __global__ void __cluster_dims__(kClusterTopk, 1, 1) __launch_bounds__(kTopkThre
   fmx = -INFINITY;
   kmn = 0xFFFFFFFFu;
   kmx = 0u;
-  for (int r = 0; r < kClusterTopk; ++r) {
-    const float* pf = cluster.map_shared_rank(mmf, r);
-    const uint32_t* pk = cluster.map_shared_rank(mmk, r);
-    fmn = fminf(fmn, pf[0]);
-    fmx = fmaxf(fmx, pf[1]);
-    kmn = min(kmn, pk[0]);
-    kmx = max(kmx, pk[1]);
+  {
+    // the peers' values: all remote reads issued before any is used
+    float pf0[kClusterTopk], pf1[kClusterTopk];
+    uint32_t pk0[kClusterTopk], pk1[kClusterTopk];
+#pragma unroll
+    for (int r = 0; r < kClusterTopk; ++r) {
+      const float* pf = cluster.map_shared_rank(mmf, r);
+      const uint32_t* pk = cluster.map_shared_rank(mmk, r);
+      pf0[r] = pf[0];
+      pf1[r] = pf[1];
+      pk0[r] = pk[0];
+      pk1[r] = pk[1];
+    }
+#pragma unroll
+    for (int r = 0; r < kClusterTopk; ++r) {
+      fmn = fminf(fmn, pf0[r]);
+      fmx = fmaxf(fmx, pf1[r]);
+      kmn = min(kmn, pk0[r]);
+      kmx = max(kmx, pk1[r]);
+    }
   }
   // Bins by value when the scores' range is finite, else by key.
   RangeBins bin_of;
@@ -330,10 +355,14 @@ __global__ void __cluster_dims__(kClusterTopk, 1, 1) __launch_bounds__(kTopkThre
   for (int i = tid; i < cn; i += NT) atomicAdd(&hist[bin_of(keys[i])], 1u);
   cluster.sync();  // (2)
   for (int b0 = tid * 4; b0 < kRangeBins; b0 += 4 * NT) {
+    uint4 h[kClusterTopk];
+#pragma unroll
+    for (int r = 0; r < kClusterTopk; ++r)
+      h[r] = *reinterpret_cast<const uint4*>(cluster.map_shared_rank(hist, r) + b0);
     uint4 t = make_uint4(0, 0, 0, 0);
+#pragma unroll
     for (int r = 0; r < kClusterTopk; ++r) {
-      const uint4 h = *reinterpret_cast<const uint4*>(cluster.map_shared_rank(hist, r) + b0);
-      t.x += h.x; t.y += h.y; t.z += h.z; t.w += h.w;
+      t.x += h[r].x; t.y += h[r].y; t.z += h[r].z; t.w += h[r].w;
     }
     *reinterpret_cast<uint4*>(ghist + b0) = t;
   }
@@ -353,25 +382,37 @@ __global__ void __cluster_dims__(kClusterTopk, 1, 1) __launch_bounds__(kTopkThre
   cluster.sync();  // (3)
   int nc = 0;
   bool fits = true;
+  int crs[kClusterTopk];  // the ranks' b1 counts
+#pragma unroll
+  for (int r = 0; r < kClusterTopk; ++r) crs[r] = *cluster.map_shared_rank(&lcount, r);
+#pragma unroll
   for (int r = 0; r < kClusterTopk; ++r) {
-    const int cr = *cluster.map_shared_rank(&lcount, r);
-    fits &= cr <= kCandCta;
-    nc += cr;
+    fits &= crs[r] <= kCandCta;
+    nc += crs[r];
   }
   fits &= nc <= kCandMax;
 
   uint32_t T;  // the k-th largest key; krem of the keys equal to T are taken
   if (fits) {
-    int off = 0;
+    // one key per thread and rank at most (kCandCta == NT): the ranks' reads
+    // are issued together
+    uint32_t kv[kClusterTopk];
+    int pv[kClusterTopk];
+#pragma unroll
     for (int r = 0; r < kClusterTopk; ++r) {
-      const int cr = *cluster.map_shared_rank(&lcount, r);
-      const uint32_t* pk = cluster.map_shared_rank(lkey, r);
-      const int* pp = cluster.map_shared_rank(lpos, r);
-      for (int c = tid; c < cr; c += NT) {
-        ckey[off + c] = pk[c];
-        cpos[off + c] = pp[c];
+      if (tid < crs[r]) {
+        kv[r] = cluster.map_shared_rank(lkey, r)[tid];
+        pv[r] = cluster.map_shared_rank(lpos, r)[tid];
       }
-      off += cr;
+    }
+    int off = 0;
+#pragma unroll
+    for (int r = 0; r < kClusterTopk; ++r) {
+      if (tid < crs[r]) {
+        ckey[off + tid] = kv[r];
+        cpos[off + tid] = pv[r];
+      }
+      off += crs[r];
     }
     __syncthreads();
     for (int c = tid; c < nc; c += NT) {
@@ -413,8 +454,12 @@ __global__ void __cluster_dims__(kClusterTopk, 1, 1) __launch_bounds__(kTopkThre
       }
       cluster.sync();
       {
+        uint32_t hr[kClusterTopk];
+#pragma unroll
+        for (int r = 0; r < kClusterTopk; ++r) hr[r] = cluster.map_shared_rank(hist, r)[tid];
         uint32_t t = 0;
-        for (int r = 0; r < kClusterTopk; ++r) t += cluster.map_shared_rank(hist, r)[tid];
+#pragma unroll
+        for (int r = 0; r < kClusterTopk; ++r) t += hr[r];
         whist[tid] = t;
       }
       __syncthreads();
@@ -454,10 +499,23 @@ __global__ void __cluster_dims__(kClusterTopk, 1, 1) __launch_bounds__(kTopkThre
   }
   cluster.sync();  // (4)
   int pos = 0, eqb = 0;
-  for (int r = 0; r < rank; ++r) {
-    const int* o = cluster.map_shared_rank(tot, r);
-    pos += o[0] + min(o[1], max(0, (int)krem - eqb));
-    eqb += o[1];
+  {
+    int t0[kClusterTopk], t1[kClusterTopk];
+#pragma unroll
+    for (int r = 0; r < kClusterTopk; ++r) {
+      if (r < rank) {
+        const int* o = cluster.map_shared_rank(tot, r);
+        t0[r] = o[0];
+        t1[r] = o[1];
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kClusterTopk; ++r) {
+      if (r < rank) {
+        pos += t0[r] + min(t1[r], max(0, (int)krem - eqb));
+        eqb += t1[r];
+      }
+    }
   }
   for (int w = 0; w < warp; ++w) {
     pos += wgt[w] + min(weq[w], max(0, (int)krem - eqb));
@@ -509,6 +567,37 @@ __global__ void __launch_bounds__(kTopkThreads, 4) k_topk_small(const float* __r
     keys[i] = key_of(f);
   }
   if (__syncthreads_or(nan_seen) && tid == 0) flag(st, DV_DEV_NONFINITE);
+
+  if (N <= 2 * kTopkThreads) {
+    // Short rows: the rank of each key (greater keys, then equal keys at lower
+    // positions) by one pass over the row; it is taken when its rank is below
+    // k. The taken positions come out ascending through two block scans
+    // (positions tid, then kTopkThreads + tid).
+    bool take[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = h * kTopkThreads + tid;
+      take[h] = false;
+      if (i < N) {
+        const uint32_t ki = keys[i];
+        int r = 0;
+        for (int j = 0; j < N; ++j) {
+          const uint32_t kj = keys[j];
+          r += (kj > ki) || (kj == ki && j < i);
+        }
+        take[h] = r < k;
+      }
+    }
+    int base = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int tot;
+      const int before = block_exscan(take[h] ? 1 : 0, tmp, &tot);
+      if (take[h]) out[base + before] = h * kTopkThreads + tid;
+      base += tot;
+    }
+    return;
+  }
 
   uint32_t prefix = 0, mask = 0, krem = (uint32_t)k;
   for (int pass = 0; pass < 4; ++pass) {
