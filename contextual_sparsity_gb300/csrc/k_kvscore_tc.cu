@@ -181,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q = warp & 3, mt = warp >> 2;
       const int qi = mt * 128 + q * 32 + lane;
       const int lim = qi < p.NQ ? p.n - p.W + qi % p.W : -1;  // last admitted key
+      const float s2 = p.scale2;
       float m = -INFINITY, l = 0.f;
       for (int i = 0; i < ntiles; ++i) {
         const int a = i & 1;
@@ -192,29 +193,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int key0 = (t0 + i) * kTcKeys;
         const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + a * (p.MT * 128) + mt * 128;
-#pragma unroll 1
-        for (int c = 0; c < kTcKeys / 32; ++c) {
-          float v[32];
-          tmem_ld32(ta + c * 32, v);
-          const int kc = key0 + c * 32;
-          float cm = -INFINITY;
+        // the tile's 128 scores of this query, four loads in flight
+        uint32_t r[kTcKeys];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            v[j] = (kc + j <= lim) ? v[j] * p.scale2 : -INFINITY;
-            cm = fmaxf(cm, v[j]);
-          }
-          if (cm > m) {
-            l *= exp2f(m - cm);
-            m = cm;
-          }
-          if (m != -INFINITY) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) l += exp2f(v[j] - m);
-          }
-        }
+        for (int c = 0; c < kTcKeys / 32; ++c) tmem_ld32_nw(ta + c * 32, r + c * 32);
+        tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acce[a]);
+        float v[kTcKeys];
+#pragma unroll
+        for (int j = 0; j < kTcKeys; ++j) v[j] = __uint_as_float(r[j]);
+        if (key0 + kTcKeys - 1 > p.n - p.W) {  // the causal limit cuts this tile for some query
+#pragma unroll
+          for (int j = 0; j < kTcKeys; ++j)
+            if (key0 + j > lim) v[j] = -INFINITY;
+        }
+        float mx = v[0];
+#pragma unroll
+        for (int j = 1; j < kTcKeys; ++j) mx = fmaxf(mx, v[j]);
+        mx *= s2;  // scale > 0: the max of the scaled scores
+        if (mx > m) {
+          l *= ex2_approx(m - mx);
+          m = mx;
+        }
+        if (m != -INFINITY) {
+          float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+          for (int j = 0; j < kTcKeys; j += 2) {
+            acc0 += ex2_approx(fmaf(v[j], s2, -m));
+            acc1 += ex2_approx(fmaf(v[j + 1], s2, -m));
+          }
+          l += acc0 + acc1;
+        }
       }
       if (qi < p.NQ) {
         float* dst = p.stats + (((size_t)u * p.NQ + qi) * p.nsplit + split) * 2;
@@ -252,20 +263,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const bool nomask = key0 + kTcKeys - 1 <= p.n - p.W;  // every query admits every key
         const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + a * p.NQ + half * cols;
+        const float s2 = p.scale2;
+        float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < cols / 32; ++c) {
-          float v[32];
-          tmem_ld32(ta + c * 32, v);
-          const int qb = half * cols + c * 32;
-          if (nomask) {
+        for (int c = 0; c < cols / 32; c += 2) {  // two 32-column loads in flight (one at an odd end)
+          uint32_t r[64];
+          const int nc = (c + 1 < cols / 32) ? 2 : 1;
+          tmem_ld32_nw(ta + c * 32, r);
+          if (nc == 2) tmem_ld32_nw(ta + c * 32 + 32, r + 32);
+          tmem_wait_ld();
+          for (int h = 0; h < nc; ++h) {
+            const int qb = half * cols + (c + h) * 32;
+            const float4* cs = reinterpret_cast<const float4*>(cst + qb);
+            if (nomask) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) sum += exp2f(fmaf(v[j], p.scale2, cst[qb + j]));
-          } else {
+              for (int j4 = 0; j4 < 8; ++j4) {
+                const float4 cc = cs[j4];
+                acc0 += ex2_approx(fmaf(__uint_as_float(r[h * 32 + 4 * j4]), s2, cc.x));
+                acc1 += ex2_approx(fmaf(__uint_as_float(r[h * 32 + 4 * j4 + 1]), s2, cc.y));
+                acc0 += ex2_approx(fmaf(__uint_as_float(r[h * 32 + 4 * j4 + 2]), s2, cc.z));
+                acc1 += ex2_approx(fmaf(__uint_as_float(r[h * 32 + 4 * j4 + 3]), s2, cc.w));
+              }
+            } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (key <= lims[qb + j]) sum += exp2f(fmaf(v[j], p.scale2, cst[qb + j]));
+              for (int j = 0; j < 32; ++j)
+                if (key <= lims[qb + j])
+                  acc0 += ex2_approx(fmaf(__uint_as_float(r[h * 32 + j]), s2, cst[qb + j]));
+            }
           }
         }
+        sum = acc0 + acc1;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acce[a]);
