@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--skip-inactive", action="store_true",
+                    help="MLP streams fc2T rows only for neurons whose activation is above zero")
     ap.add_argument("--tuning", default=None,
                     help="main,side,main_ring_kb,side_ring_kb,attn,pdl,stage_kb (see dv_set_tuning)")
     ap.add_argument("--timeline", type=int, default=0,
@@ -219,7 +221,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 class Model:
     def __init__(self, w, device, lookahead=True, seed=0, kv_dense=False, kept_inputs=False,
-                 fill=False, extra_slots=0, w4=False):
+                 fill=False, extra_slots=0, w4=False, skip_inactive=False):
         self.w = w
         self.L = w.layers
         self.n = w.n
@@ -304,6 +306,8 @@ class Model:
         self.evj = dv.event()
         self.st = torch.zeros(1, dtype=torch.int32, device=device)
         flags = (dv.DV_LOOKAHEAD if lookahead else 0) | self.kv_flags
+        if skip_inactive:
+            flags |= dv.DV_SKIP_INACTIVE
         if w4:
             flags |= dv.DV_W4
         if fill:
@@ -484,7 +488,7 @@ def run_ours(a):
         dv.set_tuning(*[int(x) for x in a.tuning.split(",")])
     w = workload(a)
     lookahead = not a.sync
-    m = Model(w, dev, lookahead=lookahead, kv_dense=a.kv_dense)
+    m = Model(w, dev, lookahead=lookahead, kv_dense=a.kv_dense, skip_inactive=a.skip_inactive)
     stream = torch.cuda.Stream(device=dev)
     g, per_step = m.capture(stream)
     torch.cuda.synchronize()
@@ -524,6 +528,22 @@ def run_ours(a):
         uH = sum(x[1] for x in c) / 2 if w.keep_H < 1 else w.h_kv
         union = (uN, uH)
     sel, pred = traffic.layer_bytes(w, keys=m.keys, union=union)
+    skip = None
+    if a.skip_inactive:
+        # the fc2T rows the MLP streamed (selected neurons with a positive
+        # activation), counted on the device over one replay of the step
+        cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+        dv.count_active(cnt)
+        gc, _ = m.capture(stream, warm=False)
+        dv.count_active(None)
+        gc.replay()
+        torch.cuda.synchronize()
+        active = cnt.item() / w.layers / w.B
+        kN_rows = union[0] if union else m.kN
+        read = sel - (kN_rows - active) * w.d * 2
+        skip = {"active_rows_per_layer": round(active, 1), "selected_rows_per_layer": kN_rows,
+                "read_bytes_per_layer": round(read),
+                "gbs_read": round(read / (median_ms_step * 1e3 / w.layers / wsz * 1e-6) / 1e9, 1)}
     # the headline: the median over the repeats (each of steps/REPEATS steps)
     job = job_figures(median_ms_step * a.steps, a.steps, w.layers, wsz, sel, pred)
     mean_us_layer = ms_total * 1e3 / a.steps / w.layers / wsz
@@ -660,6 +680,7 @@ def run_ours(a):
         "frac_of_measured_hbm_selected": round(gbs_sel / (wsz * peak), 4),
         "us_layer_per_replica": round(us_layer, 2),
         "layers_per_s_total": round(job["layers_per_s"], 1),
+        "skip_inactive": skip,
         "roofline": roof, "kernel_us": kernel_us, "kernel_launches_per_step": kernel_launches,
         "gpu_launches": per_step * a.steps, "launches_per_step": per_step,
         "clocks": clk.summary(), "e2e": e2e, "cpu_baseline": cpu,

@@ -22,6 +22,7 @@ struct Tuning {
   int attn_ctas = 0;        // split-K CTA target; 0: 4 per SM
 };
 static Tuning g_tune;
+int* g_count_active = nullptr;
 
 int sm_count() {
   static int cached = 0;
@@ -376,6 +377,11 @@ int dv_profile(cudaEvent_t* events, int* tags, int cap) {
 }
 
 long long dv_launch_count(void) { return g_launches; }
+
+int dv_count_active(int* dev_counter) {
+  g_count_active = dev_counter;
+  return DV_OK;
+}
 
 // Tuning knobs for launch shapes (aux; defaults need no call).
 int dv_set_tuning(int main_ctas, int side_ctas, int main_ring_kb, int side_ring_kb,

@@ -111,6 +111,7 @@ int launch_union(const int32_t* idx, int B, int k, int N, int32_t* out, int32_t*
                  cudaStream_t stream);
 
 extern int g_stage_target;  // bytes per weight-stream ring stage
+extern int* g_count_active; // dv_count_active: device counter of streamed fc2^T rows
 
 // Device properties (cached).
 int sm_count();

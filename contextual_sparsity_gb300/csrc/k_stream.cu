@@ -148,6 +148,9 @@ struct StreamParams {
   // partial outputs
   float* part;            // [gridDim][B][d]
   int* st;
+  // MLP with DV_SKIP_INACTIVE: each CTA adds the fc2^T rows it streams here
+  // (dv_count_active; NULL: not counted)
+  int* active_cnt;
 };
 
 // Number of selected entries this launch processes.
@@ -754,6 +757,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         }
         *list_count = c;
         mbar_arrive(act_ready);
+        if (p.active_cnt) atomicAdd(p.active_cnt, c);
       }
     }
     consumer_sync(T);
@@ -1144,6 +1148,7 @@ int launch_mlp(const uint16_t* x, int B, int d, int F, const uint16_t* ln_g, con
   p.d = d; p.B = B; p.x = x; p.ln_g = ln_g; p.ln_b = ln_b; p.eps = eps;
   p.W0 = fc1; p.W1 = fc2T; p.bias0 = b1; p.idx = idx; p.k = k; p.dev_count = dev_count;
   p.n_rows_total = F; p.flags = flags; p.part = part; p.st = st;
+  p.active_cnt = (flags & DV_SKIP_INACTIVE) ? g_count_active : nullptr;
   int grid = 0;
   int rc = launch_stream(KIND_MLP, p, k, target_ctas, ring_budget, stream, &grid, pdl);
   if (rc != DV_OK) return rc;

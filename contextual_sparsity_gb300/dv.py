@@ -150,7 +150,8 @@ EXPORTED = ["dv_version", "dv_status_string", "dv_workspace_size", "dv_set_tunin
             "dv_select_topk", "dv_sparse_mlp", "dv_sparse_attn", "dv_kv_select_attn",
             "dv_decode_layer", "dv_decode_step", "dv_sparse_mlp_noalloc", "dv_plan_bytes",
             "dv_cost_calibrate", "dv_plan_decode", "dv_plan_crossing", "dv_w4_row_bytes",
-            "dv_quantize_w4", "dv_sparse_mlp_w4", "dv_union_mlp_ws_size", "dv_union_mlp"]
+            "dv_quantize_w4", "dv_sparse_mlp_w4", "dv_union_mlp_ws_size", "dv_union_mlp",
+            "dv_count_active"]
 
 
 def status_string(code: int) -> str:
@@ -392,6 +393,13 @@ class Profiler:
         """[(tag name, ms)] of the recorded launches (call after synchronising)."""
         return [(TAGS.get(self._tags[i], str(self._tags[i])),
                  self.events[2 * i].elapsed_time(self.events[2 * i + 1])) for i in range(self.n)]
+
+
+def count_active(counter=None):
+    """MLP launches with DV_SKIP_INACTIVE add their streamed fc2T rows to the
+    device int `counter` from now on (None stops; dv_count_active)."""
+    lib().dv_count_active.argtypes = [_p]
+    lib().dv_count_active(ptr(counter))
 
 
 def launch_count() -> int:

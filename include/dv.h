@@ -192,6 +192,13 @@ int dv_set_tuning(int main_ctas, int side_ctas, int main_ring_kb, int side_ring_
 int dv_profile(cudaEvent_t* events, int* tags, int cap);
 long long dv_launch_count(void);
 
+/* Bytes actually read with DV_SKIP_INACTIVE (aux, process-wide): from now on
+ * every MLP launch with DV_SKIP_INACTIVE adds to *dev_counter (a device int,
+ * atomically; works inside stream capture, where the pointer is baked into
+ * the launch) the number of fc2T rows it streamed, i.e. the selected neurons
+ * whose activation is above zero. dv_count_active(NULL) stops. Always DV_OK. */
+int dv_count_active(int* dev_counter);
+
 /* ---- a2: predictor ([DV] §4.1 "Design", §4.2 "Approach") ------------------
  * scores[b][i] = sum_j act(sum_c y[b][c] P1[j][c]) * P2[i][j] for i < N,
  * act = identity, or ReLU with DV_PRED_RELU. y [B][d] fp16 is the layer input

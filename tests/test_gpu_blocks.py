@@ -143,6 +143,36 @@ def test_mlp_parity(wl, d, F, keep, flags):
     assert rel_err(npf(out[0]), y_ref) < TOL
 
 
+@pytest.mark.parametrize("wl,d,F,keep", [("tiny", None, None, 0.25), ("opt-175b", 12288, 4096, 0.5)])
+def test_mlp_skip_inactive_counts_active_rows(wl, d, F, keep):
+    # with DV_SKIP_INACTIVE the MLP streams the fc2T rows of the selected
+    # neurons whose activation is above zero (Eq. 1: a ReLU zero adds nothing);
+    # dv_count_active counts them: the oracle's positive activations, up to
+    # activations the fp32 and fp64 sums could put on either side of zero
+    w, W = _mlp_case(wl, d, F)
+    x = synth.hidden(w, B=1, seed=11, name="h")
+    k = oracle.k_from_keep(keep, w.F)
+    idx = np.sort(np.random.default_rng(1).choice(w.F, k, replace=False)).astype(np.int32)
+    D = _dims(w, 8)
+    ws = dv.workspace(D)
+    out = torch.empty(1, w.d, dtype=torch.float16, device="cuda")
+    cnt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dv.count_active(cnt)
+    try:
+        dv.sparse_mlp(x.cuda(), D, to_dev(W), torch.from_numpy(idx).cuda(), k, out, ws,
+                      flags=dv.DV_SKIP_INACTIVE | dv.DV_NO_RESIDUAL)
+        torch.cuda.synchronize()
+    finally:
+        dv.count_active(None)
+    Wh = host(W)
+    ref, act = oracle.mlp_gather(np16(x[0]), Wh["fc1"], Wh["b1"], Wh["fc2T"], Wh["b2"], idx,
+                                 ln_g=Wh["ln2_g"], ln_b=Wh["ln2_b"], return_act=True)
+    assert rel_err(npf(out[0]), ref) < TOL
+    near = int(np.sum(np.abs(act) < 1e-4 * max(1.0, np.abs(act).max())))
+    assert abs(cnt.item() - int(np.sum(act > 0))) <= near
+    assert 0 < cnt.item() < k
+
+
 def test_mlp_k1_and_masked_form():
     w, W = _mlp_case("tiny")
     x = synth.hidden(w, B=1, seed=5)
