@@ -190,7 +190,9 @@ static int attn_qkv(const uint16_t* x, int B, const dv_dims* D, const dv_layer_w
     // (the QKV launch below then clears their marks).
     int rc = launch_kv_fill(kv->y_side, kv->kv_missing, B, D->d, D->h_kv, D->d_h, w->ln1_g,
                             w->ln1_b, D->ln_eps, w->Wk, w->bk, w->Wv, w->bv, sel, k, dev_count,
-                            kv->K, kv->V, n, D->n_max, st, s, pdl);
+                            kv->K, kv->V, n, D->n_max, st, s, pdl, ret ? kv->Kr : nullptr,
+                            ret ? kv->Vr : nullptr, kv->kept_count, kv->b_max,
+                            (flags & DV_W4) != 0);
     if (rc != DV_OK) return rc;
     pdl = true;  // the fill waited for the index list before letting QKV start
   }
@@ -305,7 +307,6 @@ int check_weights_mlp(const dv_layer_weights* w) {
 static int check_w4(const dv_dims* D, int flags) {
   if (!(flags & DV_W4)) return DV_OK;
   REQ(D->d % 128 == 0, DV_ERR_DIMS);
-  REQ(!(flags & DV_KV_FILL), DV_ERR_UNSUPPORTED);  // the recompute reads fp16 W^K, W^V
   return DV_OK;
 }
 
@@ -317,7 +318,7 @@ static int check_kv(const dv_dims* D, const dv_kv_cache* kv, int B, int n, int f
   if (flags & DV_KV_FILL) {
     REQ_PTR(kv->y_side);
     REQ(kv->kv_missing, DV_ERR_NULL);
-    REQ(!(flags & (DV_KV_RETAINED | DV_KV_RESELECT)), DV_ERR_UNSUPPORTED);
+    REQ(!(flags & DV_KV_RESELECT), DV_ERR_UNSUPPORTED);
   }
   if (flags & (DV_KV_RETAINED | DV_KV_RESELECT)) {
     REQ(B == 1, DV_ERR_UNSUPPORTED);
@@ -667,10 +668,13 @@ static int decode_layer(const dv_dims* dims, const dv_keep* keep, int B, const d
       // beside this layer's streaming CTAs).
       const int32_t* selHn = hd ? nullptr : (B == 1 ? next->idx_H : next->uH);
       const int32_t* cntHn = (hd || B == 1) ? nullptr : next->ucnt + 1;
+      const bool retn = (flags & DV_KV_RETAINED) != 0;
       rc = launch_kv_fill(kv_next->y_side, kv_next->kv_missing, B, dims->d, dims->h_kv,
                           dims->d_h, w_next->ln1_g, w_next->ln1_b, dims->ln_eps, w_next->Wk,
                           w_next->bk, w_next->Wv, w_next->bv, selHn, kHe, cntHn, kv_next->K,
-                          kv_next->V, n, dims->n_max, dev_status, side, false);
+                          kv_next->V, n, dims->n_max, dev_status, side, false,
+                          retn ? kv_next->Kr : nullptr, retn ? kv_next->Vr : nullptr,
+                          kv_next->kept_count, kv_next->b_max, (flags & DV_W4) != 0);
       if (rc != DV_OK) return rc;
       if (side_filled) *side_filled = true;
     }

@@ -43,7 +43,8 @@ int launch_kv_fill(const uint16_t* y_side, const uint32_t* missing, int B, int d
                    const uint16_t* Wk, const uint16_t* bk, const uint16_t* Wv,
                    const uint16_t* bv, const int32_t* idx, int k, const int32_t* dev_count,
                    uint16_t* K, uint16_t* V, int n, int n_max, int* st, cudaStream_t stream,
-                   bool pdl);
+                   bool pdl, uint16_t* Kr = nullptr, uint16_t* Vr = nullptr,
+                   const int32_t* kept_count = nullptr, int b_max = 0, bool w4 = false);
 
 int launch_wo(const uint16_t* x, int B, int d, int G, int dh, int h_kv, const uint16_t* WoT,
               const uint16_t* bo, const int32_t* idx, int k, const int32_t* dev_count,

@@ -36,12 +36,30 @@ struct FillParams {
   const int32_t* dev_count;
   int k, h_kv, dh, d, n, n_max;
   uint16_t *K, *V;           // [B][h_kv][n_max][dh]
+  // The retained buffer (batch 1, nullable): the tokens decoded since the
+  // selection sit after the kept rows, position t at slot
+  // kept_count[u] - (n - t), and get the recomputed rows too.
+  uint16_t *Kr, *Vr;         // [h_kv][b_max][dh]
+  const int32_t* kept_count;
+  int b_max;
   int* st;
 };
 
 // 12 warps and 2 d bytes of shared memory per token slot (48 KB at d = 12288):
 // on the side stream a CTA runs beside the Wo / MLP streaming CTAs where their
 // registers leave room (measured faster than 8 warps of <= 64 registers).
+// 4-bit rows (DV_W4): a packed row holds d/2 bytes of codes (column 2i in the
+// low nibble of byte i, stored as q + 8), then the d/128 fp16 group scales,
+// padded to 16 bytes; a weight is q s, exact in fp32.
+__host__ __device__ inline size_t fill_w4_row_bytes(int d) { return (size_t)((d / 2 + d / 64 + 15) / 16 * 16); }
+
+// Eight codes of a 32-bit word as exact floats q in column order.
+DV_DEV void fill_w4_decode(uint32_t w, float* f) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) f[k] = (float)((int)((w >> (4 * k)) & 15u) - 8);
+}
+
+template <bool W4>
 __global__ void __launch_bounds__(kFillThreads, 2) k_kv_fill(const FillParams p) {
   extern __shared__ __align__(16) uint16_t zs[];  // [kFillTok][d]: LN1 of the pass's tokens
   __shared__ float red[kFillThreads / 32][kFillTok];
@@ -85,8 +103,9 @@ __global__ void __launch_bounds__(kFillThreads, 2) k_kv_fill(const FillParams p)
 
   const int d = p.d, nvec = d >> 3;
   // This warp's rows of the unit's [W^K; W^V] (2 dh rows).
-  const uint16_t* wrow[kFillRowsW];
+  const uint8_t* wrow[kFillRowsW];
   int rrow[kFillRowsW];
+  const size_t rbytes = W4 ? fill_w4_row_bytes(d) : (size_t)d * 2;
 #pragma unroll
   for (int r = 0; r < kFillRowsW; ++r) {
     int row = rb * kFillRows + warp * kFillRowsW + r;
@@ -94,7 +113,7 @@ __global__ void __launch_bounds__(kFillThreads, 2) k_kv_fill(const FillParams p)
     if (row >= 2 * p.dh) row = 0;  // (no such row: computed, never stored)
     const bool isk = row < p.dh;
     const int c = isk ? row : row - p.dh;
-    wrow[r] = (isk ? p.Wk : p.Wv) + ((size_t)u * p.dh + c) * d;
+    wrow[r] = reinterpret_cast<const uint8_t*>(isk ? p.Wk : p.Wv) + ((size_t)u * p.dh + c) * rbytes;
   }
 
   // Passes of kFillTok tokens; the kFillGroups CTAs of a row block take
@@ -167,6 +186,47 @@ __global__ void __launch_bounds__(kFillThreads, 2) k_kv_fill(const FillParams p)
     for (int r = 0; r < kFillRowsW; ++r)
 #pragma unroll
       for (int j = 0; j < kFillTok; ++j) acc[r][j] = 0.f;
+    if constexpr (W4) {
+      // The fp16 loop's shape over 8-column vectors: one 32-bit word of codes
+      // per vector (byte offset 4 v), its group's scale (group v / 16).
+      for (int v0 = lane; v0 < nvec; v0 += 32 * kFillUnroll) {
+        uint32_t wc[kFillUnroll][kFillRowsW];
+        float sc[kFillUnroll][kFillRowsW];
+#pragma unroll
+        for (int q = 0; q < kFillUnroll; ++q) {
+          const int v = v0 + q * 32;
+#pragma unroll
+          for (int r = 0; r < kFillRowsW; ++r) {
+            const bool on = v < nvec;
+            wc[q][r] = on ? __ldg(reinterpret_cast<const unsigned int*>(wrow[r]) + v) : 0u;
+            sc[q][r] = on ? __half2float(__ldg(reinterpret_cast<const __half*>(wrow[r] + d / 2) + (v >> 4)))
+                          : 0.f;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kFillUnroll; ++q) {
+          const int v = v0 + q * 32;
+          if (v >= nvec) break;
+          float wf[kFillRowsW][8];
+#pragma unroll
+          for (int r = 0; r < kFillRowsW; ++r) {
+            fill_w4_decode(wc[q][r], wf[r]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) wf[r][i] *= sc[q][r];
+          }
+#pragma unroll
+          for (int j = 0; j < kFillTok; ++j) {
+            if (j >= nt) break;
+            float z[8];
+            h8_to_f8(*reinterpret_cast<const uint4*>(zs + (size_t)j * d + v * 8), z);
+#pragma unroll
+            for (int r = 0; r < kFillRowsW; ++r)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) acc[r][j] = fmaf(z[i], wf[r][i], acc[r][j]);
+          }
+        }
+      }
+    } else
     for (int v0 = lane; v0 < nvec; v0 += 32 * kFillUnroll) {
       uint4 w[kFillUnroll][kFillRowsW];
 #pragma unroll
@@ -174,7 +234,7 @@ __global__ void __launch_bounds__(kFillThreads, 2) k_kv_fill(const FillParams p)
         const int v = v0 + q * 32;
 #pragma unroll
         for (int r = 0; r < kFillRowsW; ++r)
-          w[q][r] = v < nvec ? ld_nc_v4(wrow[r] + v * 8) : make_uint4(0, 0, 0, 0);
+          w[q][r] = v < nvec ? ld_nc_v4(wrow[r] + (size_t)v * 16) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int q = 0; q < kFillUnroll; ++q) {
@@ -195,6 +255,9 @@ __global__ void __launch_bounds__(kFillThreads, 2) k_kv_fill(const FillParams p)
         }
       }
     }
+    // Lanes leave the loops above after different trip counts; the warp
+    // reconverges here before the shuffles sum the partials.
+    __syncwarp();
 #pragma unroll
     for (int r = 0; r < kFillRowsW; ++r)
 #pragma unroll
@@ -208,8 +271,16 @@ __global__ void __launch_bounds__(kFillThreads, 2) k_kv_fill(const FillParams p)
         const uint16_t* bias = isk ? p.bk : p.bv;
         const float bv = bias ? h2f(bias[u * p.dh + c]) : 0.f;
         uint16_t* cache = isk ? p.K : p.V;
-        for (int j = 0; j < nt; ++j)
-          cache[(((size_t)b * p.h_kv + u) * p.n_max + t0 + j) * p.dh + c] = f2h(acc[r][j] + bv);
+        uint16_t* kept = isk ? p.Kr : p.Vr;
+        const int kc = kept ? p.kept_count[u] : 0;
+        for (int j = 0; j < nt; ++j) {
+          const uint16_t val = f2h(acc[r][j] + bv);
+          cache[(((size_t)b * p.h_kv + u) * p.n_max + t0 + j) * p.dh + c] = val;
+          if (kept) {
+            const int slot = kc - (p.n - (t0 + j));
+            if (slot >= 0 && slot < p.b_max) kept[((size_t)u * p.b_max + slot) * p.dh + c] = val;
+          }
+        }
       }
     }
     __syncthreads();  // the next pass overwrites zs
@@ -221,21 +292,25 @@ int launch_kv_fill(const uint16_t* y_side, const uint32_t* missing, int B, int d
                    const uint16_t* Wk, const uint16_t* bk, const uint16_t* Wv,
                    const uint16_t* bv, const int32_t* idx, int k, const int32_t* dev_count,
                    uint16_t* K, uint16_t* V, int n, int n_max, int* st, cudaStream_t stream,
-                   bool pdl) {
+                   bool pdl, uint16_t* Kr, uint16_t* Vr, const int32_t* kept_count, int b_max,
+                   bool w4) {
   FillParams p{};
+  p.Kr = Kr; p.Vr = Vr; p.kept_count = kept_count; p.b_max = b_max;
   p.y_side = y_side; p.missing = missing; p.ln_g = ln_g; p.ln_b = ln_b; p.eps = eps;
   p.Wk = Wk; p.bk = bk; p.Wv = Wv; p.bv = bv; p.idx = idx; p.dev_count = dev_count;
   p.k = k; p.h_kv = h_kv; p.dh = dh; p.d = d; p.n = n; p.n_max = n_max; p.K = K; p.V = V;
   p.st = st;
   const size_t smem = (size_t)kFillTok * d * sizeof(uint16_t);
-  if (cudaFuncSetAttribute((const void*)k_kv_fill, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+  const void* fn = w4 ? (const void*)k_kv_fill<true> : (const void*)k_kv_fill<false>;
+  if (w4 && d % 128 != 0) return DV_ERR_DIMS;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
     return DV_ERR_LAUNCH;
   dim3 grid((2 * dh + kFillRows - 1) / kFillRows, k, B * kFillGroups);
   void* args[] = {&p};
   note_launch(DV_TAG_KVFILL, 0, stream);
   const cudaError_t e =
-      launch_k((const void*)k_kv_fill, grid, dim3(kFillThreads), smem, stream, args, pdl);
+      launch_k(fn, grid, dim3(kFillThreads), smem, stream, args, pdl);
   note_launch(DV_TAG_KVFILL, 1, stream);
   return e == cudaSuccess ? DV_OK : DV_ERR_LAUNCH;
 }

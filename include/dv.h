@@ -83,8 +83,8 @@ extern "C" {
                                       selected units from y_side ([DV] §4.2) */
 #define DV_W4 (1u << 11)           /* the layer's Wq, Wk, Wv, WoT, fc1, fc2T point to packed
                                       4-bit rows (dv_quantize_w4; [DV] §5.2, Table 7
-                                      W4A16); P1, P2 stay fp16; d % 128 == 0; not with
-                                      DV_KV_FILL */
+                                      W4A16); P1, P2 stay fp16; d % 128 == 0; with
+                                      DV_KV_FILL the recompute reads the 4-bit W^K, W^V */
 
 /* ---- shapes ------------------------------------------------------------ */
 typedef struct {
@@ -303,15 +303,18 @@ int dv_sparse_mlp_w4(const uint16_t* x, int B, const dv_dims* dims, const dv_lay
  * out[b] = x[b] + sum_{query heads j of selected units} H_j WoT_j + bo.
  * Unselected units get no k, v at slot n: their kv_missing bit is set and
  * y_side[b][n] = x[b] (when those pointers are given).
- * With DV_KV_FILL (y_side and kv_missing required; not with DV_KV_RETAINED or
- * DV_KV_RESELECT): before the step reads the cache, every selected unit u
+ * With DV_KV_FILL (y_side and kv_missing required; not with DV_KV_RESELECT):
+ * before the step reads the cache, every selected unit u
  * gets, for each position t < n whose kv_missing bit of u is set, k and v
  * recomputed from the kept input: z = LN1(y_side[b][t]), K[b][u][t] =
  * fp16(z W^K_u^T + bk_u), V likewise ([DV] §4.2: load the stored embeddings
  * and compute the missing keys and values); the bits are then cleared. A
  * unit's set bits must form a suffix t0..n-1 of the positions, which holds
  * when every step since the cache was complete ran with DV_KV_FILL (a step
- * that selects a unit fills all of its holes).
+ * that selects a unit fills all of its holes). With DV_KV_RETAINED as well, a
+ * recomputed position t at or after the selection's context also goes to its
+ * retained slot kept_count[u] - (n - t) (every step since the selection ran
+ * with DV_KV_ADVANCE, so the decoded tokens follow the kept rows in order).
  * With DV_KV_RETAINED (batch 1): the new k, v also go to Kr/Vr[u][kept_count[u]]
  * and attention reads Kr/Vr[u][0..kept_count[u]] instead of the cache; with
  * DV_KV_ADVANCE the kept counts then grow by one.

@@ -120,9 +120,10 @@ def test_attention_and_layer_validation(L):
     assert a(*args(flags=dv.DV_KV_RETAINED)) == dv.DV_ERR_NULL   # no retained buffers
     assert a(*args(flags=dv.DV_KV_FILL)) == dv.DV_ERR_NULL       # no kept inputs / marks
     kv_f = dv.KvCache(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64)
-    assert a(*args(flags=dv.DV_KV_FILL | dv.DV_KV_RETAINED, kvp=kv_f)) == dv.DV_ERR_UNSUPPORTED
+    assert a(*args(flags=dv.DV_KV_FILL | dv.DV_KV_RESELECT, kvp=kv_f)) == dv.DV_ERR_UNSUPPORTED
+    assert a(*args(flags=dv.DV_KV_FILL | dv.DV_KV_RETAINED, kvp=kv_f)) == dv.DV_ERR_WORKSPACE
     assert a(*args(flags=dv.DV_KV_FILL, kvp=kv_f)) == dv.DV_ERR_WORKSPACE
-    assert a(*args(flags=dv.DV_W4 | dv.DV_KV_FILL, kvp=kv_f)) == dv.DV_ERR_UNSUPPORTED
+    assert a(*args(flags=dv.DV_W4 | dv.DV_KV_FILL, kvp=kv_f)) == dv.DV_ERR_WORKSPACE
     assert a(*args(flags=dv.DV_W4)) == dv.DV_ERR_WORKSPACE           # d 256: a multiple of 128
     D264 = _dims(d=264)
     assert a(FAKE, 1, ctypes.byref(D264), ctypes.byref(w), FAKE, 2, None, ctypes.byref(kv), 10,

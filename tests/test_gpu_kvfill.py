@@ -160,3 +160,84 @@ def test_multistep_missing_kv_batch4_union():
             if last >= 0:
                 rows = list(range(n0 + last + 1))
                 assert rel_err(Kg[u, rows].astype(float), Kf[u, rows].astype(float)) < TOL, (b, u)
+
+
+def test_multistep_missing_kv_with_retained_buffer():
+    # composition ("Where Activation Sparsity and KV-Cache Sparsity Cross",
+    # §3.2: neither branch discards state): attention reads the retained KV
+    # buffer (kept positions of a selection, then every decoded token), the
+    # units are head-sparse per step, and a unit's missing rows are recomputed
+    # into the full cache and into their retained slots before it is read.
+    # Reference: for each step and selected unit, the oracle's attention over
+    # the kept positions plus the decoded tokens, every token's k, v from its
+    # own input (oracle.token_kv), the new token's from this step's input.
+    setup_lib()
+    w = synth.workload("compose", d=512, h=16, h_kv=4, F=64, obs_window=16)
+    n0, T, keep = 120, 8, 0.25
+    rng = np.random.default_rng(7)
+    W = synth.layer_weights(w, 0, seed=9, full_bias=True)
+    n_max = n0 + T + 4
+    K, V = synth.kv_cache(w, 0, n_max, B=1, seed=9)
+    q_obs = synth.obs_queries(w, 0, seed=9)
+    ys = [synth.hidden(w, B=1, seed=700 + t) for t in range(T)]
+    sels = [sorted(rng.choice(w.h_kv, 2, replace=False).tolist()) for _ in range(T)]
+    b = oracle.kv_budget(n0, keep)
+    b_max = b + T + 8
+    D = dv.dims(w.d, w.h, w.h_kv, w.dh, w.F, w.r, n_max)
+    ws_sel = dv.workspace(D, 1, dv.DV_KV_RESELECT)
+    ws = dv.workspace(D, 1)
+    Kd, Vd = K.cuda(), V.cuda()
+    Kr = torch.zeros(w.h_kv, b_max, w.dh, dtype=torch.float16, device="cuda")
+    Vr = torch.zeros_like(Kr)
+    kp = torch.zeros(w.h_kv, b_max, dtype=torch.int32, device="cuda")
+    kc = torch.zeros(w.h_kv, dtype=torch.int32, device="cuda")
+    y_side = torch.zeros(1, n_max, w.d, dtype=torch.float16, device="cuda")
+    miss = torch.zeros(1, n_max, 1, dtype=torch.int32, device="cuda")
+    kv = dv.kv_cache(Kd, Vd, y_side=y_side, kv_missing=miss, Kr=Kr, Vr=Vr, kept_pos=kp,
+                     kept_count=kc, b_max=b_max)
+    H = torch.zeros(w.h, w.dh, device="cuda")
+    dv.kv_select_attn(torch.zeros(w.h, w.dh, device="cuda"), D, kv, n0, H, ws_sel,
+                      q_obs=q_obs.cuda(), obs_window=w.obs_window, kv_keep=keep,
+                      flags=dv.DV_KV_RESELECT)
+    torch.cuda.synchronize()
+    counts0 = kc.cpu().numpy().copy()
+    kept0 = [kp[u, : counts0[u]].cpu().numpy().copy() for u in range(w.h_kv)]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Wd = to_dev(W)
+    outs = []
+    flags = dv.DV_NO_RESIDUAL | dv.DV_KV_FILL | dv.DV_KV_RETAINED | dv.DV_KV_ADVANCE
+    for t in range(T):
+        out = torch.empty(1, w.d, dtype=torch.float16, device="cuda")
+        sd = torch.tensor(sels[t], dtype=torch.int32, device="cuda")
+        dv.sparse_attn(ys[t].cuda(), D, Wd, sd, len(sels[t]), kv, n0 + t, out, ws, flags=flags,
+                       dev_status=st)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(kc.cpu().numpy(), counts0 + T)
+
+    Wh = host(W)
+    Kc, Vc = np16(K[0]).copy(), np16(V[0]).copy()
+    bo = Wh.get("bo")
+    bo = np.zeros(w.d) if bo is None else bo.astype(np.float64)
+    for t in range(T):
+        n = n0 + t
+        y = np16(ys[t][0])
+        want = bo.copy()
+        for u in sels[t]:
+            pos = np.concatenate([kept0[u], np.arange(n0, n)]).astype(np.int64)
+            Ks = np.zeros((w.h_kv, len(pos) + 1, w.dh), np.float16)
+            Vs = np.zeros_like(Ks)
+            Ks[u, : len(pos)], Vs[u, : len(pos)] = Kc[u, pos], Vc[u, pos]
+            a = oracle.attn_gather(y, Wh, Ks, Vs, len(pos), [u])
+            want += a.delta - bo
+        assert rel_err(npf(outs[t][0]), want) < TOL, t
+        Kc[:, n], Vc[:, n] = oracle.token_kv(y, Wh, w.h_kv, w.dh)
+    # the retained slots of the decoded tokens hold their own k (for the
+    # positions up to each unit's last selection: later ones are still holes)
+    Krg = Kr.cpu().numpy()
+    for u in range(w.h_kv):
+        last = max([t for t in range(T) if u in sels[t]], default=-1)
+        if last >= 0:
+            slots = counts0[u] + np.arange(last + 1)
+            assert rel_err(Krg[u, slots].astype(float), Kc[u, n0:n0 + last + 1].astype(float)) < TOL, u

@@ -176,3 +176,47 @@ def test_w4_decode_layer_parity(wl, over, B):
             check_sets(selH, ref[w.F:], kH)
         y_ref, _ = ow4.layer(np16(x[b]), Wo, np16(K[b]), np16(V[b]), w.n, selH, selN)
         assert rel_err(npf(y[b]), y_ref.astype(np.float64)) < TOL, b
+
+
+@pytest.mark.parametrize("wl,over,n0,T", [
+    ("tiny", {}, 30, 8),
+    ("opt-6.7b", dict(F=64), 100, 5),                                   # d 4096, 32 units
+    ("compose", dict(d=512, h=8, h_kv=2, F=64), 60, 6),                 # GQA
+])
+def test_w4_multistep_missing_kv_recompute(wl, over, n0, T):
+    # head-sparse decode steps with 4-bit W^K, W^V: the missing k, v of a unit
+    # are recomputed from the kept inputs with the 4-bit rows ("Deja Vu" §4.2
+    # with §5.2's W4A16), against the oracle's W4 attention where every past
+    # token's k, v come from that token's own input
+    setup_lib()
+    w = synth.workload(wl, **over)
+    Wq, Wo = _w4_layer(w, seed=41)
+    rng = np.random.default_rng(n0)
+    n_max = n0 + T + 3
+    K, V = synth.kv_cache(w, 0, n_max, B=1, seed=41)
+    ys = [synth.hidden(w, B=1, seed=800 + t) for t in range(T)]
+    k = max(1, w.h_kv // 2)
+    sels = [sorted(rng.choice(w.h_kv, k, replace=False).tolist()) for _ in range(T)]
+    D = dv.dims(w.d, w.h, w.h_kv, w.dh, w.F, w.r, n_max)
+    ws = dv.workspace(D, 1)
+    Kd, Vd = K.cuda(), V.cuda()
+    y_side = torch.zeros(1, n_max, w.d, dtype=torch.float16, device="cuda")
+    miss = torch.zeros(1, n_max, (w.h_kv + 31) // 32, dtype=torch.int32, device="cuda")
+    kv = dv.kv_cache(Kd, Vd, y_side=y_side, kv_missing=miss)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for t in range(T):
+        out = torch.empty(1, w.d, dtype=torch.float16, device="cuda")
+        sd = torch.tensor(sels[t], dtype=torch.int32, device="cuda")
+        dv.sparse_attn(ys[t].cuda(), D, Wq, sd, len(sels[t]), kv, n0 + t, out, ws,
+                       flags=dv.DV_NO_RESIDUAL | dv.DV_KV_FILL | dv.DV_W4, dev_status=st)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    Kc, Vc = np16(K[0]).copy(), np16(V[0]).copy()
+    for t in range(T):
+        y = np16(ys[t][0])
+        delta, _, _ = ow4.attn(y, Wo, Kc, Vc, n0 + t, sels[t])
+        assert rel_err(npf(outs[t][0]), delta) < TOL, t
+        _, kn, vn = ow4.attn(y, Wo, Kc, Vc, n0 + t, range(w.h_kv))   # every unit's k, v
+        Kc[:, n0 + t], Vc[:, n0 + t] = kn, vn
