@@ -76,21 +76,144 @@ __host__ __device__ constexpr bool is_w4(int k) {
 }
 constexpr int kW4StageRows = 8;  // rows per ring stage for 4-bit rows
 constexpr int kW4Ilp = 4;        // 4-bit rows a consumer works on at once
-constexpr int kW4Threads = 992;  // consumer threads at B = 1 (31 warps + the producer)
+constexpr int kW4Threads = 768;  // consumer threads at B = 1 (24 warps + the producer)
 __host__ __device__ inline uint32_t w4_row_bytes(int d) { return (uint32_t)((d / 2 + d / 64 + 15) / 16 * 16); }
 
 // The 8 codes of one 32-bit word as exact floats (q = nibble - 8), in column
 // order: (w >> 4k) & 0x000F000F puts nibbles k and k + 4 into the two halves
 // of a half2 whose bits 0x6400 | n read as 1024 + n; subtracting 1032 leaves
 // n - 8 exactly.
-// The same codes as exact fp16 pairs: h[k] = {q_k, q_{k+4}}.
+// The same codes as exact fp16 pairs: h[k] = {q_k, q_{k+4}}. Two masks per
+// byte pair and one shift per word: w & 0x000F000F | 0x6400.. reads as
+// 1024 + n (minus 1032 gives q), w & 0x00F000F0 | 0x6400.. as 1024 + 16 n
+// (times 1/16 minus 72 gives q, exact in one fused multiply-add), then the
+// same on w >> 8 for codes 2, 6 and 3, 7.
 DV_DEV void w4_decode_h2(uint32_t w, __half2* h) {
   const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  const __half2 s16 = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
+  const __half2 off16 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));
+  const uint32_t w8 = w >> 8;
+  const uint32_t b0 = (w & 0x000F000Fu) | 0x64006400u;
+  const uint32_t b1 = (w & 0x00F000F0u) | 0x64006400u;
+  const uint32_t b2 = (w8 & 0x000F000Fu) | 0x64006400u;
+  const uint32_t b3 = (w8 & 0x00F000F0u) | 0x64006400u;
+  h[0] = __hsub2(*reinterpret_cast<const __half2*>(&b0), off);
+  h[1] = __hfma2(*reinterpret_cast<const __half2*>(&b1), s16, off16);
+  h[2] = __hsub2(*reinterpret_cast<const __half2*>(&b2), off);
+  h[3] = __hfma2(*reinterpret_cast<const __half2*>(&b3), s16, off16);
+}
+
+// The same decode fused with its use, as explicit f16x2 instructions (the
+// bits of the pairs are carried in 32-bit registers): five integer
+// instructions and four f16x2 instructions decode a word.
+// w4_axpy8: h[k] += {q_k, q_{k+4}} * cf.
+DV_DEV void w4_axpy8(uint32_t w, uint32_t cf, uint32_t* h) {
+  asm("{\n\t.reg .b32 t0, t1, t2, t3, w8, c0, c1, c2;\n\t"
+      "mov.b32 c0, 0x64086408;\n\t"
+      "mov.b32 c1, 0x2C002C00;\n\t"
+      "mov.b32 c2, 0xD480D480;\n\t"
+      "lop3.b32 t0, %4, 0x000F000F, 0x64006400, 0xEA;\n\t"
+      "lop3.b32 t1, %4, 0x00F000F0, 0x64006400, 0xEA;\n\t"
+      "shr.u32 w8, %4, 8;\n\t"
+      "lop3.b32 t2, w8, 0x000F000F, 0x64006400, 0xEA;\n\t"
+      "lop3.b32 t3, w8, 0x00F000F0, 0x64006400, 0xEA;\n\t"
+      "sub.rn.f16x2 t0, t0, c0;\n\t"
+      "fma.rn.f16x2 t1, t1, c1, c2;\n\t"
+      "sub.rn.f16x2 t2, t2, c0;\n\t"
+      "fma.rn.f16x2 t3, t3, c1, c2;\n\t"
+      "fma.rn.f16x2 %0, t0, %5, %0;\n\t"
+      "fma.rn.f16x2 %1, t1, %5, %1;\n\t"
+      "fma.rn.f16x2 %2, t2, %5, %2;\n\t"
+      "fma.rn.f16x2 %3, t3, %5, %3;\n\t}"
+      : "+r"(h[0]), "+r"(h[1]), "+r"(h[2]), "+r"(h[3])
+      : "r"(w), "r"(cf));
+}
+
+// w4_dot8: the fp16 pair sum {sum_k q_k z_k, sum_k q_{k+4} z_{k+4}} of a word
+// against z[k] = {z_k, z_{k+4}} (a product, then three fused multiply-adds).
+DV_DEV uint32_t w4_dot8(uint32_t w, const uint32_t* z) {
+  uint32_t r;
+  asm("{\n\t.reg .b32 t0, t1, t2, t3, w8, c0, c1, c2;\n\t"
+      "mov.b32 c0, 0x64086408;\n\t"
+      "mov.b32 c1, 0x2C002C00;\n\t"
+      "mov.b32 c2, 0xD480D480;\n\t"
+      "lop3.b32 t0, %1, 0x000F000F, 0x64006400, 0xEA;\n\t"
+      "lop3.b32 t1, %1, 0x00F000F0, 0x64006400, 0xEA;\n\t"
+      "shr.u32 w8, %1, 8;\n\t"
+      "lop3.b32 t2, w8, 0x000F000F, 0x64006400, 0xEA;\n\t"
+      "lop3.b32 t3, w8, 0x00F000F0, 0x64006400, 0xEA;\n\t"
+      "sub.rn.f16x2 t0, t0, c0;\n\t"
+      "fma.rn.f16x2 t1, t1, c1, c2;\n\t"
+      "sub.rn.f16x2 t2, t2, c0;\n\t"
+      "fma.rn.f16x2 t3, t3, c1, c2;\n\t"
+      "mul.rn.f16x2 %0, t0, %2;\n\t"
+      "fma.rn.f16x2 %0, t1, %3, %0;\n\t"
+      "fma.rn.f16x2 %0, t2, %4, %0;\n\t"
+      "fma.rn.f16x2 %0, t3, %5, %0;\n\t}"
+      : "=r"(r)
+      : "r"(w), "r"(z[0]), "r"(z[1]), "r"(z[2]), "r"(z[3]));
+  return r;
+}
+
+// Both halves of an f16x2 register as floats.
+DV_DEV float2 h2bits_to_f2(uint32_t x) {
+  float lo, hi;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(x));
+  return make_float2(lo, hi);
+}
+
+// Batch-1 launches of 4-bit rows give each consumer thread V consecutive
+// 8-column vectors (tid V .. tid V + V - 1), so its words of a row are one
+// vector load and usually share one group scale; other launches stride the
+// vectors by the thread count (tid + m T).
+template <int KIND, int B, int V>
+DV_DEV int vec_of(int tid, int m, int T) {
+  if constexpr (is_w4(KIND) && B == 1) return tid * V + m;
+  else return tid + m * T;
+}
+
+// This thread's V code words of a staged 4-bit row (vectors v0 .. v0 + V - 1,
+// all inside the row), from their address.
+template <int V>
+DV_DEV void w4_words_at(const uint8_t* src, uint32_t* w) {
+  if constexpr (V == 2) {
+    const uint2 t = *reinterpret_cast<const uint2*>(src);
+    w[0] = t.x; w[1] = t.y;
+  } else if constexpr (V % 4 == 0) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t b = ((w >> (4 * k)) & 0x000F000Fu) | 0x64006400u;
-    h[k] = __hsub2(*reinterpret_cast<const __half2*>(&b), off);
+    for (int i = 0; i < V; i += 4) {
+      const uint4 t = *reinterpret_cast<const uint4*>(src + i * 4);
+      w[i] = t.x; w[i + 1] = t.y; w[i + 2] = t.z; w[i + 3] = t.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < V; ++i) w[i] = *reinterpret_cast<const uint32_t*>(src + i * 4);
   }
+}
+
+template <int V>
+DV_DEV void w4_words(const uint8_t* row, int v0, uint32_t* w) {
+  w4_words_at<V>(row + (size_t)v0 * 4, w);
+}
+
+// Sums of four values over the warp's lanes, four rows at once: after a
+// pairwise exchange at distances 16 and 8 each lane keeps one row, then
+// three shuffles finish it. Returns the full sum of row 2 (lane / 16 % 2) +
+// (lane / 8 % 2), the same in every lane of that group of 8.
+DV_DEV float warp_sum4(const float* a, int lane) {
+  const bool h16 = lane & 16, h8 = lane & 8;
+  float x0 = h16 ? a[2] : a[0], x1 = h16 ? a[3] : a[1];
+  const float s0 = h16 ? a[0] : a[2], s1 = h16 ? a[1] : a[3];
+  x0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+  x1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+  float y = h8 ? x1 : x0;
+  y += __shfl_xor_sync(0xffffffffu, h8 ? x0 : x1, 8);
+  y += __shfl_xor_sync(0xffffffffu, y, 4);
+  y += __shfl_xor_sync(0xffffffffu, y, 2);
+  y += __shfl_xor_sync(0xffffffffu, y, 1);
+  return y;
 }
 
 DV_DEV void w4_decode(uint32_t w, float* f) {
@@ -245,7 +368,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
                     const bool has_dot, const bool has_axpy, const bool skip);
 
 template <int KIND, int B, int V>
-__global__ void __launch_bounds__((is_w4(KIND) && B == 1) ? 1024 : (B == 1 ? 544 : 416), 1)
+__global__ void __launch_bounds__((is_w4(KIND) && B == 1) ? kW4Threads + 32 : (B == 1 ? 544 : 416), 1)
     k_stream(const StreamParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const StreamGeom& g = p.g;
@@ -428,7 +551,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
       s1[b] = 0.f;
 #pragma unroll
       for (int m = 0; m < V; ++m) {
-        const int v = tid + m * T;
+        const int v = vec_of<KIND, B, V>(tid, m, T);
 #pragma unroll
         for (int e = 0; e < 8; ++e) z[b][m][e] = 0.f;
         if (kRaw) xraw[kRaw ? b : 0][kRaw ? m : 0] = make_uint4(0, 0, 0, 0);
@@ -461,7 +584,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         float s2 = 0.f;
 #pragma unroll
         for (int m = 0; m < V; ++m) {
-          const int v = tid + m * T;
+          const int v = vec_of<KIND, B, V>(tid, m, T);
           if (v < nvec) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -485,7 +608,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         const float mu = mean_inv[b * 2], inv = mean_inv[b * 2 + 1];
 #pragma unroll
         for (int m = 0; m < V; ++m) {
-          const int v = tid + m * T;
+          const int v = vec_of<KIND, B, V>(tid, m, T);
           if (v < nvec) {
             float gg[8], bb[8];
             if (p.ln_g) {
@@ -530,7 +653,76 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         ok = false;
       }
       ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the row sums below shuffle
-      if constexpr (is_w4(KIND)) {
+      if constexpr (is_w4(KIND) && B == 1) {
+        // 4-bit rows, batch 1: four rows at a time, each thread over its V
+        // consecutive words (one vector load, one group scale when V divides
+        // 16); products of the exact codes and the fp16 activations summed
+        // in fp16 pairs over each word, then scaled and accumulated in fp32.
+        if (ok) {
+          const uint8_t* st0 = smem + (size_t)s * g.stage_bytes;
+          const int v0 = tid * V;
+          const bool act = v0 < nvec;
+          if (16 % V == 0 && cnt == kW4StageRows && T * V == nvec) {
+            // a full stage and every thread on whole words: no per-row tests
+            const uint8_t* wp = st0 + (size_t)v0 * 4;
+            const uint16_t* sp = reinterpret_cast<const uint16_t*>(st0 + p.d / 2) + (v0 >> 4);
+            const int rb = (int)g.row_bytes;
+#pragma unroll
+            for (int c0 = 0; c0 < kW4StageRows; c0 += 4) {
+              float a[4];
+#pragma unroll
+              for (int r = 0; r < 4; ++r) {
+                uint32_t wd[V];
+                w4_words_at<V>(wp + (c0 + r) * rb, wd);
+                const float sc = h2f(sp[(c0 + r) * (rb >> 1)]);
+                float t = 0.f;
+#pragma unroll
+                for (int m = 0; m < V; ++m) {
+                  const float2 hf =
+                      h2bits_to_f2(w4_dot8(wd[m], reinterpret_cast<const uint32_t*>(zh[0][m])));
+                  t += hf.x + hf.y;
+                }
+                a[r] = t * sc;
+              }
+              const float sum = warp_sum4(a, lane);
+              const int rr = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+              if ((lane & 7) == 0) red[(q0 + c0 + rr) * nwc + warp] = sum;
+            }
+          } else
+          for (int c0 = 0; c0 < cnt; c0 += 4) {
+            float a[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              a[r] = 0.f;
+              if (c0 + r < cnt && act) {
+                const uint8_t* row = st0 + (size_t)(c0 + r) * g.row_bytes;
+                const uint16_t* scl = reinterpret_cast<const uint16_t*>(row + p.d / 2);
+                uint32_t wd[V];
+                w4_words<V>(row, v0, wd);
+                float t = 0.f;
+#pragma unroll
+                for (int m = 0; m < V; ++m) {
+                  if (16 % V != 0 && v0 + m >= nvec) break;
+                  const float2 hf =
+                      h2bits_to_f2(w4_dot8(wd[m], reinterpret_cast<const uint32_t*>(zh[0][m])));
+                  if constexpr (16 % V == 0) {
+                    t += hf.x + hf.y;
+                  } else {
+                    t = fmaf(h2f(scl[(v0 + m) >> 4]), hf.x + hf.y, t);
+                  }
+                }
+                a[r] = (16 % V == 0) ? t * h2f(scl[v0 >> 4]) : t;
+              }
+            }
+            const float sum = warp_sum4(a, lane);
+            const int rr = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+            if ((lane & 7) == 0 && c0 + rr < cnt) red[(q0 + c0 + rr) * nwc + warp] = sum;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        continue;
+      } else if constexpr (is_w4(KIND)) {
         // 4-bit rows: decode straight from the stage, release it afterwards
         if (ok) {
           const uint8_t* st0 = smem + (size_t)s * g.stage_bytes;
@@ -546,7 +738,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
               for (int b = 0; b < B; ++b) acc[r][b] = 0.f;
 #pragma unroll
             for (int m = 0; m < V; ++m) {
-              const int v = tid + m * T;
+              const int v = vec_of<KIND, B, V>(tid, m, T);
               if (v >= nvec) continue;
 #pragma unroll
               for (int r = 0; r < kW4Ilp; ++r) {
@@ -592,7 +784,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         for (int c = 0; c < RM; ++c)
 #pragma unroll
           for (int m = 0; m < V; ++m) {
-            const int v = tid + m * T;
+            const int v = vec_of<KIND, B, V>(tid, m, T);
             wv[c][m] = (c < cnt && v < nvec) ? stage_vec<KIND>(st0 + (size_t)c * g.row_bytes, v, p.d)
                                              : make_uint4(0, 0, 0, 0);
           }
@@ -798,7 +990,64 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         ok = false;
       }
       ok = __all_sync(0xffffffffu, ok);
-      if constexpr (is_w4(KIND)) {
+      if constexpr (is_w4(KIND) && B == 1) {
+        // 4-bit rows, batch 1: the thread's V consecutive words of each row
+        // (one vector load, one group scale when V divides 16), coefficient
+        // a_j s rounded to fp16, the stage's rows summed in fp16 pairs, then
+        // added to the fp32 accumulators once per stage.
+        if (ok) {
+          const uint8_t* st0 = smem + (size_t)s * g.stage_bytes;
+          const int v0 = tid * V;
+          if (v0 < nvec) {
+            uint32_t h[V][4];
+#pragma unroll
+            for (int m = 0; m < V; ++m)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) h[m][k] = 0u;  // +0.0 in both halves
+            if (16 % V == 0 && cnt == kW4StageRows && T * V == nvec) {
+              // a full stage and every thread on whole words: no per-row tests
+              const uint8_t* wp = st0 + (size_t)v0 * 4;
+              const uint16_t* sp = reinterpret_cast<const uint16_t*>(st0 + p.d / 2) + (v0 >> 4);
+              const int rb = (int)g.row_bytes;
+#pragma unroll
+              for (int c = 0; c < kW4StageRows; ++c) {
+                const float a = coef[skip ? list[q0 + c] : (q0 + c)];
+                uint32_t wd[V];
+                w4_words_at<V>(wp + c * rb, wd);
+                const __half2 cf = __float2half2_rn(a * h2f(sp[c * (rb >> 1)]));
+#pragma unroll
+                for (int m = 0; m < V; ++m)
+                  w4_axpy8(wd[m], *reinterpret_cast<const uint32_t*>(&cf), h[m]);
+              }
+            } else
+            for (int c = 0; c < cnt; ++c) {
+              const uint8_t* row = st0 + (size_t)c * g.row_bytes;
+              const uint16_t* scl = reinterpret_cast<const uint16_t*>(row + p.d / 2);
+              const float a = coef[skip ? list[q0 + c] : (q0 + c)];
+              uint32_t wd[V];
+              w4_words<V>(row, v0, wd);
+              __half2 cf = __float2half2_rn(a * h2f(scl[v0 >> 4]));
+#pragma unroll
+              for (int m = 0; m < V; ++m) {
+                if (16 % V != 0 && v0 + m >= nvec) break;
+                if (16 % V != 0 && m > 0) cf = __float2half2_rn(a * h2f(scl[(v0 + m) >> 4]));
+                w4_axpy8(wd[m], *reinterpret_cast<const uint32_t*>(&cf), h[m]);
+              }
+            }
+#pragma unroll
+            for (int m = 0; m < V; ++m)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float2 f = h2bits_to_f2(h[m][k]);
+                acc[0][m][k] += f.x;
+                acc[0][m][k + 4] += f.y;
+              }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        continue;
+      } else if constexpr (is_w4(KIND)) {
         if (ok) {
           const uint8_t* st0 = smem + (size_t)s * g.stage_bytes;
           // The stage's rows (at most kW4StageRows) are summed in fp16 pairs,
@@ -806,7 +1055,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
           // fp32 accumulators once per stage.
 #pragma unroll
           for (int m = 0; m < V; ++m) {
-            const int v = tid + m * T;
+            const int v = vec_of<KIND, B, V>(tid, m, T);
             if (v >= nvec) continue;
             __half2 h[B][4];
 #pragma unroll
@@ -847,7 +1096,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
         for (int c = 0; c < RM; ++c)
 #pragma unroll
           for (int m = 0; m < V; ++m) {
-            const int v = tid + m * T;
+            const int v = vec_of<KIND, B, V>(tid, m, T);
             wv[c][m] = (c < cnt && v < nvec) ? stage_vec<KIND>(st0 + (size_t)c * g.row_bytes, v, p.d)
                                              : make_uint4(0, 0, 0, 0);
           }
@@ -892,7 +1141,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
       float* dst = p.part + ((size_t)blockIdx.x * p.B + b) * p.d;
 #pragma unroll
       for (int m = 0; m < V; ++m) {
-        const int v = tid + m * T;
+        const int v = vec_of<KIND, B, V>(tid, m, T);
         if (v < nvec) {
           float4* o = reinterpret_cast<float4*>(dst + v * 8);
           o[0] = make_float4(acc[b][m][0], acc[b][m][1], acc[b][m][2], acc[b][m][3]);
@@ -1050,7 +1299,7 @@ int g_stage_target = 48 * 1024;  // bytes per ring stage (rows are grouped up to
 
 static bool make_geom(StreamGeom& g, int d, int B, int ring_budget, int CH, bool w4 = false) {
   const int nvec = d / 8;
-  // 4-bit rows cost more instructions per byte: up to 31 consumer warps at B = 1
+  // 4-bit rows cost more instructions per byte: up to 24 consumer warps at B = 1
   const int tmax = (w4 && B == 1) ? kW4Threads : (B == 1) ? 512 : 384;
   const int V = pick_V(nvec, tmax);
   g.T = ((nvec + V - 1) / V + 31) / 32 * 32;
@@ -1058,8 +1307,8 @@ static bool make_geom(StreamGeom& g, int d, int B, int ring_budget, int CH, bool
   g.row_bytes = w4 ? w4_row_bytes(d) : (uint32_t)d * 2;
   // 4-bit rows are read from the stage in place (no register copy), so a
   // stage can hold more of them
-  g.R = std::min(w4 ? kW4StageRows : rows_max(V == 7 ? 8 : V),
-                 std::max(1, (int)(g_stage_target / g.row_bytes)));
+  g.R = w4 ? std::min(kW4StageRows, std::max(1, ring_budget / (2 * (int)g.row_bytes)))
+            : std::min(rows_max(V == 7 ? 8 : V), std::max(1, (int)(g_stage_target / g.row_bytes)));
   g.stage_bytes = g.R * g.row_bytes;
   g.NS = std::min(16, ring_budget / (int)g.stage_bytes);
   if (g.NS < 2) g.NS = 2;
