@@ -167,6 +167,12 @@ __global__ void __launch_bounds__(kUThreads, 1)
   const int ksplit = PHASE == 1 ? p.ksplit1 : p.ksplit2;
   const int JS = (kk + 63) / 64;   // 64-row stages of the union (fc2)
   const int nunits = ntile * ksplit;
+  // fc1 numbers a row tile's K ranges consecutively (the CTAs of one tile run
+  // together and the last of them sums the ranges); fc2 numbers the column
+  // tiles of one union-row range consecutively, so that CTAs running at the
+  // same time read neighbouring 256-byte pieces of the same weight rows.
+  auto unit_tile = [&](int u) { return PHASE == 1 ? u / ksplit : u % ntile; };
+  auto unit_part = [&](int u) { return PHASE == 1 ? u % ksplit : u / ntile; };
   auto stage_range = [&](int part, int& s0, int& s1) {
     const int tot = PHASE == 1 ? KB : JS;
     s0 = (int)((long long)tot * part / ksplit);
@@ -191,8 +197,8 @@ __global__ void __launch_bounds__(kUThreads, 1)
       if (!__shfl_sync(0xffffffffu, go, 0)) break;
       __syncwarp();  // lane 0's wait orders the producer's reads before these writes
       int s0, s1;
-      stage_range(u % ksplit, s0, s1);
-      const int j0 = PHASE == 1 ? (u / ksplit) * 128 : s0 * 64;
+      stage_range(unit_part(u), s0, s1);
+      const int j0 = PHASE == 1 ? unit_tile(u) * 128 : s0 * 64;
       const int nj = PHASE == 1 ? 128 : (s1 - s0) * 64;
       int* dst = sidx + buf * kUIdxMax;
       for (int i0 = 0; i0 < nj; i0 += 32 * 16) {
@@ -224,7 +230,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
       tma_prefetch_map(&tmX);
     }
     for (int u = blockIdx.x; u < nunits && !*abort_flag; u += gridDim.x, ++n) {
-      const int tile = u / ksplit, part = u % ksplit;
+      const int tile = unit_tile(u), part = unit_part(u);
       int s0, s1;
       stage_range(part, s0, s1);
       const int buf = n & 1;
@@ -282,7 +288,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < nunits && ok && !*abort_flag; u += gridDim.x) {
         int s0, s1;
-        stage_range(u % ksplit, s0, s1);
+        stage_range(unit_part(u), s0, s1);
         if (s1 == s0) continue;
         const int a = nu & 1;
         if (nu >= 2 && !mbar_wait(&acce[a], ((nu >> 1) & 1) ^ 1)) {
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(kUThreads, 1)
     int nu = 0;
     bool dead = false;
     for (int u = blockIdx.x; u < nunits; u += gridDim.x) {
-      const int tile = u / ksplit, part = u % ksplit;
+      const int tile = unit_tile(u), part = unit_part(u);
       int s0, s1;
       stage_range(part, s0, s1);
       float v[BP];
@@ -400,33 +406,52 @@ __global__ void __launch_bounds__(kUThreads, 1)
   }
 }
 
-// Z[b] = fp16(LN2(x[b])): one CTA per sequence, two passes in fp32.
-__global__ void __launch_bounds__(256) k_union_ln(const uint16_t* __restrict__ x, int d,
-                                                  const uint16_t* __restrict__ g,
-                                                  const uint16_t* __restrict__ bb, float eps,
-                                                  uint16_t* __restrict__ Z) {
-  __shared__ float red[8];
+// Z[b] = fp16(LN2(x[b])): one CTA per sequence, two passes in fp32 over
+// 8-column vectors (d is a multiple of 64). CTA 0 also clears the fc1
+// tile counters (the fc1 launch that follows counts on them).
+constexpr int kULnThreads = 512;
+
+__global__ void __launch_bounds__(kULnThreads) k_union_ln(const uint16_t* __restrict__ x, int d,
+                                                         const uint16_t* __restrict__ g,
+                                                         const uint16_t* __restrict__ bb,
+                                                         float eps, uint16_t* __restrict__ Z,
+                                                         int* __restrict__ cnt1, int ncnt) {
+  __shared__ float red[kULnThreads / 32];
   __shared__ float stat[2];
   pdl_wait();
   if (threadIdx.x == 0) pdl_launch_dependents();
   const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int nw = kULnThreads / 32;
+  if (b == 0)
+    for (int i = threadIdx.x; i < ncnt; i += kULnThreads) cnt1[i] = 0;
   const uint16_t* xr = x + (size_t)b * d;
+  const int nv = d / 8;
   float s = 0.f;
-  for (int i = threadIdx.x; i < d; i += 256) s += h2f(xr[i]);
+  for (int v = threadIdx.x; v < nv; v += kULnThreads) {
+    float f[8];
+    h8_to_f8(*reinterpret_cast<const uint4*>(xr + v * 8), f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s += f[e];
+  }
   s = warp_sum(s);
   if (lane == 0) red[warp] = s;
   __syncthreads();
   if (threadIdx.x == 0) {
     float t = 0.f;
-    for (int w = 0; w < 8; ++w) t += red[w];
+    for (int w = 0; w < nw; ++w) t += red[w];
     stat[0] = t / d;
   }
   __syncthreads();
   const float mu = stat[0];
   float q = 0.f;
-  for (int i = threadIdx.x; i < d; i += 256) {
-    const float c = h2f(xr[i]) - mu;
-    q = fmaf(c, c, q);
+  for (int v = threadIdx.x; v < nv; v += kULnThreads) {
+    float f[8];
+    h8_to_f8(*reinterpret_cast<const uint4*>(xr + v * 8), f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float c = f[e] - mu;
+      q = fmaf(c, c, q);
+    }
   }
   q = warp_sum(q);
   __syncthreads();
@@ -434,15 +459,78 @@ __global__ void __launch_bounds__(256) k_union_ln(const uint16_t* __restrict__ x
   __syncthreads();
   if (threadIdx.x == 0) {
     float t = 0.f;
-    for (int w = 0; w < 8; ++w) t += red[w];
+    for (int w = 0; w < nw; ++w) t += red[w];
     stat[1] = 1.0f / sqrtf(t / d + eps);
   }
   __syncthreads();
   const float inv = stat[1];
-  for (int i = threadIdx.x; i < d; i += 256) {
-    const float gg = g ? h2f(g[i]) : 1.f, be = bb ? h2f(bb[i]) : 0.f;
-    Z[(size_t)b * d + i] = f2h((h2f(xr[i]) - mu) * inv * gg + be);
+  for (int v = threadIdx.x; v < nv; v += kULnThreads) {
+    float f[8], gg[8], be[8];
+    h8_to_f8(*reinterpret_cast<const uint4*>(xr + v * 8), f);
+    if (g) {
+      h8_to_f8(*reinterpret_cast<const uint4*>(g + v * 8), gg);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) gg[e] = 1.f;
+    }
+    if (bb) {
+      h8_to_f8(*reinterpret_cast<const uint4*>(bb + v * 8), be);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) be[e] = 0.f;
+    }
+    uint16_t o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = f2h((f[e] - mu) * inv * gg[e] + be[e]);
+    uint4 pk;
+    pk.x = (uint32_t)o[0] | ((uint32_t)o[1] << 16);
+    pk.y = (uint32_t)o[2] | ((uint32_t)o[3] << 16);
+    pk.z = (uint32_t)o[4] | ((uint32_t)o[5] << 16);
+    pk.w = (uint32_t)o[6] | ((uint32_t)o[7] << 16);
+    *reinterpret_cast<uint4*>(Z + (size_t)b * d + v * 8) = pk;
   }
+}
+
+// out[b] = fp16(x[b] + (sum_g part2[g][b] + b2)), the fc2 union-row ranges
+// summed in range order: one thread per (sequence, 4 columns), eight
+// partials' loads in flight.
+__global__ void __launch_bounds__(256) k_union_reduce(const float* __restrict__ part, int G, int B,
+                                                     int d, const uint16_t* __restrict__ x,
+                                                     const uint16_t* __restrict__ bias,
+                                                     uint16_t* __restrict__ out) {
+  pdl_wait();
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  const int n4 = d / 4;
+  const long long i = (long long)blockIdx.x * 256 + threadIdx.x;
+  if (i >= (long long)B * n4) return;
+  const int b = (int)(i / n4), c4 = (int)(i % n4);
+  const size_t stride = (size_t)B * d;
+  const float* src = part + (size_t)b * d + c4 * 4;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  int g0 = 0;
+  for (; g0 + 8 <= G; g0 += 8) {
+    float4 t[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t[j] = __ldcg(reinterpret_cast<const float4*>(src + (g0 + j) * stride));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) { s.x += t[j].x; s.y += t[j].y; s.z += t[j].z; s.w += t[j].w; }
+  }
+  for (; g0 < G; ++g0) {
+    const float4 t = __ldcg(reinterpret_cast<const float4*>(src + g0 * stride));
+    s.x += t.x; s.y += t.y; s.z += t.z; s.w += t.w;
+  }
+  const float r[4] = {s.x, s.y, s.z, s.w};
+  const uint16_t* xr = x ? x + (size_t)b * d + c4 * 4 : nullptr;
+  uint16_t o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float bv = bias ? h2f(bias[c4 * 4 + e]) : 0.f;
+    o[e] = f2h((xr ? h2f(xr[e]) : 0.f) + (r[e] + bv));
+  }
+  uint2 pk;
+  pk.x = (uint32_t)o[0] | ((uint32_t)o[1] << 16);
+  pk.y = (uint32_t)o[2] | ((uint32_t)o[3] << 16);
+  *reinterpret_cast<uint2*>(out + (size_t)b * d + c4 * 4) = pk;
 }
 
 // Host-side plan of one call (shared by the workspace size and the launch).
@@ -528,9 +616,8 @@ int launch_union_mlp_tc(const uint16_t* x, int B, int d, int F, const uint16_t* 
       cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
           cudaSuccess)
     return DV_ERR_LAUNCH;
-  if (cudaMemsetAsync(p.cnt1, 0, (size_t)P.ntile1 * 4, s) != cudaSuccess) return DV_ERR_LAUNCH;
   note_launch(DV_TAG_MLP, 0, s);
-  k_union_ln<<<B, 256, 0, s>>>(x, d, ln_g, ln_b, eps, Z);
+  k_union_ln<<<B, kULnThreads, 0, s>>>(x, d, ln_g, ln_b, eps, Z, p.cnt1, P.ntile1);
   note_launch(DV_TAG_MLP, 1, s);
   if (cudaGetLastError() != cudaSuccess) return DV_ERR_LAUNCH;
   const int grid = sm_count();
@@ -550,7 +637,19 @@ int launch_union_mlp_tc(const uint16_t* x, int B, int d, int F, const uint16_t* 
     note_launch(DV_TAG_MLP, 1, s);
     if (e != cudaSuccess) return DV_ERR_LAUNCH;
   }
-  return reduce_launch(p.part2, P.ksplit2, B, d, resid ? x : nullptr, b2, out, s);
+  {
+    const float* part = p.part2;
+    int G = P.ksplit2, Bv = B, dv_ = d;
+    const uint16_t* xres = resid ? x : nullptr;
+    void* args[] = {&part, &G, &Bv, &dv_, &xres, &b2, &out};
+    const long long n = (long long)B * (d / 4);
+    note_launch(DV_TAG_REDUCE, 0, s);
+    const cudaError_t e = launch_k((const void*)k_union_reduce, dim3((unsigned)((n + 255) / 256)),
+                                   dim3(256), 0, s, args, true);
+    note_launch(DV_TAG_REDUCE, 1, s);
+    if (e != cudaSuccess) return DV_ERR_LAUNCH;
+  }
+  return DV_OK;
 }
 
 }  // namespace dv
