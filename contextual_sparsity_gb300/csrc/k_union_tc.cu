@@ -18,13 +18,16 @@
 //        applies ReLU and writes H (fp16) -- deterministic.
 //   fc2: D[128 output columns][Bp] += fc2T[U rows][128 columns]^T * H[Bp][rows]^T.
 //        A is MN-major here (an fc2T row is contiguous along the output
-//        columns): each gathered union row lands as a 128-byte row of two
-//        64-column blocks. Work units are (column tile, union-row range);
-//        each writes an fp32 partial [range][B][d], summed in range order.
+//        columns): each gathered union row lands as 128-byte rows of
+//        64-column blocks. Work units are (256-column tile, union-row range),
+//        two M = 128 tiles that read 512 contiguous bytes of every row; each
+//        writes an fp32 partial [range][B][d], summed in range order.
 // Bp = max(B, 16) (the instruction shape with M = 128 takes N in steps of
 // 16; rows B..Bp-1 of Z and H feed only columns of D that are never read).
-// One producer warp issues the copies (one gather4 per lane), one thread
+// Eight producer warps issue the copies (one gather4 per lane), one thread
 // issues tcgen05.mma, four warps read the accumulators back (tcgen05.ld).
+#include <algorithm>
+
 #include "dv_internal.h"
 #include "dv_tc.cuh"
 #include "k_union_tc.h"
@@ -33,7 +36,12 @@ namespace dv {
 
 namespace {
 
-constexpr int kUStages = 8;
+// Ring stages: fc1 stages are 128 rows x 64 columns (16 KB); fc2 stages are
+// 64 union rows x 256 output columns (32 KB), so that one unit reads 512
+// contiguous bytes of each fc2^T row.
+template <int PHASE> constexpr int u_stages() { return PHASE == 1 ? 8 : 4; }
+template <int PHASE> constexpr int u_abytes() { return PHASE == 1 ? 128 * 128 : 64 * 512; }
+constexpr int kUCols2 = 256;         // output columns of one fc2 unit (two M = 128 tiles)
 // Warps: 0-3 epilogue, 4..4+kUProd-1 producers (each issues a quarter of a
 // stage's copies: one warp issuing all of them sets the pace), then the MMA
 // issuer and the index warp.
@@ -41,14 +49,15 @@ constexpr int kUProd = 8;
 constexpr int kUMmaWarp = 4 + kUProd;
 constexpr int kUIdxWarp = kUMmaWarp + 1;
 constexpr int kUThreads = (kUIdxWarp + 1) * 32;
-constexpr int kUOpsPerProd = 32 / kUProd;  // gather4 copies per producer warp and stage
+// gather4 copies per producer warp and stage: fc1 32 per stage, fc2 64
+template <int PHASE> constexpr int u_ops_per_prod() { return (PHASE == 1 ? 32 : 64) / kUProd; }
 constexpr int kUIdxMax = 4096;       // union indices one fc2 unit stages in shared memory
 // Each K step of a stage accumulates into its own TMEM accumulator (kUChains
 // independent chains, summed by the epilogue): with N = Bp as small as 16 one
 // instruction's latency, not its work, would otherwise set the pace.
 constexpr int kUChains = 2;
-constexpr uint32_t kUTmemCols = 512; // 2 buffers x kUChains x Bp (<= 64) columns
-constexpr int kABytes = 128 * 128;   // A stage: 128 rows (or 2 x 64 columns) x 128 bytes
+constexpr uint32_t kUTmemCols = 512; // 2 buffers x kUChains x (1 or 2 tiles) x Bp (<= 64) columns
+constexpr int kUMaxStages = 8;
 
 struct UnionTcParams {
   int B, Bp, d, F, k, kpad, ksplit1, ksplit2;
@@ -67,11 +76,12 @@ struct USmem {
   uint32_t a, b, idx, bars, misc, total;
 };
 
+template <int PHASE>
 __host__ __device__ inline USmem u_layout(int Bp) {
   USmem L{};
   L.a = 0;
-  L.b = L.a + kUStages * kABytes;
-  L.idx = L.b + kUStages * Bp * 128;
+  L.b = L.a + u_stages<PHASE>() * u_abytes<PHASE>();
+  L.idx = L.b + u_stages<PHASE>() * Bp * 128;
   L.bars = L.idx + 2 * kUIdxMax * 4;  // two index buffers: the next unit's fill ahead
   L.misc = L.bars + 256;
   L.total = L.misc + 64;
@@ -118,7 +128,11 @@ __global__ void __launch_bounds__(kUThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
-  const USmem L = u_layout(BP);
+  constexpr int kUStages = u_stages<PHASE>();
+  constexpr int kABytes = u_abytes<PHASE>();
+  constexpr int kUOpsPerProd = u_ops_per_prod<PHASE>();
+  constexpr int NT = PHASE == 1 ? 1 : 2;  // M = 128 tiles of one unit
+  const USmem L = u_layout<PHASE>(BP);
   uint8_t* sA = sm + L.a;
   uint8_t* sB = sm + L.b;
   int* sidx = reinterpret_cast<int*>(sm + L.idx);
@@ -161,16 +175,16 @@ __global__ void __launch_bounds__(kUThreads, 1)
   if (tid == 0) pdl_launch_dependents();
 
   const int kk = union_count(p);
-  // units: fc1 (row tile, K range); fc2 (column tile, union-row range)
+  // units: fc1 (row tile, K range); fc2 (256-column tile, union-row range)
   const int KB = (p.d + 63) / 64;  // 64-column slices of d
-  const int ntile = PHASE == 1 ? (kk + 127) / 128 : (p.d + 127) / 128;
+  const int ntile = PHASE == 1 ? (kk + 127) / 128 : (p.d + kUCols2 - 1) / kUCols2;
   const int ksplit = PHASE == 1 ? p.ksplit1 : p.ksplit2;
   const int JS = (kk + 63) / 64;   // 64-row stages of the union (fc2)
   const int nunits = ntile * ksplit;
   // fc1 numbers a row tile's K ranges consecutively (the CTAs of one tile run
   // together and the last of them sums the ranges); fc2 numbers the column
   // tiles of one union-row range consecutively, so that CTAs running at the
-  // same time read neighbouring 256-byte pieces of the same weight rows.
+  // same time read neighbouring 512-byte pieces of the same weight rows.
   auto unit_tile = [&](int u) { return PHASE == 1 ? u / ksplit : u % ntile; };
   auto unit_part = [&](int u) { return PHASE == 1 ? u % ksplit : u / ntile; };
   auto stage_range = [&](int part, int& s0, int& s1) {
@@ -262,11 +276,12 @@ __global__ void __launch_bounds__(kUThreads, 1)
             const int* r = sidx_u + 4 * o;
             tma_gather4(a + o * 512, &tmW, sI * 64, r[0], r[1], r[2], r[3], &full[s]);
           } else {
-            // union rows (sI - s0)*64 + 4 (o % 16) .. +3, output-column block o / 16
+            // union rows (sI - s0)*64 + 4 (o % 16) .. +3, output-column block
+            // o / 16 (64 columns; four blocks per unit)
             const int mb = o >> 4, r4 = (o & 15) * 4;
             const int* r = sidx_u + (sI - s0) * 64 + r4;
-            tma_gather4(a + mb * 8192 + r4 * 128, &tmW, tile * 128 + mb * 64, r[0], r[1], r[2],
-                        r[3], &full[s]);
+            tma_gather4(a + mb * 8192 + r4 * 128, &tmW, tile * kUCols2 + mb * 64, r[0], r[1],
+                        r[2], r[3], &full[s]);
           }
         }
         if (lane == 0 && pw == 0) tma_load_2d(sB + s * bBytes, &tmX, sI * 64, 0, &full[s]);
@@ -304,14 +319,18 @@ __global__ void __launch_bounds__(kUThreads, 1)
           }
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            // fc1: A K-major (16 columns = 32 bytes per step); fc2: A MN-major
-            // (16 union rows = 2048 bytes per step, column blocks 8 KB apart)
-            const uint64_t ad = PHASE == 1 ? sdesc_k128(a0 + s * kABytes + ks * 32)
-                                           : sdesc_sw128(a0 + s * kABytes + ks * 2048, 8192, 1024);
-            tc_mma_f16(tmem + (a * kUChains + ks % kUChains) * BP, ad,
-                       sdesc_k128(b0 + s * bBytes + ks * 32), idesc, sI > s0 || ks >= kUChains);
-          }
+          for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              // fc1: A K-major (16 columns = 32 bytes per step); fc2: A MN-major
+              // (16 union rows = 2048 bytes per step, column blocks 8 KB apart,
+              // tile t at blocks 2t and 2t + 1)
+              const uint64_t ad =
+                  PHASE == 1 ? sdesc_k128(a0 + s * kABytes + ks * 32)
+                             : sdesc_sw128(a0 + s * kABytes + t * 16384 + ks * 2048, 8192, 1024);
+              tc_mma_f16(tmem + ((a * NT + t) * kUChains + ks % kUChains) * BP, ad,
+                         sdesc_k128(b0 + s * bBytes + ks * 32), idesc, sI > s0 || ks >= kUChains);
+            }
           tc_commit(&empty[s]);
         }
         if (!ok) break;
@@ -330,6 +349,45 @@ __global__ void __launch_bounds__(kUThreads, 1)
       const int tile = unit_tile(u), part = unit_part(u);
       int s0, s1;
       stage_range(part, s0, s1);
+      if constexpr (PHASE == 2) {
+        // partial sums of this union-row range for the unit's 256 output
+        // columns (zeros for an empty range: the reduce adds every range)
+        const bool have = s1 > s0;
+        const int a = nu & 1;
+        if (have && !dead && (*abort_flag || !mbar_wait(&accf[a], (nu >> 1) & 1))) {
+          give_up();
+          dead = true;
+        }
+        if (have && !dead) tc_fence_after();
+#pragma unroll 1
+        for (int t = 0; t < NT; ++t) {
+          float v[BP];
+#pragma unroll
+          for (int b = 0; b < BP; ++b) v[b] = 0.f;
+          if (have && !dead) {
+            tmem_ld_row(tl + (a * NT + t) * kUChains * BP, BP, v);
+#pragma unroll
+            for (int c = 1; c < kUChains; ++c) {
+              float w[BP];
+              tmem_ld_row(tl + ((a * NT + t) * kUChains + c) * BP, BP, w);
+#pragma unroll
+              for (int b = 0; b < BP; ++b) v[b] += w[b];
+            }
+          }
+          const int c = tile * kUCols2 + t * 128 + row;
+          if (c < p.d && !dead)
+#pragma unroll
+            for (int b = 0; b < BP; ++b)
+              if (b < p.B) p.part2[((size_t)part * p.B + b) * p.d + c] = v[b];
+        }
+        if (have && !dead) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acce[a]);
+        }
+        if (have) ++nu;
+        continue;
+      }
       float v[BP];
 #pragma unroll
       for (int b = 0; b < BP; ++b) v[b] = 0.f;
@@ -354,15 +412,6 @@ __global__ void __launch_bounds__(kUThreads, 1)
           if (lane == 0) mbar_arrive(&acce[a]);
         }
         ++nu;
-      }
-      if (PHASE == 2) {
-        // partial sums of this union-row range for 128 output columns
-        const int c = tile * 128 + row;
-        if (c < p.d && !dead)
-#pragma unroll
-          for (int b = 0; b < BP; ++b)
-            if (b < p.B) p.part2[((size_t)part * p.B + b) * p.d + c] = v[b];
-        continue;
       }
       // fc1: partial sums of this K range, or the whole dot product
       const int j = tile * 128 + row;
@@ -548,14 +597,14 @@ UnionPlan union_plan(int B, int d, int k) {
   P.ntile1 = (k + 127) / 128;
   P.kpad = P.ntile1 * 128;
   const int KB = (d + 63) / 64;
-  // about eight fc1 and sixteen fc2 units per SM (balance: the units of a
-  // phase are equal, so a CTA's share differs by at most one), at least four
+  // about eight units per SM in each phase (balance: the units of a phase
+  // are equal, so a CTA's share differs by at most one), at least four
   // K slices per fc1 unit, and a union-row range per fc2 unit that fits its
   // index stage
   P.ksplit1 = std::max(1, std::min((8 * sms + P.ntile1 - 1) / P.ntile1, std::max(1, KB / 4)));
-  const int nct = (d + 127) / 128, JS = (k + 63) / 64;
+  const int nct = (d + kUCols2 - 1) / kUCols2, JS = (k + 63) / 64;
   const int need = (JS * 64 + kUIdxMax - 1) / kUIdxMax;
-  P.ksplit2 = std::max(need, std::min((16 * sms + nct - 1) / nct, JS));
+  P.ksplit2 = std::max(need, std::min((8 * sms + nct - 1) / nct, JS));
   P.ksplit2 = std::max(1, P.ksplit2);
   size_t off = 0;
   P.off_z = off;
@@ -606,7 +655,7 @@ int launch_union_mlp_tc(const uint16_t* x, int B, int d, int F, const uint16_t* 
       !make_tmap_f16_sw128(&tW2, fc2T, d, F, d, 1) ||
       !make_tmap_f16_sw128(&tH, p.H, P.kpad, P.Bp, P.kpad, P.Bp))
     return DV_ERR_UNSUPPORTED;
-  const size_t smem = u_layout(P.Bp).total + 1024;
+  const size_t smem = std::max(u_layout<1>(P.Bp).total, u_layout<2>(P.Bp).total) + 1024;
   const void* k1 = P.Bp == 16 ? (const void*)k_union_mlp_tc<1, 16>
                  : P.Bp == 32 ? (const void*)k_union_mlp_tc<1, 32> : (const void*)k_union_mlp_tc<1, 64>;
   const void* k2 = P.Bp == 16 ? (const void*)k_union_mlp_tc<2, 16>

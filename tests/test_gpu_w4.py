@@ -115,6 +115,11 @@ def _w4_layer(w, seed):
     ("tiny", {}, 64, [1, 3]),
     ("opt-6.7b", dict(F=64), 200, [0, 5, 31]),
     ("compose", dict(d=512, h=8, h_kv=2, F=64), 300, [1]),        # GQA, 4 query heads per unit
+    # batch-1 4-bit launches give each thread V consecutive code words: V = 2
+    # with full stages at d 12288, V = 3 (per-word scales, a partial last
+    # thread) at d 16384
+    ("opt-175b", dict(F=64), 100, [0, 7, 95]),
+    ("opt-6.7b", dict(d=16384, h=8, h_kv=8, F=64), 100, [0, 5]),
 ])
 def test_w4_attention_block_parity(wl, over, n, sel):
     setup_lib()
