@@ -19,7 +19,7 @@ struct Tuning {
   int side_ctas = 0;        // predictor CTAs on the side stream; 0: two per SM
   int main_ring = 160 * 1024;
   int side_ring = 32 * 1024;
-  int attn_ctas = 0;        // split-K CTA target; 0: 4 per SM
+  int attn_ctas = 0;        // split-K CTA target; 0: two per SM
 };
 static Tuning g_tune;
 int* g_count_active = nullptr;

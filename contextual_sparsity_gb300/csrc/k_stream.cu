@@ -40,7 +40,10 @@ __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x
 // Rows per ring stage a consumer holds in registers: at most 8 vectors of 16 B.
 __host__ __device__ constexpr int rows_max(int V) { return V >= 8 ? 1 : 8 / V; }
 
-__host__ __device__ inline void stream_layout(StreamGeom& g) {
+// `dot`: the launch has a dot phase (its per-warp row sums need `red`; a
+// Wo launch has none, and the smaller footprint lets one split-K CTA share
+// the SM with it).
+__host__ __device__ inline void stream_layout(StreamGeom& g, bool dot = true) {
   const int nwc = g.T / 32;
   uint32_t off = g.NS * g.stage_bytes;
   off = align_up(off, 16);
@@ -48,7 +51,7 @@ __host__ __device__ inline void stream_layout(StreamGeom& g) {
   off += (2 * g.NS + 2) * 8;
   off = align_up(off, 16);
   g.off_red = off;
-  off += g.CH * g.B * nwc * 4;
+  if (dot) off += g.CH * g.B * nwc * 4;
   g.off_coef = off;
   off += g.B * g.CH * 4;
   g.off_ln = off;
@@ -1297,7 +1300,8 @@ static int pick_V(int nvec, int tmax) { return (nvec + tmax - 1) / tmax; }
 
 int g_stage_target = 48 * 1024;  // bytes per ring stage (rows are grouped up to this)
 
-static bool make_geom(StreamGeom& g, int d, int B, int ring_budget, int CH, bool w4 = false) {
+static bool make_geom(StreamGeom& g, int d, int B, int ring_budget, int CH, bool w4 = false,
+                      bool dot = true) {
   const int nvec = d / 8;
   // 4-bit rows cost more instructions per byte: up to 24 consumer warps at B = 1
   const int tmax = (w4 && B == 1) ? kW4Threads : (B == 1) ? 512 : 384;
@@ -1313,7 +1317,7 @@ static bool make_geom(StreamGeom& g, int d, int B, int ring_budget, int CH, bool
   g.NS = std::min(16, ring_budget / (int)g.stage_bytes);
   if (g.NS < 2) g.NS = 2;
   g.CH = CH;
-  stream_layout(g);
+  stream_layout(g, dot);
   return g.total <= 227 * 1024;
 }
 
@@ -1346,8 +1350,8 @@ int stream_ctas_max(int CH_rows, long long rows, int target) {
 static int launch_stream(int kind, StreamParams& p, long long rows, int target_ctas,
                          int ring_budget, cudaStream_t stream, int* grid_out, bool pdl) {
   const int Bt = p.B == 1 ? 1 : 4;
-  const int CH = 256;
-  if (!make_geom(p.g, p.d, Bt, ring_budget, CH, is_w4(kind))) return DV_ERR_UNSUPPORTED;
+  const int CH = 256;  // at most this many rows per CTA
+  if (!make_geom(p.g, p.d, Bt, ring_budget, CH, is_w4(kind), !is_wo(kind))) return DV_ERR_UNSUPPORTED;
   const int V = pick_V(p.d / 8, (is_w4(kind) && Bt == 1) ? kW4Threads : (Bt == 1 ? 512 : 384));
   void* fn = nullptr;
   switch (kind) {
