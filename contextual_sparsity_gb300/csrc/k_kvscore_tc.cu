@@ -29,7 +29,7 @@ namespace {
 constexpr int kTcKeys = 128;      // keys per tile
 constexpr int kTcStages = 4;      // K tiles in flight
 constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 fp16
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;  // 4 per TMEM lane quadrant
 constexpr int kThreads = (kEpiWarps + 2) * 32;  // + producer warp + MMA warp
 constexpr uint32_t kTmemCols = 512;
 
@@ -51,8 +51,9 @@ __host__ __device__ inline KvTcSmem kvtc_layout(int KB, int MTQ) {
   L.k = L.q + KB * MTQ * kBoxBytes;
   L.bars = L.k + kTcStages * KB * kBoxBytes;
   L.misc = L.bars + 256;
-  // misc: tmem slot, abort flag, then (pass 1) cst[256], lim[256], red[2][128]
-  L.total = L.misc + 16 + 256 * 4 * 2 + 2 * 128 * 4;
+  // misc: tmem slot, abort flag, then cst[256], lim[256] (pass 0: the second
+  // key half's max and sum per query), red[2][4][128] (pass 1)
+  L.total = L.misc + 16 + 256 * 4 * 2 + 2 * 4 * 128 * 4;
   return L;
 }
 
@@ -83,7 +84,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t0 = (int)((long long)p.tiles * split / p.nsplit);
   const int t1 = (int)((long long)p.tiles * (split + 1) / p.nsplit);
   const int ntiles = t1 - t0;
-  const int epi_warps = PASS == 0 ? 4 * p.MT : kEpiWarps;
+  // pass 0: a warp per (TMEM lane quadrant, query tile, key half of a tile);
+  // pass 1: a warp per (lane quadrant, 64 query columns)
+  const int epi_warps = PASS == 0 ? 8 * p.MT : 4 * (p.NQ / 64);
 
   if (tid == 0) {
     for (int s = 0; s < kTcStages; ++s) {
@@ -178,7 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (PASS == 0) {
     // ---------------- pass 0 epilogue: running max / sum per query --------------
     if (warp < epi_warps) {
-      const int q = warp & 3, mt = warp >> 2;
+      const int hq = warp / (4 * p.MT), rest = warp % (4 * p.MT);
+      const int q = rest & 3, mt = rest >> 2;  // q = warp % 4: this warp's lane quadrant
       const int qi = mt * 128 + q * 32 + lane;
       const int lim = qi < p.NQ ? p.n - p.W + qi % p.W : -1;  // last admitted key
       const float s2 = p.scale2;
@@ -191,27 +195,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const int key0 = (t0 + i) * kTcKeys;
-        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + a * (p.MT * 128) + mt * 128;
-        // the tile's 128 scores of this query, four loads in flight
-        uint32_t r[kTcKeys];
+        const int key0 = (t0 + i) * kTcKeys + hq * (kTcKeys / 2);
+        const uint32_t ta =
+            tmem + ((uint32_t)(q * 32) << 16) + a * (p.MT * 128) + mt * 128 + hq * (kTcKeys / 2);
+        // this query's 64 scores of the tile's key half, both loads in flight
+        uint32_t r[kTcKeys / 2];
 #pragma unroll
-        for (int c = 0; c < kTcKeys / 32; ++c) tmem_ld32_nw(ta + c * 32, r + c * 32);
+        for (int c = 0; c < kTcKeys / 64; ++c) tmem_ld32_nw(ta + c * 32, r + c * 32);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acce[a]);
-        float v[kTcKeys];
+        float v[kTcKeys / 2];
 #pragma unroll
-        for (int j = 0; j < kTcKeys; ++j) v[j] = __uint_as_float(r[j]);
-        if (key0 + kTcKeys - 1 > p.n - p.W) {  // the causal limit cuts this tile for some query
+        for (int j = 0; j < kTcKeys / 2; ++j) v[j] = __uint_as_float(r[j]);
+        if (key0 + kTcKeys / 2 - 1 > p.n - p.W) {  // the causal limit cuts this half for some query
 #pragma unroll
-          for (int j = 0; j < kTcKeys; ++j)
+          for (int j = 0; j < kTcKeys / 2; ++j)
             if (key0 + j > lim) v[j] = -INFINITY;
         }
         float mx = v[0];
 #pragma unroll
-        for (int j = 1; j < kTcKeys; ++j) mx = fmaxf(mx, v[j]);
+        for (int j = 1; j < kTcKeys / 2; ++j) mx = fmaxf(mx, v[j]);
         mx *= s2;  // scale > 0: the max of the scaled scores
         if (mx > m) {
           l *= ex2_approx(m - mx);
@@ -220,17 +225,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (m != -INFINITY) {
           float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-          for (int j = 0; j < kTcKeys; j += 2) {
+          for (int j = 0; j < kTcKeys / 2; j += 2) {
             acc0 += ex2_approx(fmaf(v[j], s2, -m));
             acc1 += ex2_approx(fmaf(v[j + 1], s2, -m));
           }
           l += acc0 + acc1;
         }
       }
-      if (qi < p.NQ) {
+      // the two key halves of each query meet in shared memory
+      if (hq == 1) {
+        cst[qi] = m;
+        reinterpret_cast<float*>(lims)[qi] = l;
+      }
+      consumer_sync(epi_warps * 32);
+      if (hq == 0 && qi < p.NQ) {
+        const float m1 = cst[qi], l1 = reinterpret_cast<const float*>(lims)[qi];
+        const float M = fmaxf(m, m1);
+        float L = 0.f;
+        if (m != -INFINITY) L += l * ex2_approx(m - M);
+        if (m1 != -INFINITY) L += l1 * ex2_approx(m1 - M);
         float* dst = p.stats + (((size_t)u * p.NQ + qi) * p.nsplit + split) * 2;
-        dst[0] = m;
-        dst[1] = l;
+        dst[0] = M;
+        dst[1] = L;
       }
     }
   } else {
@@ -247,10 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       lims[qi] = p.n - p.W + qi % p.W;
     }
     consumer_sync(kEpiWarps * 32);
-    const int q = warp & 3, half = warp >> 2;
-    const int cols = p.NQ / 2;
+    const int q = warp & 3, half = warp >> 2;  // half: which 64 query columns
+    const int cols = 64;
     bool dead = false;
-    for (int i = 0; i < ntiles; ++i) {
+    for (int i = 0; i < ntiles && warp < epi_warps; ++i) {
       const int a = i & 1;
       const int key0 = (t0 + i) * kTcKeys;
       const int key = key0 + q * 32 + lane;
@@ -297,12 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&acce[a]);
       }
-      // the two column halves of a key meet in shared memory (double buffered
-      // by tile parity, so one barrier per tile suffices)
-      float* rb = red + (i & 1) * 128;
-      if (half == 1) rb[q * 32 + lane] = sum;
-      consumer_sync(kEpiWarps * 32);
-      if (half == 0 && !dead && key < p.n) p.pooled[(size_t)u * p.n + key] = sum + rb[q * 32 + lane];
+      // the column parts of a key meet in shared memory (double buffered by
+      // tile parity, so one barrier per tile suffices), summed in part order
+      float* rb = red + (i & 1) * (4 * 128);
+      if (half > 0) rb[half * 128 + q * 32 + lane] = sum;
+      consumer_sync(epi_warps * 32);
+      if (half == 0 && !dead && key < p.n) {
+        float tot = sum;
+        for (int h2 = 1; h2 < epi_warps / 4; ++h2) tot += rb[h2 * 128 + q * 32 + lane];
+        p.pooled[(size_t)u * p.n + key] = tot;
+      }
     }
   }
   __syncthreads();
