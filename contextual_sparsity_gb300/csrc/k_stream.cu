@@ -1350,7 +1350,17 @@ int stream_ctas_max(int CH_rows, long long rows, int target) {
 static int launch_stream(int kind, StreamParams& p, long long rows, int target_ctas,
                          int ring_budget, cudaStream_t stream, int* grid_out, bool pdl) {
   const int Bt = p.B == 1 ? 1 : 4;
-  const int CH = 256;  // at most this many rows per CTA
+  // At most 256 rows per CTA, or more when the CTA target (one per SM) would
+  // otherwise need a second wave of CTAs (a dense or nearly dense MLP) and the
+  // larger per-row arrays still fit in shared memory.
+  int CH = 256;
+  if (target_ctas > 0) {
+    const long long per = (rows + target_ctas - 1) / target_ctas;
+    StreamGeom wide;
+    if (per > CH && per <= 1024 &&
+        make_geom(wide, p.d, Bt, ring_budget, (int)per, is_w4(kind), !is_wo(kind)))
+      CH = (int)per;
+  }
   if (!make_geom(p.g, p.d, Bt, ring_budget, CH, is_w4(kind), !is_wo(kind))) return DV_ERR_UNSUPPORTED;
   const int V = pick_V(p.d / 8, (is_w4(kind) && Bt == 1) ? kW4Threads : (Bt == 1 ? 512 : 384));
   void* fn = nullptr;
