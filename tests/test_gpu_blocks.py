@@ -117,7 +117,10 @@ def _mlp_case(wl, d=None, F=None, seed=0, full_bias=True):
 @pytest.mark.parametrize("wl,d,F,keep", [("tiny", None, None, 0.25), ("tiny", 264, 520, 0.1),
                                          ("opt-6.7b", None, None, 0.1),
                                          ("opt-6.7b", None, None, 1.0),
-                                         ("opt-6.7b", 16384, 512, 0.25)])     # largest d
+                                         ("opt-6.7b", 16384, 512, 0.25),      # largest d
+                                         # 49152 rows per phase: more than 256 per CTA at
+                                         # one CTA per SM
+                                         ("opt-175b", None, None, 1.0)])
 @pytest.mark.parametrize("flags", [0, dv.DV_SKIP_INACTIVE])
 def test_mlp_parity(wl, d, F, keep, flags):
     w, W = _mlp_case(wl, d, F)

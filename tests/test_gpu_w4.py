@@ -53,6 +53,7 @@ def _mlp_case(wl, over, n_sel, B, seed):
     ("opt-6.7b", dict(F=2048), 300, 1, 0),
     ("opt-6.7b", dict(F=2048), 300, 1, dv.DV_SKIP_INACTIVE),
     ("opt-175b", {}, 512, 1, 0),                       # full width 49152, d 12288
+    ("opt-175b", {}, 49152, 1, 0),                     # every row: > 256 rows per CTA
     ("opt-66b", dict(F=4096), 700, 4, 0),              # batch 4 over one (union) set
     ("opt-6.7b", dict(d=16384, h=8, h_kv=8, F=512), 200, 1, 0),   # largest d
 ])
