@@ -26,15 +26,19 @@ namespace dv {
 
 namespace {
 
-constexpr int kTcKeys = 128;      // keys per tile
-constexpr int kTcStages = 4;      // K tiles in flight
+constexpr int kTcKeys = 128;      // keys per pass-1 tile (M = 128 keys)
+constexpr int kTcStages = 4;      // pass-1 K tiles in flight
+// Pass 0 takes 256 keys per tile (N = 256, the instruction width that keeps
+// the tensor pipe at full rate) in two stages of the same total size.
+template <int PASS> constexpr int tc_keys() { return PASS == 0 ? 256 : kTcKeys; }
+template <int PASS> constexpr int tc_stages() { return PASS == 0 ? 2 : kTcStages; }
 constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 fp16
 constexpr int kEpiWarps = 16;  // 4 per TMEM lane quadrant
 constexpr int kThreads = (kEpiWarps + 2) * 32;  // + producer warp + MMA warp
 constexpr uint32_t kTmemCols = 512;
 
 struct KvTcParams {
-  int h_kv, W, n, n_max, NQ, MT, KB, nsplit, tiles;
+  int h_kv, W, n, n_max, NQ, MT, KB, nsplit, tiles, tiles0;  // tiles0: pass-0 (256-key) tiles
   float scale2;
   float* stats;   // [h_kv][NQ][nsplit][2]
   float* pooled;  // [h_kv][n]
@@ -81,8 +85,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int u = blockIdx.y, split = blockIdx.x;
-  const int t0 = (int)((long long)p.tiles * split / p.nsplit);
-  const int t1 = (int)((long long)p.tiles * (split + 1) / p.nsplit);
+  constexpr int KT = tc_keys<PASS>(), NS = tc_stages<PASS>();
+  const int tiles = PASS == 0 ? p.tiles0 : p.tiles;
+  const int t0 = (int)((long long)tiles * split / p.nsplit);
+  const int t1 = (int)((long long)tiles * (split + 1) / p.nsplit);
   const int ntiles = t1 - t0;
   // pass 0: a warp per (TMEM lane quadrant, query tile, key half of a tile);
   // pass 1: a warp per (lane quadrant, 64 query columns)
@@ -96,7 +102,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(qbar, 1);
     for (int a = 0; a < 2; ++a) {
       mbar_init(&accf[a], 1);
-      mbar_init(&acce[a], epi_warps);
+      // pass 0: each accumulator is read by the 8 warps of one query tile
+      mbar_init(&acce[a], PASS == 0 ? 8 : epi_warps);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -124,21 +131,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int mt = 0; mt < MTQ; ++mt)
           tma_load_2d(sQ + (kb * MTQ + mt) * kBoxBytes, &tmQ, kb * 64, u * p.NQ + mt * 128, qbar);
       int i = 0;
+      constexpr int KBLK = KT / 128;  // 128-row boxes per 64-column slice of a tile
       for (; i < ntiles && !*abort_flag; ++i) {
-        const int s = i % kTcStages;
-        if (i >= kTcStages && !mbar_wait(&empty[s], ((i / kTcStages) & 1) ^ 1)) {
+        const int s = i % NS;
+        if (i >= NS && !mbar_wait(&empty[s], ((i / NS) & 1) ^ 1)) {
           give_up();
           break;
         }
-        mbar_arrive_expect_tx(&full[s], p.KB * kBoxBytes);
-        const int row = u * p.n_max + (t0 + i) * kTcKeys;
+        mbar_arrive_expect_tx(&full[s], p.KB * KBLK * kBoxBytes);
+        const int row = u * p.n_max + (t0 + i) * KT;
+        // slice kb of the tile: its KBLK boxes of 128 keys back to back, so
+        // the KT rows form one 128-byte-swizzled operand
         for (int kb = 0; kb < p.KB; ++kb)
-          tma_load_2d(sK + (s * p.KB + kb) * kBoxBytes, &tmK, kb * 64, row, &full[s]);
+          for (int kbk = 0; kbk < KBLK; ++kbk)
+            tma_load_2d(sK + ((s * p.KB + kb) * KBLK + kbk) * kBoxBytes, &tmK, kb * 64,
+                        row + kbk * 128, &full[s]);
       }
       // every issued copy lands before the CTA exits
       if (!mbar_wait(qbar, 0)) flag(p.st, DV_DEV_TIMEOUT);
-      for (int j = (i > kTcStages ? i - kTcStages : 0); j < i; ++j)
-        if (!mbar_wait(&full[j % kTcStages], (j / kTcStages) & 1)) flag(p.st, DV_DEV_TIMEOUT);
+      for (int j = (i > NS ? i - NS : 0); j < i; ++j)
+        if (!mbar_wait(&full[j % NS], (j / NS) & 1)) flag(p.st, DV_DEV_TIMEOUT);
     }
     __syncwarp();
   } else if (warp == kEpiWarps + 1) {
@@ -148,24 +160,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(qbar, 0);
       if (!ok) give_up();
       for (int i = 0; i < ntiles && ok && !*abort_flag; ++i) {
-        const int s = i % kTcStages, a = i & 1;
-        if (!mbar_wait(&full[s], (i / kTcStages) & 1) ||
-            (i >= 2 && !mbar_wait(&acce[a], ((i >> 1) & 1) ^ 1))) {
+        const int s = i % NS, a = i & 1;
+        if (!mbar_wait(&full[s], (i / NS) & 1)) {
+          give_up();
+          break;
+        }
+        if (PASS == 0) {
+          // 256 columns of TMEM per query tile: with two query tiles each has
+          // its own accumulator (buffer mt, used once per key tile), with one
+          // the two buffers alternate between key tiles
+          const uint32_t kst = sk + s * p.KB * 2 * kBoxBytes;
+          const uint32_t idesc = idesc_f16_f32(128, KT);
+          for (int mt = 0; mt < p.MT && ok; ++mt) {
+            const int b = p.MT == 2 ? mt : a;
+            const int use = p.MT == 2 ? i : (i >> 1);  // earlier uses of buffer b
+            if (use >= 1 && !mbar_wait(&acce[b], (use - 1) & 1)) {
+              give_up();
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            for (int kk = 0; kk < p.KB * 4; ++kk) {
+              const int kb = kk >> 2, ko = kk & 3;
+              tc_mma_f16(tmem + b * KT, sdesc_k128(sq + (kb * MTQ + mt) * kBoxBytes + ko * 32),
+                         sdesc_k128(kst + kb * 2 * kBoxBytes + ko * 32), idesc, kk > 0);
+            }
+            tc_commit(&accf[b]);  // this query tile's scores are ready
+          }
+          if (!ok) break;
+          tc_commit(&empty[s]);  // the stage is free once these products are done
+          continue;
+        }
+        if (i >= 2 && !mbar_wait(&acce[a], ((i >> 1) & 1) ^ 1)) {
           give_up();
           break;
         }
         tc_fence_after();
         const uint32_t kst = sk + s * p.KB * kBoxBytes;
-        if (PASS == 0) {
-          const uint32_t idesc = idesc_f16_f32(128, kTcKeys);
-          for (int mt = 0; mt < p.MT; ++mt)
-            for (int kk = 0; kk < p.KB * 4; ++kk) {
-              const int kb = kk >> 2, ko = kk & 3;
-              tc_mma_f16(tmem + a * (p.MT * 128) + mt * 128,
-                         sdesc_k128(sq + (kb * MTQ + mt) * kBoxBytes + ko * 32),
-                         sdesc_k128(kst + kb * kBoxBytes + ko * 32), idesc, kk > 0);
-            }
-        } else {
+        {
           const uint32_t idesc = idesc_f16_f32(128, p.NQ);
           for (int kk = 0; kk < p.KB * 4; ++kk) {
             const int kb = kk >> 2, ko = kk & 3;
@@ -188,48 +220,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float s2 = p.scale2;
       float m = -INFINITY, l = 0.f;
       for (int i = 0; i < ntiles; ++i) {
-        const int a = i & 1;
+        const int b = p.MT == 2 ? mt : (i & 1);     // this query tile's accumulator
+        const int use = p.MT == 2 ? i : (i >> 1);  // earlier uses of buffer b
         if (*abort_flag) break;
-        if (!mbar_wait(&accf[a], (i >> 1) & 1)) {
+        if (!mbar_wait(&accf[b], use & 1)) {
           give_up();
           break;
         }
         tc_fence_after();
-        const int key0 = (t0 + i) * kTcKeys + hq * (kTcKeys / 2);
-        const uint32_t ta =
-            tmem + ((uint32_t)(q * 32) << 16) + a * (p.MT * 128) + mt * 128 + hq * (kTcKeys / 2);
-        // this query's 64 scores of the tile's key half, both loads in flight
-        uint32_t r[kTcKeys / 2];
-#pragma unroll
-        for (int c = 0; c < kTcKeys / 64; ++c) tmem_ld32_nw(ta + c * 32, r + c * 32);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acce[a]);
-        float v[kTcKeys / 2];
-#pragma unroll
-        for (int j = 0; j < kTcKeys / 2; ++j) v[j] = __uint_as_float(r[j]);
-        if (key0 + kTcKeys / 2 - 1 > p.n - p.W) {  // the causal limit cuts this half for some query
-#pragma unroll
-          for (int j = 0; j < kTcKeys / 2; ++j)
-            if (key0 + j > lim) v[j] = -INFINITY;
-        }
-        float mx = v[0];
-#pragma unroll
-        for (int j = 1; j < kTcKeys / 2; ++j) mx = fmaxf(mx, v[j]);
-        mx *= s2;  // scale > 0: the max of the scaled scores
-        if (mx > m) {
-          l *= ex2_approx(m - mx);
-          m = mx;
-        }
-        if (m != -INFINITY) {
-          float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-          for (int j = 0; j < kTcKeys / 2; j += 2) {
-            acc0 += ex2_approx(fmaf(v[j], s2, -m));
-            acc1 += ex2_approx(fmaf(v[j + 1], s2, -m));
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + b * KT + hq * (KT / 2);
+        // this query's 128 scores of the tile's key half, 64 at a time
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[64];
+          tmem_ld32_nw(ta + c * 64, r);
+          tmem_ld32_nw(ta + c * 64 + 32, r + 32);
+          tmem_wait_ld();
+          if (c == 1) {  // the accumulator is read: the next key tile may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[b]);
           }
-          l += acc0 + acc1;
+          const int key0 = (t0 + i) * KT + hq * (KT / 2) + c * 64;
+          float v[64];
+#pragma unroll
+          for (int j = 0; j < 64; ++j) v[j] = __uint_as_float(r[j]);
+          if (key0 + 63 > p.n - p.W) {  // the causal limit cuts these keys for some query
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+              if (key0 + j > lim) v[j] = -INFINITY;
+          }
+          float mx = v[0];
+#pragma unroll
+          for (int j = 1; j < 64; ++j) mx = fmaxf(mx, v[j]);
+          mx *= s2;  // scale > 0: the max of the scaled scores
+          if (mx > m) {
+            l *= ex2_approx(m - mx);
+            m = mx;
+          }
+          if (m != -INFINITY) {
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 64; j += 2) {
+              acc0 += ex2_approx(fmaf(v[j], s2, -m));
+              acc1 += ex2_approx(fmaf(v[j + 1], s2, -m));
+            }
+            l += acc0 + acc1;
+          }
         }
       }
       // the two key halves of each query meet in shared memory
@@ -352,6 +389,7 @@ int launch_kv_scores_tc(const uint16_t* q_obs, const uint16_t* K, int h, int h_k
   p.MT = (NQ + 127) / 128;
   p.KB = dh / 64;
   p.tiles = (n + kTcKeys - 1) / kTcKeys;
+  p.tiles0 = (n + tc_keys<0>() - 1) / tc_keys<0>();
   const int per_head = std::max(1, sm_count() / h_kv);
   p.nsplit = std::max(1, std::min(p.tiles, per_head));
   p.scale2 = scale2;
