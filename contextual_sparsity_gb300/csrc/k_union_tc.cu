@@ -359,26 +359,33 @@ __global__ void __launch_bounds__(kUThreads, 1)
           dead = true;
         }
         if (have && !dead) tc_fence_after();
+        // sequences in pieces of at most 32 columns (BP = 64 would otherwise
+        // hold 2 x 64 accumulators per thread at once)
+        constexpr int PC = BP < 32 ? BP : 32;
 #pragma unroll 1
         for (int t = 0; t < NT; ++t) {
-          float v[BP];
-#pragma unroll
-          for (int b = 0; b < BP; ++b) v[b] = 0.f;
-          if (have && !dead) {
-            tmem_ld_row(tl + (a * NT + t) * kUChains * BP, BP, v);
-#pragma unroll
-            for (int c = 1; c < kUChains; ++c) {
-              float w[BP];
-              tmem_ld_row(tl + ((a * NT + t) * kUChains + c) * BP, BP, w);
-#pragma unroll
-              for (int b = 0; b < BP; ++b) v[b] += w[b];
-            }
-          }
           const int c = tile * kUCols2 + t * 128 + row;
-          if (c < p.d && !dead)
+#pragma unroll 1
+          for (int b0 = 0; b0 < BP; b0 += PC) {
+            float v[PC];
 #pragma unroll
-            for (int b = 0; b < BP; ++b)
-              if (b < p.B) p.part2[((size_t)part * p.B + b) * p.d + c] = v[b];
+            for (int b = 0; b < PC; ++b) v[b] = 0.f;
+            if (have && !dead) {
+              const uint32_t base = tl + (a * NT + t) * kUChains * BP + b0;
+              tmem_ld_row(base, PC, v);
+#pragma unroll
+              for (int ch = 1; ch < kUChains; ++ch) {
+                float w[PC];
+                tmem_ld_row(base + ch * BP, PC, w);
+#pragma unroll
+                for (int b = 0; b < PC; ++b) v[b] += w[b];
+              }
+            }
+            if (c < p.d && !dead)
+#pragma unroll
+              for (int b = 0; b < PC; ++b)
+                if (b0 + b < p.B) p.part2[((size_t)part * p.B + b0 + b) * p.d + c] = v[b];
+          }
         }
         if (have && !dead) {
           tc_fence_before();
