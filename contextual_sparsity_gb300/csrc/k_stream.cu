@@ -82,15 +82,12 @@ constexpr int kW4Ilp = 4;        // 4-bit rows a consumer works on at once
 constexpr int kW4Threads = 768;  // consumer threads at B = 1 (24 warps + the producer)
 __host__ __device__ inline uint32_t w4_row_bytes(int d) { return (uint32_t)((d / 2 + d / 64 + 15) / 16 * 16); }
 
-// The 8 codes of one 32-bit word as exact floats (q = nibble - 8), in column
-// order: (w >> 4k) & 0x000F000F puts nibbles k and k + 4 into the two halves
-// of a half2 whose bits 0x6400 | n read as 1024 + n; subtracting 1032 leaves
-// n - 8 exactly.
-// The same codes as exact fp16 pairs: h[k] = {q_k, q_{k+4}}. Two masks per
-// byte pair and one shift per word: w & 0x000F000F | 0x6400.. reads as
-// 1024 + n (minus 1032 gives q), w & 0x00F000F0 | 0x6400.. as 1024 + 16 n
-// (times 1/16 minus 72 gives q, exact in one fused multiply-add), then the
-// same on w >> 8 for codes 2, 6 and 3, 7.
+// The 8 codes of one 32-bit word (q = nibble - 8) as exact fp16 pairs:
+// h[k] = {q_k, q_{k+4}}. Nibbles k and k + 4 sit 16 bits apart, so one mask
+// puts a pair into the two halves of a half2: w & 0x000F000F | 0x6400.. reads
+// as 1024 + n (minus 1032 gives q), w & 0x00F000F0 | 0x6400.. as 1024 + 16 n
+// (times 1/16 minus 72 gives q, exact in one fused multiply-add); the same on
+// w >> 8 gives codes 2, 6 and 3, 7.
 DV_DEV void w4_decode_h2(uint32_t w, __half2* h) {
   const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
   const __half2 s16 = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
@@ -219,17 +216,6 @@ DV_DEV float warp_sum4(const float* a, int lane) {
   return y;
 }
 
-DV_DEV void w4_decode(uint32_t w, float* f) {
-  const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t h = ((w >> (4 * k)) & 0x000F000Fu) | 0x64006400u;
-    const float2 t = __half22float2(__hsub2(*reinterpret_cast<const __half2*>(&h), off));
-    f[k] = t.x;
-    f[k + 4] = t.y;
-  }
-}
-
 struct StreamParams {
   StreamGeom g;
   int d, B;
@@ -347,19 +333,11 @@ DV_DEV const uint16_t* row_addr(const StreamParams& p, int kind, int phase, int 
   return base + row * d;
 }
 
-// Vector v (8 columns) of a staged row: 16 bytes of fp16, or for 4-bit rows
-// {the 32-bit word of its 8 codes, its group's fp16 scale}.
-template <int KIND>
-DV_DEV uint4 stage_vec(const uint8_t* row, int v, int d) {
-  if constexpr (is_w4(KIND)) {
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(row + v * 4);
-    const uint32_t sc = *reinterpret_cast<const uint16_t*>(row + d / 2 + (v >> 4) * 2);
-    return make_uint4(w, sc, 0u, 0u);
-  } else {
-    return *reinterpret_cast<const uint4*>(row + v * 16);
-  }
+// Vector v (8 columns, 16 bytes of fp16) of a staged row (fp16 kinds; the
+// 4-bit kinds read their words in place).
+DV_DEV uint4 stage_vec(const uint8_t* row, int v) {
+  return *reinterpret_cast<const uint4*>(row + v * 16);
 }
-
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -377,7 +355,6 @@ __global__ void __launch_bounds__((is_w4(KIND) && B == 1) ? kW4Threads + 32 : (B
   const StreamGeom& g = p.g;
   const int T = g.T, nwc = T / 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nvec = p.d >> 3;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + g.off_bar);
   uint64_t* empty = full + g.NS;
@@ -788,7 +765,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
 #pragma unroll
           for (int m = 0; m < V; ++m) {
             const int v = vec_of<KIND, B, V>(tid, m, T);
-            wv[c][m] = (c < cnt && v < nvec) ? stage_vec<KIND>(st0 + (size_t)c * g.row_bytes, v, p.d)
+            wv[c][m] = (c < cnt && v < nvec) ? stage_vec(st0 + (size_t)c * g.row_bytes, v)
                                              : make_uint4(0, 0, 0, 0);
           }
       }
@@ -805,19 +782,6 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
 #pragma unroll
           for (int m = 0; m < V; ++m) {
             float w[8];
-            if constexpr (is_w4(KIND)) {
-              // codes times this group's scale: sum_e z_e q_e, then one FMA by s
-              w4_decode(wv[c][m].x, w);
-              const float sc = h2f((uint16_t)wv[c][m].y);
-#pragma unroll
-              for (int b = 0; b < B; ++b) {
-                float t = 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) t = fmaf(z[b][m][e], w[e], t);
-                acc[b] = fmaf(sc, t, acc[b]);
-              }
-              continue;
-            }
             h8_to_f8(wv[c][m], w);
             if (kRaw && raw) {
 #pragma unroll
@@ -1100,7 +1064,7 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
 #pragma unroll
           for (int m = 0; m < V; ++m) {
             const int v = vec_of<KIND, B, V>(tid, m, T);
-            wv[c][m] = (c < cnt && v < nvec) ? stage_vec<KIND>(st0 + (size_t)c * g.row_bytes, v, p.d)
+            wv[c][m] = (c < cnt && v < nvec) ? stage_vec(st0 + (size_t)c * g.row_bytes, v)
                                              : make_uint4(0, 0, 0, 0);
           }
       }
@@ -1117,17 +1081,6 @@ DV_DEV void consume(const StreamParams& p, uint8_t* smem, uint64_t* full, uint64
 #pragma unroll
           for (int m = 0; m < V; ++m) {
             float w[8];
-            if constexpr (is_w4(KIND)) {
-              w4_decode(wv[c][m].x, w);
-              const float sc = h2f((uint16_t)wv[c][m].y);
-#pragma unroll
-              for (int b = 0; b < B; ++b) {
-                const float ab = a[b] * sc;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[b][m][e] = fmaf(ab, w[e], acc[b][m][e]);
-              }
-              continue;
-            }
             h8_to_f8(wv[c][m], w);
 #pragma unroll
             for (int b = 0; b < B; ++b)
