@@ -8,16 +8,17 @@
 // Per KV head u the NQ = G * W window queries (G query heads x W positions,
 // contiguous rows of q_obs) meet the n cached keys: a dense contraction of
 // NQ x d_h by d_h x n. Two launches over the same grid (KV head, key range):
-//   pass 0  S = Q K^T per 128-key tile (M = 128 queries per instruction,
-//           N = 128 keys, K = d_h), each query's running max and sum of
-//           2^(s - max) over the CTA's key range, written per split;
+//   pass 0  S = Q K^T per 256-key tile (M = 128 queries per instruction,
+//           N = 256 keys, K = d_h; one 256-column accumulator per query
+//           tile), each query's running max and sum of 2^(s - max) over the
+//           CTA's key range, written per split;
 //   pass 1  the splits combined per query (M_q, L_q), then S^T = K Q^T per
-//           tile (M = 128 keys, N = NQ queries) so that each TMEM lane is one
-//           key: pooled[u][key] = sum_q 2^(s - M_q) / L_q over the queries
-//           whose position admits the key, a per-thread sum.
+//           128-key tile (M = 128 keys, N = NQ queries) so that each TMEM
+//           lane is one key: pooled[u][key] = sum_q 2^(s - M_q) / L_q over the
+//           queries whose position admits the key, a per-thread sum.
 // Key tiles and the queries are brought by tiled TMA loads (128-byte
 // swizzle, no multicast) into shared memory; one thread issues tcgen05.mma
-// into double-buffered TMEM accumulators; eight warps read them back with
+// into TMEM accumulators (two buffers); sixteen warps read them back with
 // tcgen05.ld. Scores are in base 2 (scaled by softmax_scale * log2 e).
 #include "dv_internal.h"
 #include "dv_tc.cuh"
